@@ -1,0 +1,133 @@
+/*
+ * register_tiled_matrix_gb300 — dense product C = A.B on one GB300 (sm_103a).
+ *
+ * C ABI of libgemm_gb300.so. Every entry point takes plain pointers and sizes,
+ * returns an int status (gemm_status), never throws, and never allocates
+ * device memory per call.
+ *
+ * The operation. Both entry points compute, for 0 <= i < M and 0 <= j < N,
+ *
+ *     C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j]
+ *
+ * the product that the register-tiling pages build on: one output element
+ * is a row of A against a column of B ("【infra之路】理解 Register Tiling",
+ * section "先看 Shared Memory 版本里，一个线程在做什么"), computed with three
+ * levels of tiling — per-block C tiles over global memory, K-slices staged in
+ * shared memory, per-thread (or per-tensor-core) accumulator tiles
+ * ("寄存器Tiling跨架构解析", section 1.1; "理解 Register Tiling", sections
+ * "Register Tiling 的核心思想" and "关键循环：为什么省了 Shared Memory 读取？").
+ * Tiling only re-associates the sum over k, so results agree with the plain
+ * definition up to floating-point summation order.
+ *
+ * Layout. All matrices are dense and row-major with no padding:
+ *     A is M x K (element (i,k) at A[i*K + k]),
+ *     B is K x N (element (k,j) at B[k*N + j]),
+ *     C is M x N (element (i,j) at C[i*N + j]).
+ * C is fully overwritten (there is no alpha/beta); entries outside M x N are
+ * never written.
+ *
+ * Ownership and memory. A, B and C are device pointers owned by the caller
+ * and must stay valid until the work queued on `stream` has finished. C must
+ * not overlap A or B (overlap is detected for the obvious cases and rejected
+ * with GEMM_ERR_INVALID_ARG).
+ *
+ * Streams. `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ * default stream. Calls are asynchronous: a GEMM_OK return means the work was
+ * queued, not that it finished. The current CUDA device must be the device
+ * that owns the pointers and the stream.
+ *
+ * Degenerate shapes. M == 0 or N == 0: nothing to do, GEMM_OK. K == 0: the
+ * empty sum, C is filled with zeros. Negative sizes: GEMM_ERR_INVALID_ARG.
+ * A null pointer is an error only when the matrix it names is non-empty.
+ *
+ * Thread safety. Entry points may be called from several host threads; the
+ * only library state is a per-device cache (SM count, driver entry point,
+ * kernel attributes) and one device error word per device, both set up on
+ * first use.
+ */
+#ifndef REGISTER_TILED_GEMM_H
+#define REGISTER_TILED_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1, /* negative size, null pointer for a non-empty
+                                  matrix, C overlapping A or B, size too large */
+    GEMM_ERR_ALIGNMENT = -2,   /* gemm_bf16f32 only: K or N not a multiple of 8,
+                                  or A, B, C not 16-byte aligned */
+    GEMM_ERR_LAUNCH = -3,      /* a CUDA runtime call failed (no device, launch
+                                  error, earlier sticky error) */
+    GEMM_ERR_TIMEOUT = -4,     /* reported by gemm_get_device_error: a bounded
+                                  wait inside a kernel gave up */
+    GEMM_ERR_DEVICE = -5       /* the current device is not compute capability
+                                  10.3 (the library holds sm_103a code only) */
+} gemm_status;
+
+/*
+ * gemm_f32 — fp32 inputs, fp32 accumulation, fp32 output, on the SIMT FP32
+ * pipes with a register micro-tile per thread (the register-tiled kernel:
+ * "理解 Register Tiling", sections "Register Tiling 的核心思想" and
+ * "关键循环"; "寄存器Tiling跨架构解析", sections 1.1 and 6.1).
+ *
+ * Any M, N, K >= 0 and any 4-byte-aligned pointers. Each output is a sum of
+ * K fp32 products formed with fused multiply-add in an order fixed by the
+ * tiling; the error against the exact sum is bounded by a small multiple of
+ * K * 2^-24 * sum_k |A[i][k] B[k][j]|.
+ */
+int gemm_f32(int64_t M, int64_t N, int64_t K,
+             const float *A, const float *B, float *C, void *stream);
+
+/*
+ * gemm_bf16f32 — bfloat16 inputs, fp32 accumulation and output, on the
+ * tcgen05 tensor cores: operands staged in shared memory by TMA, the
+ * accumulator tile held in tensor memory (the tensor-core form of the
+ * register tile; "寄存器Tiling跨架构解析", sections 2.1 and 6).
+ *
+ * A and B hold raw bfloat16 bit patterns (uint16_t). Requirements beyond the
+ * common ones: K % 8 == 0 and N % 8 == 0 (each row must start on a 16-byte
+ * boundary for the tensor-memory-access unit), and A, B, C 16-byte aligned;
+ * otherwise GEMM_ERR_ALIGNMENT. M is unrestricted. Ragged M, N and K tiles
+ * are handled by zero-filled loads and masked stores.
+ *
+ * Every wait inside the kernel is bounded (a few seconds); if one gives up
+ * the kernel records GEMM_ERR_TIMEOUT in the device error word and returns
+ * instead of hanging. Read it with gemm_get_device_error.
+ */
+int gemm_bf16f32(int64_t M, int64_t N, int64_t K,
+                 const uint16_t *A, const uint16_t *B, float *C, void *stream);
+
+/*
+ * gemm_get_device_error — synchronises `stream`, then returns and clears the
+ * current device's error word: GEMM_OK, or GEMM_ERR_TIMEOUT if a bounded wait
+ * in any kernel of this library on this device gave up since the last call.
+ * Returns GEMM_ERR_LAUNCH if the synchronisation itself fails.
+ */
+int gemm_get_device_error(void *stream);
+
+/*
+ * gemm_bf16f32_selftest_timeout — failure-detection check for the bounded
+ * waits. Launches the gemm_bf16f32 kernel on the given buffers with its
+ * tensor-memory-access producer muted, so that nothing ever arrives on the
+ * stage barriers, and with every wait limited to `wait_limit_ns`. Each
+ * waiting warp gives up, the kernel frees its tensor memory, records
+ * GEMM_ERR_TIMEOUT in the device error word and returns; the GPU context
+ * stays usable. C is left unspecified. Same argument rules as gemm_bf16f32;
+ * wait_limit_ns must be in [1e6, 1e10].
+ */
+int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K,
+                                  const uint16_t *A, const uint16_t *B, float *C,
+                                  int64_t wait_limit_ns, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gemm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REGISTER_TILED_GEMM_H */

@@ -1,0 +1,152 @@
+"""ctypes binding of libgemm_gb300.so: argument marshalling only.
+
+Every step of the product runs in the library's CUDA kernels; this module
+checks tensor metadata, allocates the output with torch when the caller gives
+none, passes raw device pointers and the current torch stream, and turns a
+non-zero status into an exception. There is no CPU fallback: if the library
+is missing the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import List, Optional
+
+import torch
+
+from . import native_build as _build
+
+STATUS = {
+    0: "GEMM_OK",
+    -1: "GEMM_ERR_INVALID_ARG",
+    -2: "GEMM_ERR_ALIGNMENT",
+    -3: "GEMM_ERR_LAUNCH",
+    -4: "GEMM_ERR_TIMEOUT",
+    -5: "GEMM_ERR_DEVICE",
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the built library (build it first with register_tiled_matrix_gb300.build())."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is not built: call register_tiled_matrix_gb300.build() "
+                "(nvcc, sm_103a) first; there is no fallback implementation")
+        lib = ctypes.CDLL(path)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        for name in ("gemm_f32", "gemm_bf16f32"):
+            f = getattr(lib, name)
+            f.argtypes = [i64, i64, i64, p, p, p, p]
+            f.restype = ctypes.c_int
+        lib.gemm_bf16f32_selftest_timeout.argtypes = [i64, i64, i64, p, p, p, i64, p]
+        lib.gemm_bf16f32_selftest_timeout.restype = ctypes.c_int
+        lib.gemm_get_device_error.argtypes = [p]
+        lib.gemm_get_device_error.restype = ctypes.c_int
+        lib.gemm_status_string.argtypes = [ctypes.c_int]
+        lib.gemm_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def header_symbols() -> List[str]:
+    """Names of the functions declared in include/gemm.h."""
+    path = os.path.join(_build.INCLUDE, "gemm.h")
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_\w+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load_library().gemm_status_string(int(status)).decode()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise GemmError(status, status_string(status))
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _prepare(A: torch.Tensor, B: torch.Tensor, dtype: torch.dtype,
+             out: Optional[torch.Tensor]) -> torch.Tensor:
+    for name, t in (("A", A), ("B", B)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 2-D (row-major) matrix")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {M}x{K}, B is {K2}x{N}")
+    if A.device != B.device:
+        raise ValueError("A and B must be on the same device")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    elif (out.dtype != torch.float32 or out.shape != (M, N) or not out.is_contiguous()
+          or out.device != A.device):
+        raise ValueError("out must be a contiguous float32 M x N tensor on A's device")
+    return out
+
+
+def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B on the SIMT FP32 register-tiled kernel (fp32 in, fp32 out)."""
+    C = _prepare(A, B, torch.float32, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        _check(load_library().gemm_f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                       _stream_handle(stream)))
+    return C
+
+
+def gemm_bf16f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B on the tcgen05 tensor-core kernel (bf16 in, fp32 accumulate and out)."""
+    C = _prepare(A, B, torch.bfloat16, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        _check(load_library().gemm_bf16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                           _stream_handle(stream)))
+    return C
+
+
+def gemm_bf16f32_selftest_timeout(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor,
+                                  wait_limit_ns: int,
+                                  stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Launch the bf16 kernel with its loads muted so every bounded wait runs out."""
+    C = _prepare(A, B, torch.bfloat16, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        _check(load_library().gemm_bf16f32_selftest_timeout(
+            M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), int(wait_limit_ns),
+            _stream_handle(stream)))
+
+
+def get_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise the stream; return and clear the device error word."""
+    return int(load_library().gemm_get_device_error(_stream_handle(stream)))

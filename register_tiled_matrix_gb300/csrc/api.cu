@@ -1,0 +1,267 @@
+// C ABI of libgemm_gb300.so (declared in include/gemm.h).
+//
+// Host-side argument checks run before any CUDA call, so invalid arguments
+// are reported without touching a device. The only library state is a
+// per-device cache (compute capability, SM count) and one device error word
+// per device, written by kernels whose bounded waits give up.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm.h"
+#include "kernels.h"
+
+namespace {
+
+// Device error word: 0, or the status of the first bounded wait that gave up.
+__device__ int g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;  // 4 s per wait
+
+struct DeviceInfo {
+    bool ready = false;
+    int cc = 0;
+    int sms = 0;
+    int *err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+void *g_encode_tiled = nullptr;
+bool g_encode_tried = false;
+
+__global__ void zero_fill_kernel(float *C, int64_t count)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride)
+        C[i] = 0.0f;
+}
+
+// Current device's cached info; GEMM_OK or an error status.
+int current_device(DeviceInfo *out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        void *err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        d.cc = major * 10 + minor;
+        d.sms = sms;
+        d.err = static_cast<int *>(err);
+        d.ready = true;
+    }
+    *out = d;
+    return d.cc == 103 ? GEMM_OK : GEMM_ERR_DEVICE;
+}
+
+void *encode_tiled_fn()
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = fn;
+        else
+            cudaGetLastError();
+    }
+    return g_encode_tiled;
+}
+
+bool overlaps(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes)
+{
+    if (!a || !b || a_bytes <= 0 || b_bytes <= 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + (uintptr_t)b_bytes && b0 < a0 + (uintptr_t)a_bytes;
+}
+
+constexpr int64_t kMaxDim = 0x7fffffff;
+
+// Checks shared by both entry points. Returns GEMM_OK and sets *nothing_to_do
+// when M or N is zero.
+int check_common(int64_t M, int64_t N, int64_t K, const void *A, const void *B, const void *C,
+                 int64_t elem, bool *nothing_to_do)
+{
+    *nothing_to_do = false;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) {
+        *nothing_to_do = true;
+        return GEMM_OK;
+    }
+    if (!C)
+        return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B))
+        return GEMM_ERR_INVALID_ARG;
+    if (M * N > (int64_t)1 << 52 || M * K > (int64_t)1 << 52 || K * N > (int64_t)1 << 52)
+        return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && (overlaps(C, M * N * 4, A, M * K * elem) || overlaps(C, M * N * 4, B, K * N * elem)))
+        return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+int finish(cudaError_t e)
+{
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
+             void *stream, uint64_t wait_limit_ns, int mute_producer)
+{
+    bool nothing = false;
+    int st = check_common(M, N, K, A, B, C, 2, &nothing);
+    if (st != GEMM_OK || nothing)
+        return st;
+    if (K % 8 != 0 || N % 8 != 0)
+        return GEMM_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(C) & 15) != 0 ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15) != 0 ||
+                   (reinterpret_cast<uintptr_t>(B) & 15) != 0)))
+        return GEMM_ERR_ALIGNMENT;
+    DeviceInfo d;
+    st = current_device(&d);
+    if (st != GEMM_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return finish(rtm::launch_zero_fill(C, M * N, s));
+    rtm::TcLaunch L;
+    L.M = (int)M;
+    L.N = (int)N;
+    L.K = (int)K;
+    L.A = A;
+    L.B = B;
+    L.C = C;
+    L.err = d.err;
+    L.wait_limit_ns = wait_limit_ns;
+    L.mute_producer = mute_producer;
+    L.sm_count = d.sms;
+    L.encode_tiled = encode_tiled_fn();
+    if (!L.encode_tiled)
+        return GEMM_ERR_LAUNCH;
+    return finish(rtm::launch_gemm_bf16_tc(L, s));
+}
+
+} // namespace
+
+namespace rtm {
+cudaError_t launch_zero_fill(float *C, int64_t count, cudaStream_t stream)
+{
+    if (count <= 0)
+        return cudaSuccess;
+    int64_t blocks = (count + 255) / 256;
+    if (blocks > 4096)
+        blocks = 4096;
+    zero_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(C, count);
+    return cudaGetLastError();
+}
+} // namespace rtm
+
+extern "C" {
+
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B, float *C,
+             void *stream)
+{
+    bool nothing = false;
+    int st = check_common(M, N, K, A, B, C, 4, &nothing);
+    if (st != GEMM_OK || nothing)
+        return st;
+    if ((reinterpret_cast<uintptr_t>(C) & 3) != 0 ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3) != 0 ||
+                   (reinterpret_cast<uintptr_t>(B) & 3) != 0)))
+        return GEMM_ERR_ALIGNMENT;
+    DeviceInfo d;
+    st = current_device(&d);
+    if (st != GEMM_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return finish(rtm::launch_zero_fill(C, M * N, s));
+    return finish(rtm::launch_sgemm_f32((int)M, (int)N, (int)K, A, B, C, s));
+}
+
+int gemm_bf16f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
+                 void *stream)
+{
+    return run_bf16(M, N, K, A, B, C, stream, kDefaultWaitLimitNs, 0);
+}
+
+int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K, const uint16_t *A,
+                                  const uint16_t *B, float *C, int64_t wait_limit_ns, void *stream)
+{
+    if (wait_limit_ns < 1000000 || wait_limit_ns > 10000000000LL)
+        return GEMM_ERR_INVALID_ARG;
+    if (K == 0)
+        return GEMM_ERR_INVALID_ARG;  // the K == 0 product launches no waiting kernel
+    return run_bf16(M, N, K, A, B, C, stream, (uint64_t)wait_limit_ns, 1);
+}
+
+int gemm_get_device_error(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    DeviceInfo d;
+    int st = current_device(&d);
+    if (st == GEMM_ERR_LAUNCH)
+        return st;
+    int value = 0;
+    const int zero = 0;
+    if (cudaMemcpy(&value, d.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(d.err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return value;
+}
+
+const char *gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK:
+        return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG:
+        return "GEMM_ERR_INVALID_ARG: negative size, null pointer, overlap or size too large";
+    case GEMM_ERR_ALIGNMENT:
+        return "GEMM_ERR_ALIGNMENT: bf16 path needs K % 8 == 0, N % 8 == 0 and 16-byte aligned "
+               "pointers";
+    case GEMM_ERR_LAUNCH:
+        return "GEMM_ERR_LAUNCH: a CUDA runtime call failed";
+    case GEMM_ERR_TIMEOUT:
+        return "GEMM_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
+    case GEMM_ERR_DEVICE:
+        return "GEMM_ERR_DEVICE: the current device is not compute capability 10.3 (sm_103a)";
+    default:
+        return "unknown gemm status";
+    }
+}
+
+} // extern "C"

@@ -1,0 +1,37 @@
+// Internal launch functions shared between the C-ABI translation unit and the
+// kernel translation units. Arguments are already validated by the caller.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rtm {
+
+// SIMT FP32 register-tiled product (sgemm_simt.cu). 1 <= K; M, N >= 1.
+cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
+                             cudaStream_t stream);
+
+// tcgen05 bf16 x bf16 -> fp32 product (gemm_tc.cu). K >= 1, K % 8 == 0,
+// N % 8 == 0, A/B/C 16-byte aligned. `err` is the device error word;
+// `wait_limit_ns` bounds every wait; `mute_producer` != 0 issues no loads
+// (failure-detection self-test only).
+struct TcLaunch {
+    int M, N, K;
+    const uint16_t *A;
+    const uint16_t *B;
+    float *C;
+    int *err;
+    uint64_t wait_limit_ns;
+    int mute_producer;
+    int sm_count;
+    void *encode_tiled;  // cuTensorMapEncodeTiled driver entry point
+};
+cudaError_t launch_gemm_bf16_tc(const TcLaunch &p, cudaStream_t stream);
+
+// C[0 .. count) = 0 (the K == 0 product).
+cudaError_t launch_zero_fill(float *C, int64_t count, cudaStream_t stream);
+
+// Status codes written into the device error word (same values as gemm.h).
+constexpr int kDevErrTimeout = -4;
+
+} // namespace rtm

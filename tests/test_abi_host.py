@@ -1,0 +1,109 @@
+"""CPU tests of the C ABI: the library builds for sm_103a, loads, exports every
+symbol that include/gemm.h declares, and rejects bad arguments on the host
+before any CUDA call. No kernel is launched here (there is no GPU)."""
+
+import ctypes
+
+import pytest
+
+import register_tiled_matrix_gb300 as rtm
+
+pytestmark = pytest.mark.cpu
+
+FAKE = 0x100000  # never dereferenced: every call below returns before any CUDA call
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rtm.build()
+    return rtm.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = rtm.header_symbols()
+    assert {"gemm_f32", "gemm_bf16f32", "gemm_get_device_error",
+            "gemm_bf16f32_selftest_timeout", "gemm_status_string"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in gemm.h but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in rtm.STATUS.items():
+        assert rtm.status_string(code).startswith(name)
+    assert rtm.status_string(12345) == "unknown gemm status"
+
+
+@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32"])
+def test_invalid_sizes(lib, fn):
+    f = getattr(lib, fn)
+    assert f(-1, 4, 4, FAKE, FAKE, FAKE * 2, None) == -1
+    assert f(4, -1, 4, FAKE, FAKE, FAKE * 2, None) == -1
+    assert f(4, 4, -8, FAKE, FAKE, FAKE * 2, None) == -1
+    assert f(1 << 31, 8, 8, FAKE, FAKE, FAKE * 2, None) == -1
+
+
+@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32"])
+def test_empty_output_is_a_noop(lib, fn):
+    f = getattr(lib, fn)
+    assert f(0, 16, 16, None, None, None, None) == 0
+    assert f(16, 0, 16, None, None, None, None) == 0
+
+
+@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32"])
+def test_null_pointers(lib, fn):
+    f = getattr(lib, fn)
+    assert f(8, 8, 8, FAKE, FAKE, None, None) == -1
+    assert f(8, 8, 8, None, FAKE, FAKE * 4, None) == -1
+    assert f(8, 8, 8, FAKE, None, FAKE * 4, None) == -1
+
+
+@pytest.mark.parametrize("fn,elem", [("gemm_f32", 4), ("gemm_bf16f32", 2)])
+def test_output_overlapping_input_rejected(lib, fn, elem):
+    f = getattr(lib, fn)
+    M = N = K = 64
+    base = 0x10000000
+    assert f(M, N, K, base, base + M * K * elem, base + 16, None) == -1     # C over A
+    assert f(M, N, K, base, base + (1 << 20), base + (1 << 20) + 16, None) == -1  # C over B
+
+
+def test_bf16_alignment_rules(lib):
+    f = lib.gemm_bf16f32
+    A, B, C = 0x10000000, 0x20000000, 0x30000000
+    assert f(16, 16, 12, A, B, C, None) == -2      # K % 8
+    assert f(16, 12, 16, A, B, C, None) == -2      # N % 8
+    assert f(16, 16, 16, A + 2, B, C, None) == -2  # A not 16-byte aligned
+    assert f(16, 16, 16, A, B + 8, C, None) == -2
+    assert f(16, 16, 16, A, B, C + 4, None) == -2
+
+
+def test_f32_alignment_rule(lib):
+    assert lib.gemm_f32(8, 8, 8, 0x10000001, 0x20000000, 0x30000000, None) == -2
+
+
+def test_selftest_limit_range(lib):
+    f = lib.gemm_bf16f32_selftest_timeout
+    A, B, C = 0x10000000, 0x20000000, 0x30000000
+    assert f(16, 16, 16, A, B, C, 10, None) == -1
+    assert f(16, 16, 16, A, B, C, 10 ** 11, None) == -1
+
+
+def test_ptxas_zero_spills(lib):
+    report = rtm.ptxas_report()
+    kernels = [k for k in report if "sgemm_rt_kernel" in k or "gemm_bf16_tc_kernel" in k]
+    assert kernels, "no kernels in the ptxas report"
+    for k in kernels:
+        r = report[k]
+        assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (k, r)
+        assert 0 < r["registers"] <= 255, (k, r)
+    simt = [report[k] for k in kernels if "sgemm_rt_kernel" in k]
+    assert all(r["registers"] <= 128 for r in simt), "two 256-thread CTAs per SM need <= 128 regs"
+
+
+def test_product_path_has_no_fallback(monkeypatch, tmp_path):
+    """With the library missing, the binding raises instead of computing elsewhere."""
+    from register_tiled_matrix_gb300 import binding
+
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load_library()

@@ -1,0 +1,133 @@
+"""GPU parity tests of gemm_bf16f32 (tcgen05 tensor-core kernel) against the
+CPU oracle fed the same bf16 values, through the C ABI (ctypes binding)."""
+
+import pytest
+import torch
+
+import oracle
+import register_tiled_matrix_gb300 as rtm
+import workloads
+from tests.parity import (assert_bit_exact, assert_close_to_oracle, guard_intact,
+                          guarded_output)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rtm.build()
+    rtm.load_library()
+
+
+def run(A, B):
+    C = rtm.gemm_bf16f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    return C
+
+
+def bf16_inputs(M, N, K, dist="normal", seed=0):
+    return workloads.make_inputs(M, N, K, dist, "bf16", seed=seed)
+
+
+def test_full_size_workload_sampled():
+    """The 8192^3 bf16 workload, as the bench launches it; 4096+ sampled entries."""
+    w = workloads.WORKLOADS["bf16_8192_normal"]
+    A, B = workloads.workload_inputs(w)
+    C = run(A, B)
+    assert_close_to_oracle(C, A, B, "bf16", full=False, seed=w.seed)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 256, 256), (1024, 1024, 1024),
+                                   (1000, 1000, 1000), (129, 264, 72), (1, 8, 8), (300, 8, 520),
+                                   (2048, 4096, 512), (4097, 3000, 1032)])
+def test_parity_shapes(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=M * 3 + N + K)
+    C = run(A, B)
+    full = M * N * K <= (1 << 31)
+    assert_close_to_oracle(C, A, B, "bf16", full=full, seed=M + N + K)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 136, 1000), (640, 512, 4096),
+                                   (1, 8, 8), (257, 264, 8)])
+def test_small_integer_bit_exact(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "int", "f32", seed=M + 2 * N + 3 * K)
+    C = run(A.to(torch.bfloat16), B.to(torch.bfloat16))  # {-4..4} is exact in bf16
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_identity_and_permutation_exact():
+    g = torch.Generator().manual_seed(41)
+    A = torch.randn(384, 256, generator=g).to(torch.bfloat16)
+    I256 = torch.eye(256).to(torch.bfloat16)
+    assert_bit_exact(run(A, I256), A.float().numpy())
+    I384 = torch.eye(384).to(torch.bfloat16)
+    assert_bit_exact(run(I384, A), A.float().numpy())
+    p = torch.randperm(384, generator=g)
+    P = torch.zeros(384, 384)
+    P[torch.arange(384), p] = 1.0
+    assert_bit_exact(run(P.to(torch.bfloat16), A), A[p].float().numpy())
+    q = torch.randperm(256, generator=g)
+    Q = torch.zeros(256, 256)
+    Q[q, torch.arange(256)] = 1.0
+    assert_bit_exact(run(A, Q.to(torch.bfloat16)), A[:, q].float().numpy())
+
+
+def test_rank_one_closed_form():
+    g = torch.Generator().manual_seed(42)
+    M, N, K = 300, 264, 1024
+    u = torch.randint(-8, 9, (M,), generator=g).float()
+    v = torch.randint(-8, 9, (N,), generator=g).float()
+    A = u[:, None].expand(M, K).contiguous().to(torch.bfloat16)
+    B = v[None, :].expand(K, N).contiguous().to(torch.bfloat16)
+    assert_bit_exact(run(A, B), (K * torch.outer(u, v)).numpy())
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 264, 136), (128, 256, 64), (3, 8, 16)])
+def test_guard_band_untouched(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=43)
+    buf, C = guarded_output(M, N, DEV, pad=4096)
+    rtm.gemm_bf16f32(A.to(DEV), B.to(DEV), out=C)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N)
+    assert_close_to_oracle(C, A, B, "bf16")
+
+
+def test_k_zero_writes_zeros():
+    C = torch.full((16, 8), 2.0, device=DEV)
+    rtm.gemm_bf16f32(torch.empty(16, 0, dtype=torch.bfloat16, device=DEV),
+                     torch.empty(0, 8, dtype=torch.bfloat16, device=DEV), out=C)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(C).item() == 0
+
+
+def test_alignment_errors_raise():
+    A = torch.zeros(16, 12, dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros(12, 16, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(rtm.GemmError) as e:
+        rtm.gemm_bf16f32(A, B)
+    assert e.value.status == -2
+
+
+def test_repeated_calls_identical():
+    A, B = bf16_inputs(2048, 2048, 2048, seed=44)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C1 = rtm.gemm_bf16f32(Ad, Bd)
+    C2 = rtm.gemm_bf16f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """With the loads muted, every wait runs out after 50 ms; the kernel records
+    a timeout and returns, and the next product on the same context is correct."""
+    A, B = bf16_inputs(256, 512, 256, seed=45)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = torch.empty(256, 512, device=DEV)
+    assert rtm.get_device_error() == 0
+    rtm.gemm_bf16f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
+    assert rtm.get_device_error() == -4
+    assert rtm.get_device_error() == 0, "reading the error word clears it"
+    C = run(A, B)
+    assert_close_to_oracle(C, A, B, "bf16")
