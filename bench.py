@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Throughput of the register-tiled product C = A.B on GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+  * gemm_f32      on the fp32 4096 x 4096 x 4096 workload (A, B ~ N(0,1)),
+  * gemm_bf16f32  on the bf16 8192 x 8192 x 8192 workload (A, B ~ N(0,1)
+                  rounded to bf16), fp32 accumulation and output.
+Together they exercise every tiling level of both CUDA paths (global C tiles,
+shared-memory K slices, register / tensor-memory accumulator tiles, ragged
+edge handling is covered by the tests).
+
+Metric: TFLOP/s = 2*M*N*K summed over the step's products / step time, with
+inputs resident in HBM. Each product's own launch duration is timed with CUDA
+events on its stream, giving per-kernel TFLOP/s and the roofline fraction
+(FP32 SIMT peak for gemm_f32, dense bf16 tensor peak for gemm_bf16f32).
+`e2e` repeats the step through the same public calls with host buffers:
+pinned host -> device copies of A and B, the product, device -> host copy of C.
+
+Multi-GPU: the product does not need an exchange, so N GPUs run N independent
+replicas (weak scaling); value = all ranks' flops / the slowest rank's time.
+
+--impl reference times the CPU oracle (plain fp64 triple loop) on a bounded
+sample of the same workloads, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from typing import Dict, List, Optional
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "GEMM TFLOP/s at 1 GB300 and % of FP32-SIMT / bf16-tensor roofline"
+UNIT = "TFLOP/s"
+STEP = ["f32_4096_normal", "bf16_8192_normal"]
+FP32_LANES_PER_SM = 128   # FP32 FMA lanes per Blackwell SM (4 partitions x 32)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of each kernel, keyed to the kernel source it was taken on;
+# reported as null once the source changes. See profiles/.
+TRAFFIC = {
+    "gemm_f32": {"bytes": None, "source_sha1": None, "note": ""},
+    "gemm_bf16f32": {"bytes": None, "source_sha1": None, "note": ""},
+}
+KERNEL_SOURCE = {
+    "gemm_f32": "register_tiled_matrix_gb300/csrc/sgemm_simt.cu",
+    "gemm_bf16f32": "register_tiled_matrix_gb300/csrc/gemm_tc.cu",
+}
+
+
+def source_sha1(kernel: str) -> str:
+    with open(os.path.join(ROOT, KERNEL_SOURCE[kernel]), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def load_peaks() -> Dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def reduce_over_ranks(elapsed_s: float, flops: float, device) -> (float, float):
+    """(max elapsed over ranks, sum of flops over ranks); identity at world 1."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return elapsed_s, flops
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    f = torch.tensor([flops], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(f, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(f.item())
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.lines: List[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms), "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)  # let the first sample land before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> Dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, pw = [], [], []
+        active = set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower() == "active":
+                    active.add(name)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(active),
+            "samples": len(sm),
+            "power_w_max": max(pw) if pw else None,
+        }
+
+
+# ------------------------------------------------------------------ our arm
+def make_step_inputs(device, names):
+    items = []
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        A, B = workloads.workload_inputs(w)
+        items.append({
+            "name": name, "w": w,
+            "A_host": A.pin_memory(), "B_host": B.pin_memory(),
+            "A": A.to(device), "B": B.to(device),
+            "C": torch.empty((w.M, w.N), dtype=torch.float32, device=device),
+            "C_host": torch.empty((w.M, w.N), dtype=torch.float32).pin_memory(),
+        })
+    return items
+
+
+def kernel_of(w) -> str:
+    return "gemm_f32" if w.dtype == "f32" else "gemm_bf16f32"
+
+
+def step_names(only: Optional[str]) -> List[str]:
+    names = [n for n in STEP if only is None or kernel_of(workloads.WORKLOADS[n]) == only]
+    if not names:
+        raise SystemExit(f"--only {only}: no such entry point in the step")
+    return names
+
+
+def step_config(names: List[str], world: int) -> Dict:
+    parts = []
+    for n in names:
+        w = workloads.WORKLOADS[n]
+        kind = "fp32" if w.dtype == "f32" else "bf16->fp32"
+        parts.append(f"{kernel_of(w)} {w.M}x{w.N}x{w.K} {kind}")
+    return {
+        "workload": "one step = " + " + ".join(parts) + ", row-major, N(0,1) inputs",
+        "products": [{"name": n, "M": workloads.WORKLOADS[n].M, "N": workloads.WORKLOADS[n].N,
+                      "K": workloads.WORKLOADS[n].K, "entry": kernel_of(workloads.WORKLOADS[n])}
+                     for n in names],
+        "parallelism": f"replicas x{world} (no exchange)",
+        "l2": "no explicit flush: the step's working set of A, B and C exceeds the 129 MB L2 "
+              "and each product evicts the other's operands between iterations",
+    }
+
+
+def run_ours(args) -> Optional[Dict]:
+    import register_tiled_matrix_gb300 as rtm
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (sm_103a)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    if rank == 0:
+        rtm.build()
+    barrier()
+    rtm.load_library()
+    fns = {"gemm_f32": rtm.gemm_f32, "gemm_bf16f32": rtm.gemm_bf16f32}
+
+    names = step_names(args.only)
+    items = make_step_inputs(device, names)
+    stream = torch.cuda.current_stream(device)
+    step_flops = sum(it["w"].flops for it in items)
+
+    def step(record=None):
+        for i, it in enumerate(items):
+            if record is not None:
+                record[i][0].record(stream)
+            fns[kernel_of(it["w"])](it["A"], it["B"], out=it["C"])
+            if record is not None:
+                record[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if rtm.get_device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    # ---- timed region: K steps, inputs resident in HBM
+    per_kernel = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in items] for _ in range(args.steps)]
+    e_all0 = torch.cuda.Event(enable_timing=True)
+    e_all1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(device)
+    e_all0.record(stream)
+    for k in range(args.steps):
+        step(per_kernel[k])
+    e_all1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    clock_summary = clocks.stop()
+    elapsed_s = e_all0.elapsed_time(e_all1) / 1e3
+    dev_err = rtm.get_device_error()
+    if dev_err != 0:
+        raise SystemExit(f"device error in the timed region: {rtm.status_string(dev_err)}")
+    launches = args.steps * len(items)
+
+    kernel_ms = {}
+    for i, it in enumerate(items):
+        ts = [per_kernel[k][i][0].elapsed_time(per_kernel[k][i][1]) for k in range(args.steps)]
+        kernel_ms[it["name"]] = {"mean": statistics.fmean(ts), "median": statistics.median(ts),
+                                 "min": min(ts)}
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e_steps = 0 if args.no_e2e else max(3, args.steps // 5)
+    h2d = sum(it["A_host"].numel() * it["A_host"].element_size()
+              + it["B_host"].numel() * it["B_host"].element_size() for it in items)
+    d2h = sum(it["C_host"].numel() * 4 for it in items)
+
+    def step_e2e():
+        for it in items:
+            it["A"].copy_(it["A_host"], non_blocking=True)
+            it["B"].copy_(it["B_host"], non_blocking=True)
+            fns[kernel_of(it["w"])](it["A"], it["B"], out=it["C"])
+            it["C_host"].copy_(it["C"], non_blocking=True)
+
+    e2e_s = 0.0
+    if e2e_steps:
+        step_e2e()
+        torch.cuda.synchronize(device)
+        barrier()
+        x0 = torch.cuda.Event(enable_timing=True)
+        x1 = torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(e2e_steps):
+            step_e2e()
+        x1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+        e2e_s = x0.elapsed_time(x1) / 1e3
+
+    max_elapsed, all_flops = reduce_over_ranks(elapsed_s, step_flops * args.steps, device)
+    max_e2e, all_e2e_flops = reduce_over_ranks(e2e_s, step_flops * e2e_steps, device)
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    max_mhz = float(peaks.get("sm_max_mhz") or FALLBACK_PEAKS["sm_max_mhz"])
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    bf16_peak = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+
+    rooflines = {}
+    for it in items:
+        w = it["w"]
+        kern = kernel_of(w)
+        ms = kernel_ms[it["name"]]["mean"]
+        achieved = w.flops / (ms / 1e3) / 1e12
+        if kern == "gemm_f32":
+            bound, peak, peak_note = "alu", fp32_peak, (
+                f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {max_mhz:.0f} MHz")
+        else:
+            bound, peak, peak_note = "tensor", bf16_peak, (
+                f"{peaks['source']} dense bf16, sustained (kernel timed inside a long step)")
+        traffic = TRAFFIC[kern]
+        tb = traffic["bytes"] if traffic["source_sha1"] == source_sha1(kern) else None
+        rooflines[kern] = {
+            "bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": tb,
+            "peak_source": peak_note, "workload": it["name"],
+            "ms_mean": round(ms, 4), "ms_median": round(kernel_ms[it["name"]]["median"], 4),
+            "algorithmic_flops": w.flops,
+            "algorithmic_bytes": w.in_bytes + w.out_bytes,
+        }
+    dominant = max(items, key=lambda it: kernel_ms[it["name"]]["mean"])
+    out = {
+        "metric": METRIC,
+        "value": round(all_flops / max_elapsed / 1e12, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_elapsed * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 (gemm_f32) + bf16 in / f32 accumulate (gemm_bf16f32)",
+        "data": "synthetic (seeded N(0,1); bf16 inputs rounded to nearest even)",
+        "config": step_config(names, world),
+        "roofline": rooflines[kernel_of(dominant["w"])],
+        "rooflines": rooflines,
+        "kernel_ms": {k: {kk: round(vv, 4) for kk, vv in v.items()} for k, v in kernel_ms.items()},
+        "e2e": ({"value": round(all_e2e_flops / max_e2e / 1e12, 3), "unit": UNIT,
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+                if e2e_steps else None),
+        "gpu_launches": launches,
+        "clocks": clock_summary,
+        "peaks": {"source": peaks["source"], "fp32_simt_tflops": round(fp32_peak, 2),
+                  "bf16_tflops_sustained": bf16_peak,
+                  "bf16_tflops_burst": float(peaks.get("bf16_tflops", 0.0))},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(names, items, budget_s=args.cpu_budget)
+    return out
+
+
+# ------------------------------------------------------------------ oracle timing
+def _oracle_inputs(names, items=None):
+    import numpy as np
+
+    res = []
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        if items is not None:
+            it = next(x for x in items if x["name"] == name)
+            A, B = it["A_host"], it["B_host"]
+        else:
+            A, B = workloads.workload_inputs(w)
+        res.append((w, np.ascontiguousarray(A.float().numpy()),
+                    np.ascontiguousarray(B.float().numpy())))
+    return res
+
+
+def _oracle_sample(oracle, w, A, B, count, seed):
+    rows, cols = workloads.sample_indices(w.M, w.N, count=count, seed=seed, edge_count=0)
+    rows, cols = rows[:count], cols[:count]
+    t0 = time.perf_counter()
+    oracle.gemm_sampled(A, B, rows, cols)
+    return time.perf_counter() - t0, 2.0 * w.K * len(rows)
+
+
+def _calibrate(oracle, inputs, probe=256):
+    """Seconds per sampled entry of each product (entries split over all threads)."""
+    rates = []
+    for (w, A, B) in inputs:
+        dt, _ = _oracle_sample(oracle, w, A, B, probe, seed=w.seed)
+        rates.append(dt / probe)
+    return rates
+
+
+def cpu_baseline(names, items=None, budget_s: float = 15.0) -> Dict:
+    """Time the oracle as it stands on a bounded sample of the step's products."""
+    import oracle
+
+    oracle.build()
+    inputs = _oracle_inputs(names, items)
+    per_entry = _calibrate(oracle, inputs)
+    share = budget_s / len(inputs)
+    total_t, total_f, desc = 0.0, 0.0, []
+    for (w, A, B), pe in zip(inputs, per_entry):
+        count = max(oracle.max_threads(), int(share / max(pe, 1e-9)))
+        dt, fl = _oracle_sample(oracle, w, A, B, count, seed=w.seed + 7)
+        total_t += dt
+        total_f += fl
+        desc.append(f"{count} seeded entries of C for {w.name}")
+    return {"value": total_f / total_t / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "; ".join(desc) + f" (fp64 dot products of length K, {total_t:.1f} s)"}
+
+
+def run_reference(args) -> Optional[Dict]:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    names = step_names(args.only)
+    inputs = _oracle_inputs(names)
+    per_entry = _calibrate(oracle, inputs)
+    steps_total = args.steps + args.warmup
+    per_step_budget = args.reference_budget / max(steps_total, 1)
+    counts = [max(1, int(per_step_budget / len(inputs) / max(pe, 1e-9))) for pe in per_entry]
+    for i in range(args.warmup):
+        for (w, A, B), c in zip(inputs, counts):
+            _oracle_sample(oracle, w, A, B, c, seed=w.seed + 100 + i)
+    total_t, total_f = 0.0, 0.0
+    for k in range(args.steps):
+        for (w, A, B), c in zip(inputs, counts):
+            dt, fl = _oracle_sample(oracle, w, A, B, c, seed=w.seed + 1000 + k)
+            total_t += dt
+            total_f += fl
+    value = total_f / total_t / 1e12
+    sample = "per step: " + "; ".join(
+        f"{c} seeded entries of C for {w.name}" for (w, _, _), c in zip(inputs, counts))
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_t * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle accumulation)",
+        "data": "synthetic (seeded N(0,1); bf16 inputs rounded to nearest even)",
+        "config": step_config(names, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--only", choices=["gemm_f32", "gemm_bf16f32"], default=None,
+                   help="time one entry point's product instead of the whole step")
+    p.add_argument("--cpu-budget", type=float, default=15.0,
+                   help="seconds of oracle work for the cpu_baseline sample")
+    p.add_argument("--reference-budget", type=float, default=120.0,
+                   help="seconds of oracle work for the whole --impl reference run")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    world, rank, _ = dist_env()
+    if args.gpus != world and not (world == 1 and args.gpus == 1):
+        if world == 1:
+            p.error(f"--gpus {args.gpus} needs torchrun with --nproc-per-node {args.gpus}")
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
