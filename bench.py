@@ -55,8 +55,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
 # reported as null once the source changes. See profiles/.
 TRAFFIC = {
-    "gemm_f32": {"bytes": None, "source_sha1": None, "note": ""},
-    "gemm_bf16f32": {"bytes": None, "source_sha1": None, "note": ""},
+    "gemm_f32": {"bytes": 390920448, "source_sha1": "1ab2fd976e930e775d82a3726afdc5b825dae288",
+                 "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
+    "gemm_bf16f32": {"bytes": 1254241320,
+                     "source_sha1": "88f1f62840bb10818b39aa356f0738dbb650f6d5",
+                     "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {
     "gemm_f32": "register_tiled_matrix_gb300/csrc/sgemm_simt.cu",
@@ -319,7 +322,12 @@ def run_ours(args) -> Optional[Dict]:
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     max_mhz = float(peaks.get("sm_max_mhz") or FALLBACK_PEAKS["sm_max_mhz"])
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
-    bf16_peak = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+    # The step alternates an FP32-pipe product with the tensor-core product and
+    # does not reach the power cap (the clock record shows it), so the tensor
+    # product is compared with the burst bf16 figure; the power-capped
+    # sustained figure is reported beside it.
+    bf16_peak = float(peaks["bf16_tflops"])
+    bf16_sustained = float(peaks.get("bf16_tflops_sustained") or bf16_peak)
 
     rooflines = {}
     for it in items:
@@ -332,7 +340,8 @@ def run_ours(args) -> Optional[Dict]:
                 f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {max_mhz:.0f} MHz")
         else:
             bound, peak, peak_note = "tensor", bf16_peak, (
-                f"{peaks['source']} dense bf16, sustained (kernel timed inside a long step)")
+                f"{peaks['source']} dense bf16 burst (cuBLAS 8192^3); clocks stay at max in "
+                f"this step")
         traffic = TRAFFIC[kern]
         tb = traffic["bytes"] if traffic["source_sha1"] == source_sha1(kern) else None
         rooflines[kern] = {
@@ -343,6 +352,8 @@ def run_ours(args) -> Optional[Dict]:
             "algorithmic_flops": w.flops,
             "algorithmic_bytes": w.in_bytes + w.out_bytes,
         }
+        if kern == "gemm_bf16f32":
+            rooflines[kern]["frac_of_sustained"] = round(achieved / bf16_sustained, 4)
     dominant = max(items, key=lambda it: kernel_ms[it["name"]]["mean"])
     out = {
         "metric": METRIC,
@@ -367,8 +378,7 @@ def run_ours(args) -> Optional[Dict]:
         "gpu_launches": launches,
         "clocks": clock_summary,
         "peaks": {"source": peaks["source"], "fp32_simt_tflops": round(fp32_peak, 2),
-                  "bf16_tflops_sustained": bf16_peak,
-                  "bf16_tflops_burst": float(peaks.get("bf16_tflops", 0.0))},
+                  "bf16_tflops_burst": bf16_peak, "bf16_tflops_sustained": bf16_sustained},
     }
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(names, items, budget_s=args.cpu_budget)
