@@ -55,7 +55,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
 # reported as null once the source changes. See profiles/.
 TRAFFIC = {
-    "gemm_f32": {"bytes": 390920448, "source_sha1": "1ab2fd976e930e775d82a3726afdc5b825dae288",
+    "gemm_f32": {"bytes": 394298368, "source_sha1": "95ed9c3bc1204705753ae5096927587ab0cd17c0",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
     "gemm_bf16f32": {"bytes": 1254241320,
                      "source_sha1": "88f1f62840bb10818b39aa356f0738dbb650f6d5",

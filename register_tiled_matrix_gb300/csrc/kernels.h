@@ -7,7 +7,8 @@
 
 namespace rtm {
 
-// SIMT FP32 register-tiled product (sgemm_simt.cu). 1 <= K; M, N >= 1.
+// SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
+// 4-byte-aligned pointers. 1 <= K; M, N >= 1.
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
                              cudaStream_t stream);
 

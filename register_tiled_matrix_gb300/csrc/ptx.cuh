@@ -36,6 +36,17 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
                  : "memory");
 }
 
+// Unpredicated forms (whole element in bounds).
+__device__ __forceinline__ void cp_async_4_full(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16_full(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
