@@ -478,6 +478,46 @@ def run_reference(args) -> Optional[Dict]:
     }
 
 
+def run_ladder(args) -> Optional[Dict]:
+    """Time the page's ablation ladder (gemm_f32_ladder rungs 0-3) on one square size."""
+    import register_tiled_matrix_gb300 as rtm
+    from oracle import tiling_model
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --ladder needs a CUDA GPU (sm_103a)")
+    rtm.build()
+    n = args.ladder_size
+    A, B = workloads.make_inputs(n, n, n, "normal", "f32", seed=workloads.SEED_BASE + 99)
+    A, B = A.cuda(), B.cuda()
+    C = torch.empty(n, n, device="cuda")
+    flops = 2.0 * n ** 3
+    # Model of shared reads per output per k for each rung (counting model of
+    # the page's loops): naive 0, shared-tiled 2, 4x4 register 0.5, 8x8 0.25.
+    model = {0: 0.0, 1: 2.0, 2: tiling_model.predicted_shared_reads_per_output_per_k(4, 4),
+             3: tiling_model.predicted_shared_reads_per_output_per_k(8, 8)}
+    rungs = []
+    for rung in range(4):
+        for _ in range(args.warmup):
+            rtm.gemm_f32_ladder(rung, A, B, out=C)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            rtm.gemm_f32_ladder(rung, A, B, out=C)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        rungs.append({"rung": rung, "kernel": rtm.LADDER[rung], "ms": round(ms, 4),
+                      "tflops": round(flops / ms / 1e9, 2),
+                      "model_shared_reads_per_output_per_k": model[rung]})
+    if rtm.get_device_error() != 0:
+        raise SystemExit("device error in the ladder")
+    return {"metric": "ablation ladder: GEMM TFLOP/s per tiling level", "unit": UNIT,
+            "config": {"workload": f"gemm_f32_ladder {n}x{n}x{n} fp32, N(0,1) inputs"},
+            "steps": args.steps, "warmup": args.warmup, "rungs": rungs}
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -492,6 +532,9 @@ def main(argv=None):
                    help="seconds of oracle work for the cpu_baseline sample")
     p.add_argument("--reference-budget", type=float, default=120.0,
                    help="seconds of oracle work for the whole --impl reference run")
+    p.add_argument("--ladder", action="store_true",
+                   help="time the ablation ladder (gemm_f32_ladder rungs 0-3) instead of the step")
+    p.add_argument("--ladder-size", type=int, default=4096)
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -499,7 +542,10 @@ def main(argv=None):
     if args.gpus != world and not (world == 1 and args.gpus == 1):
         if world == 1:
             p.error(f"--gpus {args.gpus} needs torchrun with --nproc-per-node {args.gpus}")
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.ladder:
+        out = run_ladder(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
     if torch.distributed.is_available() and torch.distributed.is_initialized():

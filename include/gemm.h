@@ -83,6 +83,28 @@ int gemm_f32(int64_t M, int64_t N, int64_t K,
              const float *A, const float *B, float *C, void *stream);
 
 /*
+ * gemm_f32_ladder — the ablation ladder of the register-tiling page: the same
+ * fp32 product computed by the kernels the page compares, kept as the page
+ * describes them, for measuring what each tiling level buys
+ * ("【infra之路】理解 Register Tiling", sections "先看 Shared Memory 版本里，一个
+ * 线程在做什么", "Register Tiling 的核心思想", "关键循环", "用一张图对比三个版本").
+ *
+ *   rung 0  naive: one thread per output, operands read from global memory;
+ *   rung 1  shared-memory tiled, TILE = 32, one output per thread
+ *           (2 shared reads per output per k);
+ *   rung 2  register tiled, 64 x 64 block, 16 x 16 threads, a 4 x 4 block of
+ *           outputs per thread (0.5 shared reads per output per k);
+ *   rung 3  gemm_f32 itself (8 x 8 per thread, 0.25).
+ *
+ * Same layout, ownership, degenerate-shape and error rules as gemm_f32; any
+ * shape. Rungs 0-2 also return GEMM_ERR_INVALID_ARG for a rung outside 0..3 or
+ * when M exceeds what their grid can cover (65535 tiles along M: M > 1,048,560
+ * for rung 0, 2,097,120 for rung 1, 4,194,240 for rung 2).
+ */
+int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
+                    const float *A, const float *B, float *C, void *stream);
+
+/*
  * gemm_bf16f32 — bfloat16 inputs, fp32 accumulation and output, on the
  * tcgen05 tensor cores: operands staged in shared memory by TMA, the
  * accumulator tile held in tensor memory (the tensor-core form of the

@@ -13,11 +13,13 @@ memory and streams) plus the in-tree build step.
 
 from .native_build import build, ptxas_report  # noqa: F401
 from .binding import (  # noqa: F401
+    LADDER,
     STATUS,
     GemmError,
     gemm_bf16f32,
     gemm_bf16f32_selftest_timeout,
     gemm_f32,
+    gemm_f32_ladder,
     get_device_error,
     header_symbols,
     library_path,

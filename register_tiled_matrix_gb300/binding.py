@@ -55,6 +55,8 @@ def load_library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [i64, i64, i64, p, p, p, p]
             f.restype = ctypes.c_int
+        lib.gemm_f32_ladder.argtypes = [ctypes.c_int, i64, i64, i64, p, p, p, p]
+        lib.gemm_f32_ladder.restype = ctypes.c_int
         lib.gemm_bf16f32_selftest_timeout.argtypes = [i64, i64, i64, p, p, p, i64, p]
         lib.gemm_bf16f32_selftest_timeout.restype = ctypes.c_int
         lib.gemm_get_device_error.argtypes = [p]
@@ -119,6 +121,23 @@ def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = Non
     with torch.cuda.device(A.device):
         _check(load_library().gemm_f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                        _stream_handle(stream)))
+    return C
+
+
+LADDER = {0: "naive", 1: "shared-tiled 32x32", 2: "register-tiled 64x64, 4x4/thread",
+          3: "register-tiled 128x128, 8x8/thread (gemm_f32)"}
+
+
+def gemm_f32_ladder(rung: int, A: torch.Tensor, B: torch.Tensor,
+                    out: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B with rung `rung` of the page's ablation ladder (see LADDER)."""
+    C = _prepare(A, B, torch.float32, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        _check(load_library().gemm_f32_ladder(int(rung), M, N, K, A.data_ptr(), B.data_ptr(),
+                                              C.data_ptr(), _stream_handle(stream)))
     return C
 
 

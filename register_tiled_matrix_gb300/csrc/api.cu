@@ -207,6 +207,34 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B, fl
     return finish(rtm::launch_sgemm_f32((int)M, (int)N, (int)K, A, B, C, s));
 }
 
+int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K, const float *A, const float *B,
+                    float *C, void *stream)
+{
+    if (rung < 0 || rung > 3)
+        return GEMM_ERR_INVALID_ARG;
+    if (rung == 3)
+        return gemm_f32(M, N, K, A, B, C, stream);
+    bool nothing = false;
+    int st = check_common(M, N, K, A, B, C, 4, &nothing);
+    if (st != GEMM_OK || nothing)
+        return st;
+    if ((reinterpret_cast<uintptr_t>(C) & 3) != 0 ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3) != 0 ||
+                   (reinterpret_cast<uintptr_t>(B) & 3) != 0)))
+        return GEMM_ERR_ALIGNMENT;
+    DeviceInfo d;
+    st = current_device(&d);
+    if (st != GEMM_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return finish(rtm::launch_zero_fill(C, M * N, s));
+    const cudaError_t e = rtm::launch_sgemm_ladder(rung, (int)M, (int)N, (int)K, A, B, C, s);
+    if (e == cudaErrorInvalidValue)
+        return GEMM_ERR_INVALID_ARG;  // grid larger than the launch limits
+    return finish(e);
+}
+
 int gemm_bf16f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
                  void *stream)
 {

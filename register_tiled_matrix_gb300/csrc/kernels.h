@@ -12,6 +12,11 @@ namespace rtm {
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
                              cudaStream_t stream);
 
+// The page's ablation ladder (sgemm_ladder.cu): rung 0 naive, 1 shared-memory
+// tiled (TILE 32), 2 register tiled (64 x 64 block, 4 x 4 per thread).
+cudaError_t launch_sgemm_ladder(int rung, int M, int N, int K, const float *A, const float *B,
+                                float *C, cudaStream_t stream);
+
 // tcgen05 bf16 x bf16 -> fp32 product (gemm_tc.cu). K >= 1, K % 8 == 0,
 // N % 8 == 0, A/B/C 16-byte aligned. `err` is the device error word;
 // `wait_limit_ns` bounds every wait; `mute_producer` != 0 issues no loads
