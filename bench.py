@@ -518,6 +518,63 @@ def run_ladder(args) -> Optional[Dict]:
             "steps": args.steps, "warmup": args.warmup, "rungs": rungs}
 
 
+def run_configs(args) -> Optional[Dict]:
+    """Time every configuration's product (report only; the headline is the step)."""
+    import register_tiled_matrix_gb300 as rtm
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --configs needs a CUDA GPU (sm_103a)")
+    rtm.build()
+    peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * float(peaks.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    rows = []
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    for name, w in workloads.WORKLOADS.items():
+        A, B = workloads.workload_inputs(w)
+        A, B = A.cuda(), B.cuda()
+        C = torch.empty(w.M, w.N, device="cuda")
+        entries = []
+        if w.dtype == "f32":
+            entries.append(("gemm_f32", lambda: rtm.gemm_f32(A, B, out=C), fp32_peak))
+            need = rtm.gemm_f32_workspace_bytes(w.M, w.N, w.K)
+            if need > 0:
+                ws = torch.empty(need // 4, device="cuda")
+                entries.append((f"gemm_f32_ws (split-K x{need // (w.M * w.N * 4)})",
+                                lambda: rtm.gemm_f32_ws(A, B, out=C, workspace=ws), fp32_peak))
+        else:
+            entries.append(("gemm_bf16f32", lambda: rtm.gemm_bf16f32(A, B, out=C),
+                            float(peaks["bf16_tflops"])))
+        for entry, fn, peak in entries:
+            ms = timed(fn)
+            tf = w.flops / ms / 1e9
+            rows.append({"config": name, "M": w.M, "N": w.N, "K": w.K, "entry": entry,
+                         "ms": round(ms, 4), "tflops": round(tf, 2),
+                         "frac_of_peak": round(tf / peak, 4)})
+        del A, B, C
+        torch.cuda.empty_cache()
+    if rtm.get_device_error() != 0:
+        raise SystemExit("device error in the configs run")
+    return {"metric": "GEMM TFLOP/s per configuration (report only)", "unit": UNIT,
+            "steps": args.steps, "warmup": args.warmup,
+            "peaks": {"fp32_simt_tflops": round(fp32_peak, 2),
+                      "bf16_tflops_burst": float(peaks["bf16_tflops"])},
+            "l2": "back-to-back launches (L2-warm for the smaller configs)", "configs": rows}
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -535,6 +592,8 @@ def main(argv=None):
     p.add_argument("--ladder", action="store_true",
                    help="time the ablation ladder (gemm_f32_ladder rungs 0-3) instead of the step")
     p.add_argument("--ladder-size", type=int, default=4096)
+    p.add_argument("--configs", action="store_true",
+                   help="time every configuration's product (report only)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -544,6 +603,8 @@ def main(argv=None):
             p.error(f"--gpus {args.gpus} needs torchrun with --nproc-per-node {args.gpus}")
     if args.ladder:
         out = run_ladder(args)
+    elif args.configs:
+        out = run_configs(args)
     else:
         out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:

@@ -83,6 +83,34 @@ int gemm_f32(int64_t M, int64_t N, int64_t K,
              const float *A, const float *B, float *C, void *stream);
 
 /*
+ * gemm_f32_workspace_bytes — bytes of scratch memory gemm_f32_ws uses for an
+ * M x N x K product on the current device: 0 when the product has enough C
+ * tiles to fill the GPU (gemm_f32_ws then needs no workspace), otherwise
+ * splits * M * N * 4 for the split-K schedule described below. Returns a
+ * negative status on invalid sizes (GEMM_ERR_INVALID_ARG) or when no usable
+ * device is current (GEMM_ERR_LAUNCH, GEMM_ERR_DEVICE).
+ *
+ * gemm_f32_ws — the same product as gemm_f32 (same layout, ownership and
+ * degenerate-shape rules) for shapes with few C tiles, such as skinny or
+ * small products: when workspace_bytes >= gemm_f32_workspace_bytes(M, N, K)
+ * > 0, K is split into `splits` chunks (a multiple of 32 deep); each chunk's
+ * partial M x N product is written to its own slab of `workspace` (device
+ * memory owned by the caller, 4-byte aligned, 16-byte aligned for the
+ * vector path, not overlapping A, B or C), and a second kernel adds the slabs
+ * into C in increasing chunk order, so results are bit-for-bit reproducible
+ * from call to call. Otherwise (no split needed, or the workspace too small)
+ * it runs exactly what gemm_f32 runs. The workspace contents on return are
+ * unspecified; two calls in flight at once must not share a workspace. The
+ * split is the pages' global tiling applied to K as well as to C tiles
+ * ("寄存器Tiling跨架构解析", section 1.1: global tiling decides how much work
+ * each block gets) and changes only the summation order.
+ */
+int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int gemm_f32_ws(int64_t M, int64_t N, int64_t K,
+                const float *A, const float *B, float *C,
+                void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
  * gemm_f32_ladder — the ablation ladder of the register-tiling page: the same
  * fp32 product computed by the kernels the page compares, kept as the page
  * describes them, for measuring what each tiling level buys

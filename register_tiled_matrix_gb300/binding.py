@@ -55,6 +55,10 @@ def load_library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [i64, i64, i64, p, p, p, p]
             f.restype = ctypes.c_int
+        lib.gemm_f32_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.gemm_f32_workspace_bytes.restype = ctypes.c_int64
+        lib.gemm_f32_ws.argtypes = [i64, i64, i64, p, p, p, p, i64, p]
+        lib.gemm_f32_ws.restype = ctypes.c_int
         lib.gemm_f32_ladder.argtypes = [ctypes.c_int, i64, i64, i64, p, p, p, p]
         lib.gemm_f32_ladder.restype = ctypes.c_int
         lib.gemm_bf16f32_selftest_timeout.argtypes = [i64, i64, i64, p, p, p, i64, p]
@@ -121,6 +125,35 @@ def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = Non
     with torch.cuda.device(A.device):
         _check(load_library().gemm_f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                        _stream_handle(stream)))
+    return C
+
+
+def gemm_f32_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace bytes gemm_f32_ws uses for this shape on the current device (0: none)."""
+    n = int(load_library().gemm_f32_workspace_bytes(int(M), int(N), int(K)))
+    _check(n if n < 0 else 0)
+    return n
+
+
+def gemm_f32_ws(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B, splitting K over a workspace when the shape has too few C tiles.
+
+    `workspace` is a CUDA tensor of at least gemm_f32_workspace_bytes(M, N, K)
+    bytes; when None, one is allocated with torch for this call."""
+    C = _prepare(A, B, torch.float32, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        if workspace is None:
+            need = gemm_f32_workspace_bytes(M, N, K)
+            workspace = torch.empty(max(need // 4, 1), dtype=torch.float32, device=A.device)
+        if not workspace.is_cuda or workspace.device != A.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor on A's device")
+        nbytes = workspace.numel() * workspace.element_size()
+        _check(load_library().gemm_f32_ws(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                          workspace.data_ptr(), nbytes, _stream_handle(stream)))
     return C
 
 

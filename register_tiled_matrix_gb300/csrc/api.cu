@@ -207,6 +207,53 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B, fl
     return finish(rtm::launch_sgemm_f32((int)M, (int)N, (int)K, A, B, C, s));
 }
 
+int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim ||
+        M * N > (int64_t)1 << 52 || M * K > (int64_t)1 << 52 || K * N > (int64_t)1 << 52)
+        return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0 || K == 0)
+        return 0;
+    DeviceInfo d;
+    const int st = current_device(&d);
+    if (st != GEMM_OK)
+        return st;
+    const rtm::SplitK plan = rtm::sgemm_splitk_plan((int)M, (int)N, (int)K, d.sms);
+    return plan.splits > 1 ? (int64_t)plan.splits * M * N * (int64_t)sizeof(float) : 0;
+}
+
+int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B, float *C,
+                void *workspace, int64_t workspace_bytes, void *stream)
+{
+    bool nothing = false;
+    int st = check_common(M, N, K, A, B, C, 4, &nothing);
+    if (st != GEMM_OK || nothing)
+        return st;
+    if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace))
+        return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(C) & 3) != 0 ||
+        (reinterpret_cast<uintptr_t>(workspace) & 3) != 0 ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3) != 0 ||
+                   (reinterpret_cast<uintptr_t>(B) & 3) != 0)))
+        return GEMM_ERR_ALIGNMENT;
+    DeviceInfo d;
+    st = current_device(&d);
+    if (st != GEMM_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return finish(rtm::launch_zero_fill(C, M * N, s));
+    const rtm::SplitK plan = rtm::sgemm_splitk_plan((int)M, (int)N, (int)K, d.sms);
+    const int64_t need = plan.splits > 1 ? (int64_t)plan.splits * M * N * 4 : 0;
+    if (need == 0 || workspace_bytes < need)
+        return finish(rtm::launch_sgemm_f32((int)M, (int)N, (int)K, A, B, C, s));
+    if (overlaps(workspace, need, A, M * K * 4) || overlaps(workspace, need, B, K * N * 4) ||
+        overlaps(workspace, need, C, M * N * 4))
+        return GEMM_ERR_INVALID_ARG;
+    return finish(rtm::launch_sgemm_f32_splitk((int)M, (int)N, (int)K, A, B, C, plan,
+                                               static_cast<float *>(workspace), s));
+}
+
 int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K, const float *A, const float *B,
                     float *C, void *stream)
 {

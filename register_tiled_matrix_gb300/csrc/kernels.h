@@ -12,6 +12,19 @@ namespace rtm {
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
                              cudaStream_t stream);
 
+// Split-K schedule of the SIMT product for shapes with too few C tiles to
+// fill the GPU: `splits` CTA rows each sum `kchunk` of K (a multiple of the
+// 32-deep slice) into their own M x N slab of a workspace, then a reduction
+// kernel adds the slabs in increasing split order (deterministic).
+struct SplitK {
+    int splits;  // 1: no split (plain product)
+    int kchunk;
+};
+SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count);
+// workspace: plan.splits * M * N floats. 1 <= K; M, N >= 1; plan.splits >= 2.
+cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
+                                    const SplitK &plan, float *workspace, cudaStream_t stream);
+
 // The page's ablation ladder (sgemm_ladder.cu): rung 0 naive, 1 shared-memory
 // tiled (TILE 32), 2 register tiled (64 x 64 block, 4 x 4 per thread).
 cudaError_t launch_sgemm_ladder(int rung, int M, int N, int K, const float *A, const float *B,

@@ -89,9 +89,19 @@ __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n,
 // the next row's and can be reused by the operand cache).
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC>
 __global__ void __launch_bounds__(kThreads, MINB)
-    sgemm_rt_kernel(int M, int N, int K, const float *__restrict__ A,
-                    const float *__restrict__ B, float *__restrict__ C)
+    sgemm_rt_kernel(int M, int N, int K_total, int kchunk, const float *__restrict__ A,
+                    const float *__restrict__ B, float *__restrict__ C, size_t c_split_stride)
 {
+    // Split-K: CTA row blockIdx.y of the grid sums k in [y * kchunk, +kchunk)
+    // and writes its partial tile to C + y * c_split_stride (one split: the
+    // whole of K straight into C). A keeps its full row stride K_total.
+    const int lda = K_total;
+    const int k_begin = blockIdx.y * kchunk;
+    const int K = min(kchunk, K_total - k_begin);
+    A += k_begin;
+    B += (size_t)k_begin * N;
+    C += blockIdx.y * c_split_stride;
+
     using G = Cfg<BM, BN, BK, STAGES>;
     constexpr int TM = G::TM, TN = G::TN, QM = G::QM, QN = G::QN;
     constexpr int SUBM = G::SUBM, SUBN = G::SUBN;
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     constexpr int JROWS = G::JROWS;
     const int a_m = warp * (BM / 8) + (lane >> 3);
     const int a_k = lane & 7;
-    const float *a_src = A + (size_t)min(m0 + a_m, M - 1) * K + a_k;
+    const float *a_src = A + (size_t)min(m0 + a_m, M - 1) * lda + a_k;
     const uint32_t a_dst0 = smem_u32(sA + a_k * LDA + a_m);
 
     // B loader, 16-byte path: copy i moves B[k0 + 8i + warp][n0 + 4 lane .. +3]
@@ -150,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (c < G::A_PER_THREAD) {
             const int h = c / JROWS, j = c % JROWS;
             cp_async_4_full(a_dst0 + stage * A_STAGE_BYTES + (uint32_t)((8 * h * LDA + 4 * j) * 4),
-                            a_src + (size_t)(4 * j) * K + (k0 + 8 * h));
+                            a_src + (size_t)(4 * j) * lda + (k0 + 8 * h));
         } else {
             const int i = c - G::A_PER_THREAD;
             const int krow = i * (kThreads / (BN / 4));
@@ -169,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
             for (int j = 0; j < JROWS; ++j) {
                 const bool ok = k_ok && (m0 + a_m + 4 * j < M);
-                const float *src = ok ? a_src + (size_t)(4 * j) * K + (k0 + 8 * h) : A;
+                const float *src = ok ? a_src + (size_t)(4 * j) * lda + (k0 + 8 * h) : A;
                 cp_async_4(a_dst + (uint32_t)((8 * h * LDA + 4 * j) * 4), src, ok ? 4u : 0u);
             }
         }
@@ -300,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC>
 cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, float *C,
-                       cudaStream_t stream)
+                       cudaStream_t stream, int splits = 1, int kchunk = 0)
 {
     using G = Cfg<BM, BN, BK, STAGES>;
     auto kernel = sgemm_rt_kernel<BM, BN, BK, STAGES, MINB, ORDER, B_VEC, C_VEC>;
@@ -323,31 +333,121 @@ cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, floa
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     if (tiles > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    kernel<<<(unsigned)tiles, kThreads, G::SMEM_BYTES, stream>>>(M, N, K, A, B, C);
+    if (splits < 1 || splits > 65535)
+        return cudaErrorInvalidValue;
+    if (splits == 1)
+        kchunk = K;
+    kernel<<<dim3((unsigned)tiles, (unsigned)splits), kThreads, G::SMEM_BYTES, stream>>>(
+        M, N, K, kchunk, A, B, C, (size_t)M * N);
     return cudaGetLastError();
 }
 
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER>
 cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, float *C,
-                       cudaStream_t stream)
+                       cudaStream_t stream, int splits = 1, int kchunk = 0)
 {
     const bool b_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(B) & 15) == 0);
     const bool c_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
     // Three instantiations: the 4-byte B path (rows not 16-byte aligned) also
     // takes the 4-byte C stores.
     if (b_vec && c_vec)
-        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, true>(M, N, K, A, B, C, stream);
+        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, true>(M, N, K, A, B, C, stream,
+                                                                       splits, kchunk);
     if (b_vec)
-        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, false>(M, N, K, A, B, C, stream);
-    return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, false, false>(M, N, K, A, B, C, stream);
+        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, false>(M, N, K, A, B, C, stream,
+                                                                        splits, kchunk);
+    return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, false, false>(M, N, K, A, B, C, stream,
+                                                                     splits, kchunk);
 }
 
 } // namespace simt
 
+namespace {
+constexpr int kTileM = 128, kTileN = 128, kSliceK = 32;
+
+__global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restrict__ C,
+                                     int64_t count, int splits)
+{
+    // C[i] = W[0][i] + W[1][i] + ... in increasing split order (deterministic).
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
+        float s = W[i];
+        for (int t = 1; t < splits; ++t)
+            s += W[(int64_t)t * count + i];
+        C[i] = s;
+    }
+}
+
+__global__ void splitk_reduce4_kernel(const float4 *__restrict__ W, float4 *__restrict__ C,
+                                      int64_t count4, int splits)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count4; i += stride) {
+        float4 s = W[i];
+        for (int t = 1; t < splits; ++t) {
+            const float4 v = W[(int64_t)t * count4 + i];
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        C[i] = s;
+    }
+}
+} // namespace
+
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
                              cudaStream_t stream)
 {
-    return simt::launch_any<128, 128, 32, 2, 2, 1>(M, N, K, A, B, C, stream);
+    return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
+}
+
+SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count)
+{
+    SplitK p{1, K};
+    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
+    const long long slots = 2LL * sm_count;  // two CTAs per SM
+    if (tiles * 2 > slots)
+        return p;  // at least half the CTA slots busy without splitting
+    int s = (int)((slots + tiles - 1) / tiles);
+    const int max_by_k = K / (4 * kSliceK);  // each split keeps >= 4 slices
+    if (s > max_by_k)
+        s = max_by_k;
+    if (s > 32)
+        s = 32;
+    if (s < 2)
+        return p;
+    int kchunk = (K + s - 1) / s;
+    kchunk = (kchunk + kSliceK - 1) / kSliceK * kSliceK;
+    p.splits = (K + kchunk - 1) / kchunk;
+    p.kchunk = kchunk;
+    if (p.splits < 2)
+        p = SplitK{1, K};
+    return p;
+}
+
+cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
+                                    const SplitK &plan, float *workspace, cudaStream_t stream)
+{
+    cudaError_t e = simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(
+        M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t count = (int64_t)M * N;
+    const bool vec = (count % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(workspace) & 15) == 0);
+    const int64_t items = vec ? count / 4 : count;
+    int64_t blocks = (items + 255) / 256;
+    if (blocks > 4096)
+        blocks = 4096;
+    if (vec)
+        splitk_reduce4_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+            reinterpret_cast<const float4 *>(workspace), reinterpret_cast<float4 *>(C),
+            count / 4, plan.splits);
+    else
+        splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(workspace, C, count,
+                                                                  plan.splits);
+    return cudaGetLastError();
 }
 
 } // namespace rtm

@@ -21,7 +21,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = rtm.header_symbols()
-    assert {"gemm_f32", "gemm_f32_ladder", "gemm_bf16f32", "gemm_get_device_error",
+    assert {"gemm_f32", "gemm_f32_ladder", "gemm_f32_ws", "gemm_f32_workspace_bytes",
+            "gemm_bf16f32", "gemm_get_device_error",
             "gemm_bf16f32_selftest_timeout", "gemm_status_string"} <= set(names)
     for name in names:
         assert hasattr(lib, name), f"{name} declared in gemm.h but not exported"
@@ -86,6 +87,19 @@ def test_ladder_rung_range(lib):
     assert f(4, 8, 8, 8, FAKE, FAKE, FAKE * 4, None) == -1
     assert f(1, -8, 8, 8, FAKE, FAKE, FAKE * 4, None) == -1
     assert f(2, 0, 8, 8, None, None, None, None) == 0
+
+
+def test_workspace_entry_points_host_checks(lib):
+    assert lib.gemm_f32_workspace_bytes(-1, 8, 8) == -1
+    assert lib.gemm_f32_workspace_bytes(8, 8, 1 << 31) == -1
+    assert lib.gemm_f32_workspace_bytes(0, 8, 8) == 0
+    assert lib.gemm_f32_workspace_bytes(8, 8, 0) == 0
+    f = lib.gemm_f32_ws
+    A, B, C, W = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+    assert f(8, 8, 8, A, B, C, W, -4, None) == -1        # negative workspace size
+    assert f(8, 8, 8, A, B, C, None, 64, None) == -1     # size without a buffer
+    assert f(8, 8, 8, A, B, C, W + 2, 64, None) == -2    # misaligned workspace
+    assert f(0, 8, 8, None, None, None, None, 0, None) == 0
 
 
 def test_selftest_limit_range(lib):
