@@ -111,6 +111,30 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K,
                 void *workspace, int64_t workspace_bytes, void *stream);
 
 /*
+ * gemm_f32_noalloc — the gemm_f32_ws product for callers that cannot
+ * allocate device memory: code hosted by an application that owns all device
+ * memory through its own pool and forbids other allocations, and code that
+ * must not be able to fail for lack of memory once loaded. It allocates
+ * nothing: the split-K workspace is a fixed 24 MiB array built into the
+ * library (every GPU that loads the library holds it until the process
+ * exits). The register-tiling pages have no counterpart of this entry point.
+ *
+ * Same arguments, layout, ownership, degenerate-shape and alignment rules as
+ * gemm_f32. Products that need no split run gemm_f32's schedule; products
+ * whose split needs more than 24 MiB (splits * M * N * 4 bytes, see
+ * gemm_f32_workspace_bytes) are rejected with GEMM_ERR_INVALID_ARG.
+ *
+ * The first call on each device looks up the device address of the built-in
+ * array (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture. All calls on a device share the array:
+ * its contents persist between calls, nothing in it needs to start at zero
+ * (a call writes every element it reads), and two calls whose work overlaps
+ * on the GPU (for example on two streams) race on it.
+ */
+int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
+                     const float *A, const float *B, float *C, void *stream);
+
+/*
  * gemm_f32_ladder — the ablation ladder of the register-tiling page: the same
  * fp32 product computed by the kernels the page compares, kept as the page
  * describes them, for measuring what each tiling level buys
