@@ -58,8 +58,9 @@ typedef enum gemm_status {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = -1, /* negative size, null pointer for a non-empty
                                   matrix, C overlapping A or B, size too large */
-    GEMM_ERR_ALIGNMENT = -2,   /* gemm_bf16f32 only: K or N not a multiple of 8,
-                                  or A, B, C not 16-byte aligned */
+    GEMM_ERR_ALIGNMENT = -2,   /* gemm_bf16f32 / gemm_f16f32: K or N not a
+                                  multiple of 8, or A, B, C not 16-byte aligned;
+                                  any entry point: a pointer not 4-byte aligned */
     GEMM_ERR_LAUNCH = -3,      /* a CUDA runtime call failed (no device, launch
                                   error, earlier sticky error) */
     GEMM_ERR_TIMEOUT = -4,     /* reported by gemm_get_device_error: a bounded
@@ -174,6 +175,17 @@ int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  */
 int gemm_bf16f32(int64_t M, int64_t N, int64_t K,
                  const uint16_t *A, const uint16_t *B, float *C, void *stream);
+
+/*
+ * gemm_f16f32 — IEEE half-precision (fp16) inputs, fp32 accumulation and
+ * output, on the same tcgen05 kernel as gemm_bf16f32 with the operands'
+ * format set to fp16: the pages' own worked example is this HGEMM, fp16 in
+ * and fp32 accumulate ("寄存器Tiling跨架构解析", section 6 and 6.1). A and B hold
+ * raw fp16 bit patterns; every rule of gemm_bf16f32 applies (K % 8 == 0,
+ * N % 8 == 0, 16-byte-aligned A, B, C; bounded waits).
+ */
+int gemm_f16f32(int64_t M, int64_t N, int64_t K,
+                const uint16_t *A, const uint16_t *B, float *C, void *stream);
 
 /*
  * gemm_get_device_error — synchronises `stream`, then returns and clears the

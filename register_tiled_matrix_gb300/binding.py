@@ -51,7 +51,7 @@ def load_library() -> ctypes.CDLL:
                 "(nvcc, sm_103a) first; there is no fallback implementation")
         lib = ctypes.CDLL(path)
         i64, p = ctypes.c_int64, ctypes.c_void_p
-        for name in ("gemm_f32", "gemm_bf16f32"):
+        for name in ("gemm_f32", "gemm_bf16f32", "gemm_f16f32"):
             f = getattr(lib, name)
             f.argtypes = [i64, i64, i64, p, p, p, p]
             f.restype = ctypes.c_int
@@ -183,6 +183,18 @@ def gemm_bf16f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] =
     with torch.cuda.device(A.device):
         _check(load_library().gemm_bf16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                            _stream_handle(stream)))
+    return C
+
+
+def gemm_f16f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B on the tcgen05 tensor-core kernel (fp16 in, fp32 accumulate and out)."""
+    C = _prepare(A, B, torch.float16, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        _check(load_library().gemm_f16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                          _stream_handle(stream)))
     return C
 
 

@@ -133,7 +133,7 @@ int finish(cudaError_t e)
 }
 
 int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
-             void *stream, uint64_t wait_limit_ns, int mute_producer)
+             void *stream, uint64_t wait_limit_ns, int mute_producer, int f16 = 0)
 {
     bool nothing = false;
     int st = check_common(M, N, K, A, B, C, 2, &nothing);
@@ -163,6 +163,7 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     L.wait_limit_ns = wait_limit_ns;
     L.mute_producer = mute_producer;
     L.sm_count = d.sms;
+    L.f16 = f16;
     L.encode_tiled = encode_tiled_fn();
     if (!L.encode_tiled)
         return GEMM_ERR_LAUNCH;
@@ -288,6 +289,12 @@ int gemm_bf16f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint1
     return run_bf16(M, N, K, A, B, C, stream, kDefaultWaitLimitNs, 0);
 }
 
+int gemm_f16f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
+                void *stream)
+{
+    return run_bf16(M, N, K, A, B, C, stream, kDefaultWaitLimitNs, 0, 1);
+}
+
 int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K, const uint16_t *A,
                                   const uint16_t *B, float *C, int64_t wait_limit_ns, void *stream)
 {
@@ -326,8 +333,8 @@ const char *gemm_status_string(int status)
     case GEMM_ERR_INVALID_ARG:
         return "GEMM_ERR_INVALID_ARG: negative size, null pointer, overlap or size too large";
     case GEMM_ERR_ALIGNMENT:
-        return "GEMM_ERR_ALIGNMENT: bf16 path needs K % 8 == 0, N % 8 == 0 and 16-byte aligned "
-               "pointers";
+        return "GEMM_ERR_ALIGNMENT: bf16/fp16 path needs K % 8 == 0, N % 8 == 0 and 16-byte "
+               "aligned pointers";
     case GEMM_ERR_LAUNCH:
         return "GEMM_ERR_LAUNCH: a CUDA runtime call failed";
     case GEMM_ERR_TIMEOUT:

@@ -1,4 +1,5 @@
-// bf16 x bf16 -> fp32 product C = A.B on the sm_103a tensor cores (tcgen05).
+// bf16 x bf16 (or fp16 x fp16) -> fp32 product C = A.B on the sm_103a tensor
+// cores (tcgen05, kind::f16; the template argument picks the operand format).
 //
 // The same three tiling levels as the SIMT kernel, mapped onto Blackwell's
 // asynchronous units ("寄存器Tiling跨架构解析", sections 2.1 and 6: on tensor
@@ -35,7 +36,7 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;                 // 64 bf16 = 128 bytes = one swizzle row
+constexpr int BK = 64;                 // 64 16-bit values = 128 bytes = one swizzle row
 constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
@@ -47,15 +48,19 @@ constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;                     // 512: two accumulators
 constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major,
-// B MN-major, N = 256, M = 128.
-constexpr uint32_t IDESC = (1u << 4)                      // D format: f32
-                           | (1u << 7)                    // A format: bf16
-                           | (1u << 10)                   // B format: bf16
-                           | (0u << 15)                   // A major: K
-                           | (1u << 16)                   // B major: MN
-                           | ((uint32_t)(BN >> 3) << 17)  // N / 8
-                           | ((uint32_t)(BM >> 4) << 24); // M / 16
+// Instruction descriptor, kind::f16: D fp32, A and B both bf16 (format 1) or
+// both fp16 (format 0), A K-major, B MN-major, N = 256, M = 128.
+template <bool F16>
+constexpr uint32_t idesc()
+{
+    return (1u << 4)                               // D format: f32
+           | ((F16 ? 0u : 1u) << 7)                // A format
+           | ((F16 ? 0u : 1u) << 10)               // B format
+           | (0u << 15)                            // A major: K
+           | (1u << 16)                            // B major: MN
+           | ((uint32_t)(BN >> 3) << 17)           // N / 8
+           | ((uint32_t)(BM >> 4) << 24);          // M / 16
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle (layout type 2),
 // descriptor version 1. Offsets in bytes.
@@ -90,8 +95,9 @@ __device__ __forceinline__ void give_up(int *err, volatile int *abort)
     *abort = 1;
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -208,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t adesc = sdesc_sw128(sa + kk * UMMA_K * 2, 16, 1024);
                         const uint64_t bdesc =
                             sdesc_sw128(sb + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
-                        umma_f16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16(d_tmem, adesc, bdesc, idesc<F16>(), (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
                     umma_commit(&empty[stage]);  // frees the stage when these MMAs finish
@@ -295,15 +301,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Row-major rows x cols bf16 matrix, box of box_rows x 64 columns, 128 B swizzle.
+// Row-major rows x cols 16-bit matrix (bf16 or fp16), box of box_rows x 64
+// columns, 128 B swizzle.
 static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, uint64_t rows,
-                       uint64_t cols, uint32_t box_rows)
+                       uint64_t cols, uint32_t box_rows, bool f16)
 {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+    CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void *>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -320,27 +328,28 @@ cudaError_t launch_gemm_bf16_tc(const TcLaunch &L, cudaStream_t stream)
     CUtensorMap ta, tb;
     // A: M rows x K cols, boxes of 128 rows (m) x 64 k.
     // B: K rows x N cols, boxes of 64 rows (k) x 64 n.
-    if (!encode_map(fn, &ta, L.A, (uint64_t)L.M, (uint64_t)L.K, BM) ||
-        !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, BK))
+    if (!encode_map(fn, &ta, L.A, (uint64_t)L.M, (uint64_t)L.K, BM, L.f16 != 0) ||
+        !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, BK, L.f16 != 0))
         return cudaErrorInvalidValue;
 
-    static bool attr_done[64] = {};
+    auto kernel = L.f16 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+    static bool attr_done[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (dev < 0 || dev >= 64 || !attr_done[L.f16 != 0][dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
         if (dev >= 0 && dev < 64)
-            attr_done[dev] = true;
+            attr_done[L.f16 != 0][dev] = true;
     }
     const long long ntiles = (long long)((L.M + BM - 1) / BM) * ((L.N + BN - 1) / BN);
     const int grid = (int)(ntiles < L.sm_count ? ntiles : L.sm_count);
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};
-    gemm_bf16_tc_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(ta, tb, p);
+    kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(ta, tb, p);
     return cudaGetLastError();
 }
 

@@ -30,7 +30,7 @@ cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const f
 cudaError_t launch_sgemm_ladder(int rung, int M, int N, int K, const float *A, const float *B,
                                 float *C, cudaStream_t stream);
 
-// tcgen05 bf16 x bf16 -> fp32 product (gemm_tc.cu). K >= 1, K % 8 == 0,
+// tcgen05 bf16 x bf16 (or fp16 x fp16) -> fp32 product (gemm_tc.cu). K >= 1, K % 8 == 0,
 // N % 8 == 0, A/B/C 16-byte aligned. `err` is the device error word;
 // `wait_limit_ns` bounds every wait; `mute_producer` != 0 issues no loads
 // (failure-detection self-test only).
@@ -44,6 +44,7 @@ struct TcLaunch {
     int mute_producer;
     int sm_count;
     void *encode_tiled;  // cuTensorMapEncodeTiled driver entry point
+    int f16;             // 0: A and B are bf16; 1: A and B are fp16
 };
 cudaError_t launch_gemm_bf16_tc(const TcLaunch &p, cudaStream_t stream);
 

@@ -22,7 +22,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = rtm.header_symbols()
     assert {"gemm_f32", "gemm_f32_ladder", "gemm_f32_ws", "gemm_f32_workspace_bytes",
-            "gemm_bf16f32", "gemm_get_device_error",
+            "gemm_f32_noalloc", "gemm_bf16f32", "gemm_f16f32", "gemm_get_device_error",
             "gemm_bf16f32_selftest_timeout", "gemm_status_string"} <= set(names)
     for name in names:
         assert hasattr(lib, name), f"{name} declared in gemm.h but not exported"
@@ -34,7 +34,7 @@ def test_status_strings(lib):
     assert rtm.status_string(12345) == "unknown gemm status"
 
 
-@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32"])
+@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32", "gemm_f16f32"])
 def test_invalid_sizes(lib, fn):
     f = getattr(lib, fn)
     assert f(-1, 4, 4, FAKE, FAKE, FAKE * 2, None) == -1
@@ -43,14 +43,14 @@ def test_invalid_sizes(lib, fn):
     assert f(1 << 31, 8, 8, FAKE, FAKE, FAKE * 2, None) == -1
 
 
-@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32"])
+@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32", "gemm_f16f32"])
 def test_empty_output_is_a_noop(lib, fn):
     f = getattr(lib, fn)
     assert f(0, 16, 16, None, None, None, None) == 0
     assert f(16, 0, 16, None, None, None, None) == 0
 
 
-@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32"])
+@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16f32", "gemm_f16f32"])
 def test_null_pointers(lib, fn):
     f = getattr(lib, fn)
     assert f(8, 8, 8, FAKE, FAKE, None, None) == -1
@@ -67,8 +67,9 @@ def test_output_overlapping_input_rejected(lib, fn, elem):
     assert f(M, N, K, base, base + (1 << 20), base + (1 << 20) + 16, None) == -1  # C over B
 
 
-def test_bf16_alignment_rules(lib):
-    f = lib.gemm_bf16f32
+@pytest.mark.parametrize("fn", ["gemm_bf16f32", "gemm_f16f32"])
+def test_tensor_core_alignment_rules(lib, fn):
+    f = getattr(lib, fn)
     A, B, C = 0x10000000, 0x20000000, 0x30000000
     assert f(16, 16, 12, A, B, C, None) == -2      # K % 8
     assert f(16, 12, 16, A, B, C, None) == -2      # N % 8

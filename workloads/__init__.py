@@ -88,8 +88,8 @@ def make_inputs(M: int, N: int, K: int, dist: str = "uniform", dtype: str = "f32
                 seed: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
     """Return (A, B): A is M x K, B is K x N, contiguous CPU tensors.
 
-    dtype "f32" gives torch.float32; "bf16" gives torch.bfloat16 (the fp32
-    draw rounded to nearest even).
+    dtype "f32" gives torch.float32; "bf16" gives torch.bfloat16 and "f16"
+    torch.float16 (the fp32 draw rounded to nearest even).
     """
     gen = torch.Generator(device="cpu")
     gen.manual_seed(int(seed))
@@ -98,6 +98,9 @@ def make_inputs(M: int, N: int, K: int, dist: str = "uniform", dtype: str = "f32
     if dtype == "bf16":
         A = A.to(torch.bfloat16)
         B = B.to(torch.bfloat16)
+    elif dtype == "f16":
+        A = A.to(torch.float16)
+        B = B.to(torch.float16)
     elif dtype != "f32":
         raise ValueError(f"unknown dtype {dtype!r}")
     return A.contiguous(), B.contiguous()
