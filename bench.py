@@ -57,13 +57,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     "gemm_f32": {"bytes": 394298368, "source_sha1": "95ed9c3bc1204705753ae5096927587ab0cd17c0",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
-    "gemm_bf16f32": {"bytes": 1254241320,
-                     "source_sha1": "88f1f62840bb10818b39aa356f0738dbb650f6d5",
+    "gemm_bf16f32": {"bytes": 1331420160,
+                     "source_sha1": "a4ed42f2398c43699e598ea69aeef18e93850028",
                      "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {
     "gemm_f32": "register_tiled_matrix_gb300/csrc/sgemm_simt.cu",
-    "gemm_bf16f32": "register_tiled_matrix_gb300/csrc/gemm_tc.cu",
+    "gemm_bf16f32": "register_tiled_matrix_gb300/csrc/gemm_tc2.cu",  # M > 128: CTA pairs
 }
 
 

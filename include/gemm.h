@@ -161,7 +161,10 @@ int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * gemm_bf16f32 — bfloat16 inputs, fp32 accumulation and output, on the
  * tcgen05 tensor cores: operands staged in shared memory by TMA, the
  * accumulator tile held in tensor memory (the tensor-core form of the
- * register tile; "寄存器Tiling跨架构解析", sections 2.1 and 6).
+ * register tile; "寄存器Tiling跨架构解析", sections 2.1 and 6). For M > 128 a
+ * cluster of two CTAs computes each 256 x 256 tile with the two-SM MMA
+ * (each SM stages half of A and half of B); for M <= 128 one CTA per
+ * 128 x 256 tile.
  *
  * A and B hold raw bfloat16 bit patterns (uint16_t). Requirements beyond the
  * common ones: K % 8 == 0 and N % 8 == 0 (each row must start on a 16-byte

@@ -167,7 +167,8 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     L.encode_tiled = encode_tiled_fn();
     if (!L.encode_tiled)
         return GEMM_ERR_LAUNCH;
-    return finish(rtm::launch_gemm_bf16_tc(L, s));
+    // CTA pairs (256-row tiles) unless M fits one 128-row tile.
+    return finish(M > 128 ? rtm::launch_gemm_tc_pair(L, s) : rtm::launch_gemm_bf16_tc(L, s));
 }
 
 } // namespace

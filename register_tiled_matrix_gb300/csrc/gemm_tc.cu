@@ -51,7 +51,7 @@ constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barr
 // Instruction descriptor, kind::f16: D fp32, A and B both bf16 (format 1) or
 // both fp16 (format 0), A K-major, B MN-major, N = 256, M = 128.
 template <bool F16>
-constexpr uint32_t idesc()
+__host__ __device__ constexpr uint32_t idesc()
 {
     return (1u << 4)                               // D format: f32
            | ((F16 ? 0u : 1u) << 7)                // A format

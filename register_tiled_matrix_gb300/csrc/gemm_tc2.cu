@@ -1,0 +1,377 @@
+// bf16 x bf16 (or fp16 x fp16) -> fp32 product C = A.B on CTA pairs: the
+// two-SM form of tcgen05 (cta_group::2) on sm_103a.
+//
+// Same tiling levels as gemm_tc.cu ("寄存器Tiling跨架构解析", sections 2.1 and
+// 6: on tensor cores the register tile becomes the matrix instruction's
+// accumulator), with one change that matters on Blackwell: a cluster of two
+// CTAs on the two SMs of a pair computes a 256 x 256 C tile with one MMA
+// instruction stream. Each CTA stages only its own half of the operands —
+// 128 rows of A and 128 columns of B per 64-deep K-slice, 32 KB instead of
+// the 48 KB a lone 128 x 256 tile needs — so the bytes every SM must pull
+// from L2 per tensor-core cycle fall by a third, while each SM still keeps a
+// 128 x 256 fp32 accumulator in its own tensor memory.
+//
+//  * global tiling — persistent clusters walk 256 x 256 tiles in groups of
+//    GROUP_M tile-rows (L2 reuse);
+//  * shared tiling — in each CTA one thread issues the TMA boxes of its
+//    halves into a 6-stage ring; the copies of both CTAs signal one mbarrier
+//    in the even CTA, which expects the pair's 64 KB per stage;
+//  * accumulator tiling — one thread of the even CTA issues
+//    tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): rows 0-127 land in
+//    the even CTA's tensor memory, rows 128-255 in the odd CTA's; completions
+//    are multicast to the stage and accumulator barriers of both CTAs;
+//    accumulators are double-buffered (2 x 256 columns);
+//  * epilogue — in each CTA four warps read their CTA's accumulator rows
+//    with tcgen05.ld and store them; the eight epilogue warps of the pair hand
+//    the accumulator back to the even CTA.
+//
+// Every mbarrier wait is bounded in time (see gemm_tc.cu); the cluster
+// barriers at start and end are reached on every path.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace rtm {
+namespace tc2 {
+
+constexpr int PM = 256;            // pair tile rows (128 per CTA)
+constexpr int PN = 256;            // pair tile columns
+constexpr int HM = 128;            // A rows staged per CTA
+constexpr int HN = 128;            // B columns staged per CTA
+constexpr int BK = 64;             // 64 16-bit values = one 128-byte swizzle row
+constexpr int STAGES = 6;
+constexpr int UMMA_K = 16;
+constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA (even CTA), warps 2-5 epilogue
+constexpr int kGroupM = 8;
+constexpr uint32_t A_BYTES = HM * BK * 2;          // 16 KB
+constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;     // 8 KB: 64 k-rows x 64 columns
+constexpr uint32_t B_BYTES = BK * HN * 2;          // 16 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * PN;             // 512: two accumulators
+constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint16_t kBothCtas = 0x3;
+constexpr uint16_t kEvenCta = 0x1;
+
+// kind::f16 instruction descriptor for the pair: D fp32, A/B bf16 (1) or fp16
+// (0), A K-major, B MN-major, N = 256, M = 256.
+template <bool F16>
+__host__ __device__ constexpr uint32_t idesc()
+{
+    return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) | (0u << 15) |
+           (1u << 16) | ((uint32_t)(PN >> 3) << 17) | ((uint32_t)(PM >> 4) << 24);
+}
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+struct Params {
+    int M, N, K;
+    float *C;
+    int *err;
+    unsigned long long limit_ns;
+    int mute_producer;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &n0)
+{
+    const int group_size = kGroupM * tiles_n;
+    const int group = t / group_size;
+    const int first_m = group * kGroupM;
+    const int rows = min(tiles_m - first_m, kGroupM);
+    const int in_group = t - group * group_size;
+    m0 = (first_m + in_group % rows) * PM;
+    n0 = (in_group / rows) * PN;
+}
+
+__device__ __forceinline__ void give_up(int *err, volatile int *abort)
+{
+    atomicCAS(err, 0, kDevErrTimeout);
+    *abort = 1;
+}
+
+template <bool F16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: the even CTA, which issues the MMAs
+    const bool even = rank == 0;
+    const int cluster_id = blockIdx.x >> 1;
+    const int num_clusters = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);   // even CTA: its producer's expect_tx arrival
+            mbar_init(&empty[s], 1);  // one multicast commit per stage use
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);  // even CTA: the pair's eight epilogue warps
+        }
+        mbar_init(drain, 1);
+        *abort = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised before any remote signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int tiles_m = (p.M + PM - 1) / PM;
+    const int tiles_n = (p.N + PN - 1) / PN;
+    const int ntiles = tiles_m * tiles_n;
+    const int kblocks = (p.K + BK - 1) / BK;
+    const uint64_t limit = p.limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0 && !p.mute_producer) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued = 0, issued_parity = 0;
+            for (int t = cluster_id; t < ntiles && !*abort; t += num_clusters) {
+                int m0, n0;
+                tile_coords(t, tiles_m, tiles_n, m0, n0);
+                const int row0 = m0 + (int)rank * HM;
+                const int col0 = n0 + (int)rank * HN;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1, limit, abort)) {
+                        give_up(p.err, abort);
+                        break;
+                    }
+                    if (even)
+                        mbar_arrive_expect_tx(&full[stage], PAIR_STAGE_BYTES);
+                    const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    tma_load_2d_pair(sa, &tmA, fb, kb * BK, row0);
+                    tma_load_2d_pair(sb, &tmB, fb, col0, kb * BK);
+                    tma_load_2d_pair(sb + B_ATOM_BYTES, &tmB, fb, col0 + 64, kb * BK);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // No copy into this CTA's shared memory may outlive the pair.
+            if (even) {
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued & (1u << s)) {
+                        volatile int no_abort = 0;
+                        mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, limit, &no_abort);
+                    }
+            } else if (issued && *abort) {
+                // The odd CTA's copies signal the even CTA's barriers; on the
+                // abort path give them time to land before leaving.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        if (even && lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t acc = 0, acc_phase = 0;
+            bool issued_any = false;
+            for (int t = cluster_id; t < ntiles && !*abort; t += num_clusters) {
+                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, limit, abort)) {
+                    give_up(p.err, abort);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * PN;
+                bool ok = true;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, limit, abort)) {
+                        give_up(p.err, abort);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t adesc = sdesc_sw128(sa + kk * UMMA_K * 2, 16, 1024);
+                        const uint64_t bdesc =
+                            sdesc_sw128(sb + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
+                        umma_f16_pair(d_tmem, adesc, bdesc, idesc<F16>(), (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    umma_commit_pair_multicast(&empty[stage], kBothCtas);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit_pair_multicast(&tfull[acc], kBothCtas);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            if (issued_any) {
+                umma_commit_pair_multicast(drain, kEvenCta);
+                volatile int no_abort = 0;
+                mbar_wait_bounded(drain, 0, limit, &no_abort);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int quarter = warp & 3;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int t = cluster_id; t < ntiles && !*abort; t += num_clusters) {
+            int m0, n0;
+            tile_coords(t, tiles_m, tiles_n, m0, n0);
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, limit, abort)) {
+                give_up(p.err, abort);
+                break;
+            }
+            tc_fence_after();
+            const int row = m0 + (int)rank * HM + quarter * 32 + lane;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * PN;
+            float *crow = p.C + (size_t)row * p.N;
+#pragma unroll 1
+            for (int c = 0; c < PN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                tmem_wait_ld();
+                if (c == PN / 32 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+                }
+                if (row < p.M) {
+                    const int col = n0 + c * 32;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        if (col + v * 4 < p.N) {
+                            float4 o;
+                            o.x = __uint_as_float(r[v * 4 + 0]);
+                            o.y = __uint_as_float(r[v * 4 + 1]);
+                            o.z = __uint_as_float(r[v * 4 + 2]);
+                            o.w = __uint_as_float(r[v * 4 + 3]);
+                            *reinterpret_cast<float4 *>(crow + col + v * 4) = o;
+                        }
+                    }
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still signal or read it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, uint64_t rows,
+                       uint64_t cols, uint32_t box_rows, bool f16)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+} // namespace tc2
+
+cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
+{
+    using namespace tc2;
+    auto fn = reinterpret_cast<EncodeTiledFn>(L.encode_tiled);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    CUtensorMap ta, tb;
+    // A: M x K, boxes of 128 rows x 64 k; B: K x N, boxes of 64 k-rows x 64 n.
+    if (!encode_map(fn, &ta, L.A, (uint64_t)L.M, (uint64_t)L.K, HM, L.f16 != 0) ||
+        !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, BK, L.f16 != 0))
+        return cudaErrorInvalidValue;
+    auto kernel = L.f16 ? gemm_tc2_kernel<true> : gemm_tc2_kernel<false>;
+    static bool attr_done[2][64] = {};
+    static int max_clusters[2][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const int fi = L.f16 != 0;
+    if (dev < 0 || dev >= 64 || !attr_done[fi][dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        // How many pairs can be resident at once (persistent grid size).
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (L.sm_count / 2), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = L.sm_count / 2;
+        }
+        if (dev >= 0 && dev < 64) {
+            max_clusters[fi][dev] = n;
+            attr_done[fi][dev] = true;
+        }
+    }
+    const int clusters_max = (dev >= 0 && dev < 64) ? max_clusters[fi][dev] : L.sm_count / 2;
+    const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
+    const int clusters = (int)(ntiles < clusters_max ? ntiles : clusters_max);
+    Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};
+    kernel<<<2 * clusters, kThreads, SMEM_BYTES, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+} // namespace rtm

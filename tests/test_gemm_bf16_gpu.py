@@ -119,15 +119,25 @@ def test_repeated_calls_identical():
     assert torch.equal(C1, C2)
 
 
-def test_bounded_wait_gives_up_and_context_survives():
+@pytest.mark.parametrize("M", [256, 128], ids=["cta_pair", "single_cta"])
+def test_bounded_wait_gives_up_and_context_survives(M):
     """With the loads muted, every wait runs out after 50 ms; the kernel records
-    a timeout and returns, and the next product on the same context is correct."""
-    A, B = bf16_inputs(256, 512, 256, seed=45)
+    a timeout and returns, and the next product on the same context is correct.
+    M = 256 runs the CTA-pair kernel, M = 128 the single-CTA kernel."""
+    A, B = bf16_inputs(M, 512, 256, seed=45)
     Ad, Bd = A.to(DEV), B.to(DEV)
-    C = torch.empty(256, 512, device=DEV)
+    C = torch.empty(M, 512, device=DEV)
     assert rtm.get_device_error() == 0
     rtm.gemm_bf16f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
     assert rtm.get_device_error() == -4
     assert rtm.get_device_error() == 0, "reading the error word clears it"
     C = run(A, B)
     assert_close_to_oracle(C, A, B, "bf16")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 1024, 512), (100, 264, 1000), (129, 256, 64),
+                                   (257, 520, 128)])
+def test_single_cta_and_pair_boundary(M, N, K):
+    """M <= 128 runs the single-CTA kernel, M > 128 the CTA pair: both near the switch."""
+    A, B = bf16_inputs(M, N, K, seed=M * N)
+    assert_close_to_oracle(run(A, B), A, B, "bf16")
