@@ -58,9 +58,8 @@ typedef enum gemm_status {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = -1, /* negative size, null pointer for a non-empty
                                   matrix, C overlapping A or B, size too large */
-    GEMM_ERR_ALIGNMENT = -2,   /* gemm_bf16f32 / gemm_f16f32: K or N not a
-                                  multiple of 8, or A, B, C not 16-byte aligned;
-                                  any entry point: a pointer not 4-byte aligned */
+    GEMM_ERR_ALIGNMENT = -2,   /* a pointer not aligned to its element size
+                                  (fp32: 4 bytes, bf16/fp16: 2 bytes; C: 4) */
     GEMM_ERR_LAUNCH = -3,      /* a CUDA runtime call failed (no device, launch
                                   error, earlier sticky error) */
     GEMM_ERR_TIMEOUT = -4,     /* reported by gemm_get_device_error: a bounded
@@ -166,11 +165,13 @@ int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * (each SM stages half of A and half of B); for M <= 128 one CTA per
  * 128 x 256 tile.
  *
- * A and B hold raw bfloat16 bit patterns (uint16_t). Requirements beyond the
- * common ones: K % 8 == 0 and N % 8 == 0 (each row must start on a 16-byte
- * boundary for the tensor-memory-access unit), and A, B, C 16-byte aligned;
- * otherwise GEMM_ERR_ALIGNMENT. M is unrestricted. Ragged M, N and K tiles
- * are handled by zero-filled loads and masked stores.
+ * A and B hold raw bfloat16 bit patterns (uint16_t), 2-byte aligned; C is
+ * 4-byte aligned (else GEMM_ERR_ALIGNMENT). Any M, N, K. When every row starts
+ * on a 16-byte boundary (K % 8 == 0, N % 8 == 0, A, B, C 16-byte aligned) the
+ * operands are staged by the tensor-memory-access unit; otherwise by producer
+ * warps that load them element by element into the same swizzled layout
+ * (slower, same arithmetic). Ragged M, N and K tiles are handled by
+ * zero-filled loads and masked stores.
  *
  * Every wait inside the kernel is bounded (a few seconds); if one gives up
  * the kernel records GEMM_ERR_TIMEOUT in the device error word and returns
@@ -184,8 +185,8 @@ int gemm_bf16f32(int64_t M, int64_t N, int64_t K,
  * output, on the same tcgen05 kernel as gemm_bf16f32 with the operands'
  * format set to fp16: the pages' own worked example is this HGEMM, fp16 in
  * and fp32 accumulate ("寄存器Tiling跨架构解析", section 6 and 6.1). A and B hold
- * raw fp16 bit patterns; every rule of gemm_bf16f32 applies (K % 8 == 0,
- * N % 8 == 0, 16-byte-aligned A, B, C; bounded waits).
+ * raw fp16 bit patterns; every rule of gemm_bf16f32 applies (alignment,
+ * the two staging paths, bounded waits).
  */
 int gemm_f16f32(int64_t M, int64_t N, int64_t K,
                 const uint16_t *A, const uint16_t *B, float *C, void *stream);
@@ -200,13 +201,15 @@ int gemm_get_device_error(void *stream);
 
 /*
  * gemm_bf16f32_selftest_timeout — failure-detection check for the bounded
- * waits. Launches the gemm_bf16f32 kernel on the given buffers with its
- * tensor-memory-access producer muted, so that nothing ever arrives on the
- * stage barriers, and with every wait limited to `wait_limit_ns`. Each
- * waiting warp gives up, the kernel frees its tensor memory, records
- * GEMM_ERR_TIMEOUT in the device error word and returns; the GPU context
- * stays usable. C is left unspecified. Same argument rules as gemm_bf16f32;
- * wait_limit_ns must be in [1e6, 1e10].
+ * waits. Launches the gemm_bf16f32 TMA kernel the shape selects (CTA pair for
+ * M > 128, single CTA otherwise) on the given buffers with its tensor-memory-
+ * access producer muted, so that nothing ever arrives on the stage barriers,
+ * and with every wait limited to `wait_limit_ns`. Each waiting warp gives up,
+ * the kernel frees its tensor memory, records GEMM_ERR_TIMEOUT in the device
+ * error word and returns; the GPU context stays usable. C is left
+ * unspecified. Same argument rules as gemm_bf16f32, and the shape must take
+ * the TMA path (K % 8 == 0, N % 8 == 0, 16-byte-aligned pointers) else
+ * GEMM_ERR_INVALID_ARG; wait_limit_ns must be in [1e6, 1e10].
  */
 int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K,
                                   const uint16_t *A, const uint16_t *B, float *C,

@@ -139,12 +139,17 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     int st = check_common(M, N, K, A, B, C, 2, &nothing);
     if (st != GEMM_OK || nothing)
         return st;
-    if (K % 8 != 0 || N % 8 != 0)
+    if ((reinterpret_cast<uintptr_t>(C) & 3) != 0 ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 1) != 0 ||
+                   (reinterpret_cast<uintptr_t>(B) & 1) != 0)))
         return GEMM_ERR_ALIGNMENT;
-    if ((reinterpret_cast<uintptr_t>(C) & 15) != 0 ||
-        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15) != 0 ||
-                   (reinterpret_cast<uintptr_t>(B) & 15) != 0)))
-        return GEMM_ERR_ALIGNMENT;
+    // Rows on 16-byte boundaries (the TMA stride rule) take the TMA kernels;
+    // anything else the kernel with load-and-swizzle producer warps.
+    const bool tma_ok = K % 8 == 0 && N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(A) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(B) & 15) == 0;
+    if (mute_producer && !tma_ok)
+        return GEMM_ERR_INVALID_ARG;  // the self-test exercises the TMA kernels
     DeviceInfo d;
     st = current_device(&d);
     if (st != GEMM_OK)
@@ -167,6 +172,8 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     L.encode_tiled = encode_tiled_fn();
     if (!L.encode_tiled)
         return GEMM_ERR_LAUNCH;
+    if (!tma_ok)
+        return finish(rtm::launch_gemm_tc_any(L, s));
     // CTA pairs (256-row tiles) unless M fits one 128-row tile.
     return finish(M > 128 ? rtm::launch_gemm_tc_pair(L, s) : rtm::launch_gemm_bf16_tc(L, s));
 }
@@ -334,8 +341,8 @@ const char *gemm_status_string(int status)
     case GEMM_ERR_INVALID_ARG:
         return "GEMM_ERR_INVALID_ARG: negative size, null pointer, overlap or size too large";
     case GEMM_ERR_ALIGNMENT:
-        return "GEMM_ERR_ALIGNMENT: bf16/fp16 path needs K % 8 == 0, N % 8 == 0 and 16-byte "
-               "aligned pointers";
+        return "GEMM_ERR_ALIGNMENT: a pointer is not aligned to its element size (C: 4 bytes, "
+               "bf16/fp16 A and B: 2 bytes, fp32 A and B: 4 bytes)";
     case GEMM_ERR_LAUNCH:
         return "GEMM_ERR_LAUNCH: a CUDA runtime call failed";
     case GEMM_ERR_TIMEOUT:

@@ -50,6 +50,9 @@ cudaError_t launch_gemm_bf16_tc(const TcLaunch &p, cudaStream_t stream);
 // The same product on CTA pairs (gemm_tc2.cu, tcgen05 cta_group::2, 256 x 256
 // tiles); used for M > 128, where a pair tile is not mostly empty.
 cudaError_t launch_gemm_tc_pair(const TcLaunch &p, cudaStream_t stream);
+// The same product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu):
+// operands loaded by producer warps instead of TMA. mute_producer unused.
+cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);
 
 // C[0 .. count) = 0 (the K == 0 product).
 cudaError_t launch_zero_fill(float *C, int64_t count, cudaStream_t stream);

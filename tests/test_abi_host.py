@@ -69,13 +69,19 @@ def test_output_overlapping_input_rejected(lib, fn, elem):
 
 @pytest.mark.parametrize("fn", ["gemm_bf16f32", "gemm_f16f32"])
 def test_tensor_core_alignment_rules(lib, fn):
+    """Only pointers off their element size are rejected on the host: any K, N
+    and 2-byte-aligned operands are served (by the load-and-swizzle kernel)."""
     f = getattr(lib, fn)
     A, B, C = 0x10000000, 0x20000000, 0x30000000
-    assert f(16, 16, 12, A, B, C, None) == -2      # K % 8
-    assert f(16, 12, 16, A, B, C, None) == -2      # N % 8
-    assert f(16, 16, 16, A + 2, B, C, None) == -2  # A not 16-byte aligned
-    assert f(16, 16, 16, A, B + 8, C, None) == -2
-    assert f(16, 16, 16, A, B, C + 4, None) == -2
+    assert f(16, 16, 16, A + 1, B, C, None) == -2  # A not 2-byte aligned
+    assert f(16, 16, 16, A, B + 3, C, None) == -2
+    assert f(16, 16, 16, A, B, C + 2, None) == -2  # C not 4-byte aligned
+
+
+def test_selftest_needs_tma_shape(lib):
+    f = lib.gemm_bf16f32_selftest_timeout
+    A, B, C = 0x10000000, 0x20000000, 0x30000000
+    assert f(16, 16, 12, A, B, C, 10 ** 8, None) == -1  # K % 8: not a TMA shape
 
 
 def test_f32_alignment_rule(lib):

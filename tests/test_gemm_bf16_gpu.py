@@ -102,12 +102,48 @@ def test_k_zero_writes_zeros():
     assert torch.count_nonzero(C).item() == 0
 
 
-def test_alignment_errors_raise():
-    A = torch.zeros(16, 12, dtype=torch.bfloat16, device=DEV)
-    B = torch.zeros(12, 16, dtype=torch.bfloat16, device=DEV)
-    with pytest.raises(rtm.GemmError) as e:
-        rtm.gemm_bf16f32(A, B)
-    assert e.value.status == -2
+@pytest.mark.parametrize("M,N,K", [(16, 16, 12), (300, 129, 77), (1, 1, 1), (257, 260, 1000),
+                                   (1000, 1000, 999), (130, 257, 65), (4097, 3001, 1023)])
+def test_unaligned_shapes_parity(M, N, K):
+    """K or N not a multiple of 8: the load-and-swizzle kernel."""
+    A, B = bf16_inputs(M, N, K, seed=M + 7 * N + K)
+    full = M * N * K <= (1 << 31)
+    assert_close_to_oracle(run(A, B), A, B, "bf16", full=full, seed=K)
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 33, 1001), (64, 255, 63)])
+def test_unaligned_small_integer_bit_exact(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "int", "f32", seed=M + N + K)
+    C = run(A.to(torch.bfloat16), B.to(torch.bfloat16))
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_offset_pointers_take_the_load_path():
+    """A, B, C at 2/2/4-byte offsets (rows aligned, bases not): correct results."""
+    M, N, K = 200, 264, 136
+    A, B = bf16_inputs(M, N, K, seed=46)
+    Ab = torch.zeros(M * K + 1, dtype=torch.bfloat16, device=DEV)
+    Bb = torch.zeros(K * N + 1, dtype=torch.bfloat16, device=DEV)
+    Cb = torch.full((M * N + 1,), float("nan"), device=DEV)
+    Ab[1:] = A.flatten().to(DEV)
+    Bb[1:] = B.flatten().to(DEV)
+    lib = rtm.load_library()
+    st = lib.gemm_bf16f32(M, N, K, Ab.data_ptr() + 2, Bb.data_ptr() + 2, Cb.data_ptr() + 4,
+                          torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(Cb[1:].view(M, N), A, B, "bf16")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 130, 90), (120, 100, 33)])
+def test_unaligned_guard_band(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=47)
+    buf, C = guarded_output(M, N, DEV, pad=4096)
+    rtm.gemm_bf16f32(A.to(DEV), B.to(DEV), out=C)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N)
+    assert_close_to_oracle(C, A, B, "bf16")
 
 
 def test_repeated_calls_identical():

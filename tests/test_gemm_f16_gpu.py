@@ -26,7 +26,8 @@ def run(A, B):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (1024, 1024, 1024), (1000, 1000, 1000),
-                                   (129, 264, 72), (1, 8, 8), (2048, 4096, 512)])
+                                   (129, 264, 72), (1, 8, 8), (2048, 4096, 512),
+                                   (300, 129, 77), (1000, 999, 1001)])
 def test_parity_shapes(M, N, K):
     A, B = workloads.make_inputs(M, N, K, "normal", "f16", seed=M + N + K)
     full = M * N * K <= (1 << 31)
