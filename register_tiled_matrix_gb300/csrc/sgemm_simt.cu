@@ -87,20 +87,26 @@ __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n,
 // ORDER 0: accumulator tile walked row by row; 1: serpentine (odd rows walk
 // the columns backwards, so the B operand of a row's last FFMA is the first of
 // the next row's and can be reused by the operand cache).
-template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC>
+template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC,
+          bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MINB)
     sgemm_rt_kernel(int M, int N, int K_total, int kchunk, const float *__restrict__ A,
                     const float *__restrict__ B, float *__restrict__ C, size_t c_split_stride)
 {
-    // Split-K: CTA row blockIdx.y of the grid sums k in [y * kchunk, +kchunk)
-    // and writes its partial tile to C + y * c_split_stride (one split: the
-    // whole of K straight into C). A keeps its full row stride K_total.
-    const int lda = K_total;
-    const int k_begin = blockIdx.y * kchunk;
-    const int K = min(kchunk, K_total - k_begin);
-    A += k_begin;
-    B += (size_t)k_begin * N;
-    C += blockIdx.y * c_split_stride;
+    // Split-K (SPLIT): CTA row blockIdx.y of the grid sums k in
+    // [y * kchunk, +kchunk) and writes its partial tile to C + y * c_split_stride;
+    // A keeps its full row stride K_total. Without SPLIT the kernel is the plain
+    // product, compiled without any of this (the extra runtime offsets changed
+    // the register allocation of the FFMA loop and cost 6 % on GB300).
+    int lda = K_total;
+    int K = K_total;
+    if constexpr (SPLIT) {
+        const int k_begin = blockIdx.y * kchunk;
+        K = min(kchunk, K_total - k_begin);
+        A += k_begin;
+        B += (size_t)k_begin * N;
+        C += blockIdx.y * c_split_stride;
+    }
 
     using G = Cfg<BM, BN, BK, STAGES>;
     constexpr int TM = G::TM, TN = G::TN, QM = G::QM, QN = G::QN;
@@ -308,12 +314,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
 }
 
-template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC>
+template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC,
+          bool SPLIT>
 cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, float *C,
                        cudaStream_t stream, int splits = 1, int kchunk = 0)
 {
     using G = Cfg<BM, BN, BK, STAGES>;
-    auto kernel = sgemm_rt_kernel<BM, BN, BK, STAGES, MINB, ORDER, B_VEC, C_VEC>;
+    auto kernel = sgemm_rt_kernel<BM, BN, BK, STAGES, MINB, ORDER, B_VEC, C_VEC, SPLIT>;
     if (G::SMEM_BYTES > 48 * 1024) {
         // Once per device and instantiation.
         static bool done[64] = {};
@@ -333,7 +340,7 @@ cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, floa
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     if (tiles > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    if (splits < 1 || splits > 65535)
+    if (splits < 1 || splits > 65535 || (!SPLIT && splits != 1))
         return cudaErrorInvalidValue;
     if (splits == 1)
         kchunk = K;
@@ -342,7 +349,7 @@ cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, floa
     return cudaGetLastError();
 }
 
-template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER>
+template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool SPLIT = false>
 cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, float *C,
                        cudaStream_t stream, int splits = 1, int kchunk = 0)
 {
@@ -351,13 +358,13 @@ cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, floa
     // Three instantiations: the 4-byte B path (rows not 16-byte aligned) also
     // takes the 4-byte C stores.
     if (b_vec && c_vec)
-        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, true>(M, N, K, A, B, C, stream,
-                                                                       splits, kchunk);
+        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, true, SPLIT>(
+            M, N, K, A, B, C, stream, splits, kchunk);
     if (b_vec)
-        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, false>(M, N, K, A, B, C, stream,
-                                                                        splits, kchunk);
-    return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, false, false>(M, N, K, A, B, C, stream,
-                                                                     splits, kchunk);
+        return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, false, SPLIT>(
+            M, N, K, A, B, C, stream, splits, kchunk);
+    return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, false, false, SPLIT>(
+        M, N, K, A, B, C, stream, splits, kchunk);
 }
 
 } // namespace simt
@@ -429,7 +436,7 @@ SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count)
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
                                     const SplitK &plan, float *workspace, cudaStream_t stream)
 {
-    cudaError_t e = simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(
+    cudaError_t e = simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, true>(
         M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
     if (e != cudaSuccess)
         return e;
