@@ -86,8 +86,7 @@ __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n,
 
 // ORDER 0: accumulator tile walked row by row; 1: serpentine (odd rows walk
 // the columns backwards, so the B operand of a row's last FFMA is the first of
-// the next row's and can be reused by the operand cache); 2: serpentine by
-// columns; 3: row pairs (each B value feeds two rows back to back).
+// the next row's and can be reused by the operand cache).
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC,
           bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MINB)
@@ -272,34 +271,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 b[p * 4 + 2] = v.z;
                 b[p * 4 + 3] = v.w;
             }
-            if constexpr (ORDER <= 1) {
 #pragma unroll
-                for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < TM; ++i)
 #pragma unroll
-                    for (int jj = 0; jj < TN; ++jj) {
-                        const int j = (ORDER == 1 && (i & 1)) ? TN - 1 - jj : jj;
-                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                    }
-            } else if constexpr (ORDER == 2) {
-                // column-serpentine: b[j] shared along a column walk
-#pragma unroll
-                for (int j = 0; j < TN; ++j)
-#pragma unroll
-                    for (int ii = 0; ii < TM; ++ii) {
-                        const int i = (j & 1) ? TM - 1 - ii : ii;
-                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                    }
-            } else {
-                // row pairs: each b[j] feeds rows i and i+1 back to back
-#pragma unroll
-                for (int i = 0; i < TM; i += 2)
-#pragma unroll
-                    for (int jj = 0; jj < TN; ++jj) {
-                        const int j = ((i >> 1) & 1) ? TN - 1 - jj : jj;
-                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                        acc[i + 1][j] = fmaf(a[i + 1], b[j], acc[i + 1][j]);
-                    }
-            }
+                for (int jj = 0; jj < TN; ++jj) {
+                    const int j = (ORDER == 1 && (i & 1)) ? TN - 1 - jj : jj;
+                    acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                }
 #pragma unroll
             for (int q = 0; q < G::COPIES_PER_K; ++q)
                 if (fast && k * G::COPIES_PER_K + q < FAST_COPIES)
