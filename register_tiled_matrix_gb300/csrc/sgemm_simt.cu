@@ -31,6 +31,7 @@
 //    order (odd rows backwards), so consecutive FFMA always share an operand
 //    and the hardware operand-reuse cache can serve it (measured: +4 % over
 //    row-by-row order on GB300);
+//  * products with N <= 64 use 128 x 64 tiles (8 x 4 per thread);
 //  * BK = 32 with two stages (66.6 KB of shared memory per CTA): a sweep of
 //    BK in {8..48} and 2-4 stages on GB300 put this on top (59 TFLOP/s at
 //    4096^3 against 56 for three stages);
@@ -155,7 +156,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // B loader, 16-byte path: copy i moves B[k0 + 8i + warp][n0 + 4 lane .. +3]
     // (a warp reads one 512-byte row run). 4-byte path: copy i moves
     // B[k0 + 2i + tid / 128][n0 + tid % 128].
-    const uint32_t b_dst0 = smem_u32(sB + warp * BN + lane * 4);
+    // (BN = 128: a warp moves one 512-byte row; narrower tiles: BN / 4 threads
+    // per row.)
+    uint32_t b_dst0;
+    if constexpr (BN == 128)
+        b_dst0 = smem_u32(sB + warp * BN + lane * 4);
+    else
+        b_dst0 = smem_u32(sB + (tid / (BN / 4)) * BN + (tid % (BN / 4)) * 4);
 
     // Unpredicated copies of K-slice kt into `stage` (interior tiles, full
     // slices), one per call so they can be spread over the FMA loop: copies
@@ -170,8 +177,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         } else {
             const int i = c - G::A_PER_THREAD;
             const int krow = i * (kThreads / (BN / 4));
-            cp_async_16_full(b_dst0 + stage * B_STAGE_BYTES + (uint32_t)(krow * BN * 4),
-                             B + (size_t)(k0 + krow + warp) * N + (n0 + lane * 4));
+            if constexpr (BN == 128)
+                cp_async_16_full(b_dst0 + stage * B_STAGE_BYTES + (uint32_t)(krow * BN * 4),
+                                 B + (size_t)(k0 + krow + warp) * N + (n0 + lane * 4));
+            else
+                cp_async_16_full(b_dst0 + stage * B_STAGE_BYTES + (uint32_t)(krow * BN * 4),
+                                 B + (size_t)(k0 + krow + tid / (BN / 4)) * N +
+                                     (n0 + (tid % (BN / 4)) * 4));
         }
     };
 
@@ -371,6 +383,9 @@ cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, floa
 
 namespace {
 constexpr int kTileM = 128, kTileN = 128, kSliceK = 32;
+// Products with N <= 64 use 128 x 64 tiles (8 x 4 per thread): a 128-wide
+// tile would be at least half empty.
+constexpr int kNarrowN = 64;
 
 __global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restrict__ C,
                                      int64_t count, int splits)
@@ -406,13 +421,16 @@ __global__ void splitk_reduce4_kernel(const float4 *__restrict__ W, float4 *__re
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
                              cudaStream_t stream)
 {
+    if (N <= kNarrowN)
+        return simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
     return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
 }
 
 SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count)
 {
     SplitK p{1, K};
-    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
+    const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
+    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((N + tile_n - 1) / tile_n);
     const long long slots = 2LL * sm_count;  // two CTAs per SM
     if (tiles * 2 > slots)
         return p;  // at least half the CTA slots busy without splitting
@@ -436,8 +454,12 @@ SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count)
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
                                     const SplitK &plan, float *workspace, cudaStream_t stream)
 {
-    cudaError_t e = simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, true>(
-        M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
+    cudaError_t e =
+        N <= kNarrowN
+            ? simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, true>(
+                  M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk)
+            : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, true>(
+                  M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
     if (e != cudaSuccess)
         return e;
     const int64_t count = (int64_t)M * N;

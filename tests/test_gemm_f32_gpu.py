@@ -164,3 +164,13 @@ def test_on_side_stream():
         C = rtm.gemm_f32(Ad, Bd)
     s.synchronize()
     assert_close_to_oracle(C, A, B, "f32")
+
+
+@pytest.mark.parametrize("N", [1, 17, 33, 63, 64, 65])
+def test_narrow_tile_boundary(N):
+    """N <= 64 runs 128 x 64 tiles, N > 64 128 x 128 tiles; exercise both sides."""
+    M, K = 300, 257
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=N)
+    assert_close_to_oracle(run(A, B), A, B, "f32")
+    Ai, Bi = small_int_inputs(M, N, K, seed=N + 1)
+    assert_bit_exact(run(Ai, Bi), (Ai.to(torch.int64) @ Bi.to(torch.int64)).numpy())

@@ -85,3 +85,11 @@ def test_workspace_overlapping_output_rejected():
     with pytest.raises(rtm.GemmError) as e:
         rtm.gemm_f32_ws(Ad, Bd, out=C, workspace=buf)
     assert e.value.status == -1
+
+
+@pytest.mark.parametrize("N", [8, 63, 64, 65, 128])
+def test_split_narrow_tile_boundary(N):
+    M, K = 1024, 2048
+    assert rtm.gemm_f32_workspace_bytes(M, N, K) > 0
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=N + 5)
+    assert_close_to_oracle(run_ws(A, B), A, B, "f32")
