@@ -56,7 +56,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
 # reported as null once the source changes. See profiles/.
 TRAFFIC = {
-    "gemm_f32": {"bytes": 394303488, "source_sha1": "e4197ff0ed3e1639993ece4836af7605f5d64b35",
+    "gemm_f32": {"bytes": 387557632, "source_sha1": "875376860276fc3ecb7d8cc1de108df916517078",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
     "gemm_bf16f32": {"bytes": 1331420160,
                      "source_sha1": "a4ed42f2398c43699e598ea69aeef18e93850028",
