@@ -333,19 +333,10 @@ cudaError_t launch_gemm_bf16_tc(const TcLaunch &L, cudaStream_t stream)
         return cudaErrorInvalidValue;
 
     auto kernel = L.f16 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
-    static bool attr_done[2][64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<uint64_t> done[2] = {{0}, {0}};
+    const cudaError_t e = set_smem_limit_once(kernel, (int)SMEM_BYTES, done[L.f16 != 0]);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64 || !attr_done[L.f16 != 0][dev]) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES);
-        if (e != cudaSuccess)
-            return e;
-        if (dev >= 0 && dev < 64)
-            attr_done[L.f16 != 0][dev] = true;
-    }
     const long long ntiles = (long long)((L.M + BM - 1) / BM) * ((L.N + BN - 1) / BN);
     const int grid = (int)(ntiles < L.sm_count ? ntiles : L.sm_count);
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};

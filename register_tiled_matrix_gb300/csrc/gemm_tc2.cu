@@ -339,34 +339,32 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
         !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, BK, L.f16 != 0))
         return cudaErrorInvalidValue;
     auto kernel = L.f16 ? gemm_tc2_kernel<true> : gemm_tc2_kernel<false>;
-    static bool attr_done[2][64] = {};
-    static int max_clusters[2][64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const int fi = L.f16 != 0;
+    static std::atomic<uint64_t> done[2] = {{0}, {0}};
+    cudaError_t e = set_smem_limit_once(kernel, (int)SMEM_BYTES, done[fi]);
     if (e != cudaSuccess)
         return e;
-    const int fi = L.f16 != 0;
-    if (dev < 0 || dev >= 64 || !attr_done[fi][dev]) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES);
-        if (e != cudaSuccess)
-            return e;
-        // How many pairs can be resident at once (persistent grid size).
+    // How many pairs can be resident at once (the persistent grid), cached
+    // per device; 0 means not yet known.
+    static std::atomic<int> max_clusters[2][64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    int clusters_max = (dev >= 0 && dev < 64) ? max_clusters[fi][dev].load() : 0;
+    if (clusters_max <= 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (L.sm_count / 2), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = SMEM_BYTES;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&clusters_max, kernel, &cfg) != cudaSuccess ||
+            clusters_max <= 0) {
             cudaGetLastError();
-            n = L.sm_count / 2;
+            clusters_max = L.sm_count / 2;
         }
-        if (dev >= 0 && dev < 64) {
-            max_clusters[fi][dev] = n;
-            attr_done[fi][dev] = true;
-        }
+        if (dev >= 0 && dev < 64)
+            max_clusters[fi][dev].store(clusters_max);
     }
-    const int clusters_max = (dev >= 0 && dev < 64) ? max_clusters[fi][dev] : L.sm_count / 2;
     const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
     const int clusters = (int)(ntiles < clusters_max ? ntiles : clusters_max);
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};

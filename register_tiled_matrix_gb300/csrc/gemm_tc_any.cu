@@ -319,19 +319,10 @@ template <bool F16, bool C_VEC>
 static cudaError_t launch(const TcLaunch &L, cudaStream_t stream)
 {
     auto kernel = gemm_tc_any_kernel<F16, C_VEC>;
-    static bool done[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<uint64_t> done{0};  // per instantiation
+    const cudaError_t e = set_smem_limit_once(kernel, (int)SMEM_BYTES, done);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64 || !done[dev]) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES);
-        if (e != cudaSuccess)
-            return e;
-        if (dev >= 0 && dev < 64)
-            done[dev] = true;
-    }
     const long long ntiles = (long long)((L.M + BM - 1) / BM) * ((L.N + BN - 1) / BN);
     const int grid = (int)(ntiles < L.sm_count ? ntiles : L.sm_count);
     Params p{L.M, L.N, L.K, L.A, L.B, L.C, L.err, (unsigned long long)L.wait_limit_ns};

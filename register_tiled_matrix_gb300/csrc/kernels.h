@@ -2,10 +2,31 @@
 // kernel translation units. Arguments are already validated by the caller.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace rtm {
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` the first time it is
+// launched on the current device. `done` is one bit per device (a static of
+// the call site); concurrent first callers may both set the attribute, which
+// is harmless, and no flag is read or written without atomics.
+template <typename Kernel>
+cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit)
+        done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
 // 4-byte-aligned pointers. 1 <= K; M, N >= 1.

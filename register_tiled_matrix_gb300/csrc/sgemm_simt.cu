@@ -334,20 +334,10 @@ cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, floa
     using G = Cfg<BM, BN, BK, STAGES>;
     auto kernel = sgemm_rt_kernel<BM, BN, BK, STAGES, MINB, ORDER, B_VEC, C_VEC, SPLIT>;
     if (G::SMEM_BYTES > 48 * 1024) {
-        // Once per device and instantiation.
-        static bool done[64] = {};
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
+        static std::atomic<uint64_t> done{0};  // per instantiation
+        const cudaError_t e = set_smem_limit_once(kernel, (int)G::SMEM_BYTES, done);
         if (e != cudaSuccess)
             return e;
-        if (dev < 0 || dev >= 64 || !done[dev]) {
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)G::SMEM_BYTES);
-            if (e != cudaSuccess)
-                return e;
-            if (dev >= 0 && dev < 64)
-                done[dev] = true;
-        }
     }
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     if (tiles > 0x7fffffffLL)
