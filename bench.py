@@ -56,10 +56,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
 # reported as null once the source changes. See profiles/.
 TRAFFIC = {
-    "gemm_f32": {"bytes": 387557632, "source_sha1": "875376860276fc3ecb7d8cc1de108df916517078",
+    "gemm_f32": {"bytes": 396672000, "source_sha1": "2299e10d25cbcaf7b57126fe91dbd4897bc23c88",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
-    "gemm_bf16f32": {"bytes": 1331420160,
-                     "source_sha1": "a4ed42f2398c43699e598ea69aeef18e93850028",
+    "gemm_bf16f32": {"bytes": 1287995648,
+                     "source_sha1": "c7fa824afef5857306ee21d823e7cc355ce0ffb1",
                      "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {
