@@ -592,6 +592,12 @@ def run_configs(args) -> Optional[Dict]:
         else:
             entries.append(("gemm_bf16f32", lambda: rtm.gemm_bf16f32(A, B, out=C),
                             float(peaks["bf16_tflops"])))
+            if w.K % 8 or w.N % 8:
+                wsb = torch.empty(rtm.gemm_bf16f32_workspace_bytes(w.M, w.N, w.K),
+                                  dtype=torch.uint8, device="cuda")
+                entries.append(("gemm_bf16f32_ws (rows re-pitched, CTA pairs)",
+                                lambda: rtm.gemm_bf16f32_ws(A, B, out=C, workspace=wsb),
+                                float(peaks["bf16_tflops"])))
         for entry, fn, peak in entries:
             ms = timed(fn)
             tf = w.flops / ms / 1e9

@@ -166,12 +166,14 @@ int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * 128 x 256 tile.
  *
  * A and B hold raw bfloat16 bit patterns (uint16_t), 2-byte aligned; C is
- * 4-byte aligned (else GEMM_ERR_ALIGNMENT). Any M, N, K. When every row starts
- * on a 16-byte boundary (K % 8 == 0, N % 8 == 0, A, B, C 16-byte aligned) the
- * operands are staged by the tensor-memory-access unit; otherwise by producer
- * warps that load them element by element into the same swizzled layout
- * (slower, same arithmetic). Ragged M, N and K tiles are handled by
- * zero-filled loads and masked stores.
+ * 4-byte aligned (else GEMM_ERR_ALIGNMENT). Any M, N, K. When the rows of A
+ * and B start on 16-byte boundaries (K % 8 == 0, N % 8 == 0, A and B 16-byte
+ * aligned) the operands are staged by the tensor-memory-access unit (for
+ * M <= 128 C must be 16-byte aligned with N % 8 == 0 as well; for M > 128 C
+ * rows may start anywhere 4-byte aligned); otherwise by producer warps that
+ * load them element by element into the same swizzled layout (slower, same
+ * arithmetic; gemm_bf16f32_ws avoids this for M > 128). Ragged M, N and K
+ * tiles are handled by zero-filled loads and masked stores.
  *
  * Every wait inside the kernel is bounded (a few seconds); if one gives up
  * the kernel records GEMM_ERR_TIMEOUT in the device error word and returns
@@ -190,6 +192,40 @@ int gemm_bf16f32(int64_t M, int64_t N, int64_t K,
  */
 int gemm_f16f32(int64_t M, int64_t N, int64_t K,
                 const uint16_t *A, const uint16_t *B, float *C, void *stream);
+
+/*
+ * gemm_bf16f32_workspace_bytes — bytes of scratch memory gemm_bf16f32_ws and
+ * gemm_f16f32_ws may use for an M x N x K product, whatever the pointers:
+ * 0 when M <= 128 or K == 0 or N == 0, otherwise room for a copy of A with
+ * rows padded to a multiple of 8 values plus one of B, each rounded up to
+ * 256 bytes: ceil256(M * ceil8(K) * 2) + ceil256(K * ceil8(N) * 2). A call
+ * uses only the part for the operands it copies (below). Returns
+ * GEMM_ERR_INVALID_ARG for negative or oversized dimensions.
+ *
+ * gemm_bf16f32_ws / gemm_f16f32_ws — the product of gemm_bf16f32 /
+ * gemm_f16f32 (same layout, alignment, ownership, degenerate-shape and error
+ * rules), fast also when rows do not start on 16-byte boundaries. For M > 128,
+ * an operand whose rows are not 16-byte aligned (A when K % 8 != 0 or A is
+ * not 16-byte aligned; B likewise with N) is first copied into `workspace`
+ * (device memory owned by the caller, 16-byte aligned, not overlapping A, B
+ * or C) with its rows padded to 16-byte multiples — A's copy first, B's
+ * after it at a 256-byte-rounded offset — and the CTA-pair tensor-core kernel
+ * then stages the copies by TMA. The copy is the global level of the pages'
+ * tiling adapted to Blackwell, whose tensor-memory-access unit can only start
+ * a tile on a 16-byte boundary; the arithmetic is unchanged. When no copy is
+ * needed, or the workspace is null, misaligned or smaller than the copies,
+ * the call runs exactly what gemm_bf16f32 / gemm_f16f32 runs. The workspace
+ * contents on return are unspecified; two calls in flight at once must not
+ * share a workspace. A workspace that overlaps A, B or C returns
+ * GEMM_ERR_INVALID_ARG.
+ */
+int64_t gemm_bf16f32_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int gemm_bf16f32_ws(int64_t M, int64_t N, int64_t K,
+                    const uint16_t *A, const uint16_t *B, float *C,
+                    void *workspace, int64_t workspace_bytes, void *stream);
+int gemm_f16f32_ws(int64_t M, int64_t N, int64_t K,
+                   const uint16_t *A, const uint16_t *B, float *C,
+                   void *workspace, int64_t workspace_bytes, void *stream);
 
 /*
  * gemm_get_device_error — synchronises `stream`, then returns and clears the

@@ -17,7 +17,10 @@ from .binding import (  # noqa: F401
     STATUS,
     GemmError,
     gemm_bf16f32,
+    gemm_bf16f32_workspace_bytes,
+    gemm_bf16f32_ws,
     gemm_f16f32,
+    gemm_f16f32_ws,
     gemm_bf16f32_selftest_timeout,
     gemm_f32,
     gemm_f32_ladder,

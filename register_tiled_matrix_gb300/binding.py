@@ -59,6 +59,12 @@ def load_library() -> ctypes.CDLL:
         lib.gemm_f32_workspace_bytes.restype = ctypes.c_int64
         lib.gemm_f32_ws.argtypes = [i64, i64, i64, p, p, p, p, i64, p]
         lib.gemm_f32_ws.restype = ctypes.c_int
+        lib.gemm_bf16f32_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.gemm_bf16f32_workspace_bytes.restype = ctypes.c_int64
+        for name in ("gemm_bf16f32_ws", "gemm_f16f32_ws"):
+            f = getattr(lib, name)
+            f.argtypes = [i64, i64, i64, p, p, p, p, i64, p]
+            f.restype = ctypes.c_int
         lib.gemm_f32_ladder.argtypes = [ctypes.c_int, i64, i64, i64, p, p, p, p]
         lib.gemm_f32_ladder.restype = ctypes.c_int
         lib.gemm_bf16f32_selftest_timeout.argtypes = [i64, i64, i64, p, p, p, i64, p]
@@ -196,6 +202,54 @@ def gemm_f16f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = 
         _check(load_library().gemm_f16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                           _stream_handle(stream)))
     return C
+
+
+def gemm_bf16f32_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Largest workspace gemm_bf16f32_ws / gemm_f16f32_ws may use for this shape (0: none)."""
+    n = int(load_library().gemm_bf16f32_workspace_bytes(int(M), int(N), int(K)))
+    _check(n if n < 0 else 0)
+    return n
+
+
+def _rows_on_16_bytes(t: torch.Tensor) -> bool:
+    return t.shape[1] % 8 == 0 and t.data_ptr() % 16 == 0
+
+
+def _gemm_2byte_ws(entry: str, A: torch.Tensor, B: torch.Tensor, dtype: torch.dtype,
+                   out: Optional[torch.Tensor], workspace: Optional[torch.Tensor],
+                   stream: Optional[torch.cuda.Stream]) -> torch.Tensor:
+    C = _prepare(A, B, dtype, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        if workspace is None and M > 128 and not (_rows_on_16_bytes(A) and _rows_on_16_bytes(B)):
+            workspace = torch.empty(gemm_bf16f32_workspace_bytes(M, N, K), dtype=torch.uint8,
+                                    device=A.device)
+        ptr, nbytes = 0, 0
+        if workspace is not None:
+            if (not workspace.is_cuda or workspace.device != A.device
+                    or not workspace.is_contiguous()):
+                raise ValueError("workspace must be a contiguous CUDA tensor on A's device")
+            ptr, nbytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        _check(getattr(load_library(), entry)(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                              ptr, nbytes, _stream_handle(stream)))
+    return C
+
+
+def gemm_bf16f32_ws(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """gemm_bf16f32, re-pitching operands whose rows are not 16-byte aligned into
+    `workspace` (a CUDA tensor of at least gemm_bf16f32_workspace_bytes(M, N, K)
+    bytes; allocated with torch for this call when None and a copy is needed)."""
+    return _gemm_2byte_ws("gemm_bf16f32_ws", A, B, torch.bfloat16, out, workspace, stream)
+
+
+def gemm_f16f32_ws(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """gemm_f16f32 with the workspace rule of gemm_bf16f32_ws."""
+    return _gemm_2byte_ws("gemm_f16f32_ws", A, B, torch.float16, out, workspace, stream)
 
 
 def gemm_bf16f32_selftest_timeout(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor,

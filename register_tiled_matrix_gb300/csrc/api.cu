@@ -132,22 +132,42 @@ int finish(cudaError_t e)
     return GEMM_OK;
 }
 
+// Bytes of a copy of a rows x cols matrix of 2-byte values with every row
+// padded to a multiple of 8 values (16 bytes), rounded up to 256 bytes.
+int64_t padded_copy_bytes(int64_t rows, int64_t cols)
+{
+    return (rows * ((cols + 7) / 8 * 8) * 2 + 255) / 256 * 256;
+}
+
+bool rows_on_16_bytes(const void *base, int64_t cols)
+{
+    return cols % 8 == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0;
+}
+
+// Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
+// CTA-pair kernel run on re-pitched copies of operands whose rows do not start
+// on 16-byte boundaries.
 int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
-             void *stream, uint64_t wait_limit_ns, int mute_producer, int f16 = 0)
+             void *stream, uint64_t wait_limit_ns, int mute_producer, int f16 = 0,
+             void *workspace = nullptr, int64_t workspace_bytes = 0)
 {
     bool nothing = false;
     int st = check_common(M, N, K, A, B, C, 2, &nothing);
     if (st != GEMM_OK || nothing)
         return st;
+    if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace))
+        return GEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(C) & 3) != 0 ||
         (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 1) != 0 ||
                    (reinterpret_cast<uintptr_t>(B) & 1) != 0)))
         return GEMM_ERR_ALIGNMENT;
     // Rows on 16-byte boundaries (the TMA stride rule) take the TMA kernels;
-    // anything else the kernel with load-and-swizzle producer warps.
-    const bool tma_ok = K % 8 == 0 && N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0 &&
-                        (reinterpret_cast<uintptr_t>(A) & 15) == 0 &&
-                        (reinterpret_cast<uintptr_t>(B) & 15) == 0;
+    // anything else the kernel with load-and-swizzle producer warps, unless a
+    // workspace allows re-pitched copies for the CTA-pair kernel.
+    const bool a_rows16 = rows_on_16_bytes(A, K);
+    const bool b_rows16 = rows_on_16_bytes(B, N);
+    const bool c_rows16 = rows_on_16_bytes(C, N);
+    const bool tma_ok = a_rows16 && b_rows16 && c_rows16;
     if (mute_producer && !tma_ok)
         return GEMM_ERR_INVALID_ARG;  // the self-test exercises the TMA kernels
     DeviceInfo d;
@@ -172,10 +192,45 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     L.encode_tiled = encode_tiled_fn();
     if (!L.encode_tiled)
         return GEMM_ERR_LAUNCH;
+    if (M > 128) {
+        // CTA pairs (256-row tiles). C needs only 4-byte alignment there; A
+        // and B rows must start on 16-byte boundaries, directly or in copies.
+        const int64_t need = (a_rows16 ? 0 : padded_copy_bytes(M, K)) +
+                             (b_rows16 ? 0 : padded_copy_bytes(K, N));
+        if (need == 0)
+            return finish(rtm::launch_gemm_tc_pair(L, s));
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        if (ws && (reinterpret_cast<uintptr_t>(ws) & 15) == 0 && workspace_bytes >= need) {
+            if (overlaps(ws, need, A, M * K * 2) || overlaps(ws, need, B, K * N * 2) ||
+                overlaps(ws, need, C, M * N * 4))
+                return GEMM_ERR_INVALID_ARG;
+            if (!a_rows16) {
+                uint16_t *a_copy = reinterpret_cast<uint16_t *>(ws);
+                const int64_t lda = (K + 7) / 8 * 8;
+                cudaError_t e = rtm::launch_pack_rows_2b(A, M, K, a_copy, lda, d.sms, s);
+                if (e != cudaSuccess)
+                    return finish(e);
+                L.A = a_copy;
+                L.lda = lda;
+                ws += padded_copy_bytes(M, K);
+            }
+            if (!b_rows16) {
+                uint16_t *b_copy = reinterpret_cast<uint16_t *>(ws);
+                const int64_t ldb = (N + 7) / 8 * 8;
+                cudaError_t e = rtm::launch_pack_rows_2b(B, K, N, b_copy, ldb, d.sms, s);
+                if (e != cudaSuccess)
+                    return finish(e);
+                L.B = b_copy;
+                L.ldb = ldb;
+            }
+            return finish(rtm::launch_gemm_tc_pair(L, s));
+        }
+        return finish(rtm::launch_gemm_tc_any(L, s));
+    }
+    // One CTA per 128 x 256 tile.
     if (!tma_ok)
         return finish(rtm::launch_gemm_tc_any(L, s));
-    // CTA pairs (256-row tiles) unless M fits one 128-row tile.
-    return finish(M > 128 ? rtm::launch_gemm_tc_pair(L, s) : rtm::launch_gemm_bf16_tc(L, s));
+    return finish(rtm::launch_gemm_bf16_tc(L, s));
 }
 
 } // namespace
@@ -301,6 +356,30 @@ int gemm_f16f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16
                 void *stream)
 {
     return run_bf16(M, N, K, A, B, C, stream, kDefaultWaitLimitNs, 0, 1);
+}
+
+int64_t gemm_bf16f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim ||
+        M * N > (int64_t)1 << 52 || M * K > (int64_t)1 << 52 || K * N > (int64_t)1 << 52)
+        return GEMM_ERR_INVALID_ARG;
+    if (M <= 128 || N == 0 || K == 0)
+        return 0;
+    return padded_copy_bytes(M, K) + padded_copy_bytes(K, N);
+}
+
+int gemm_bf16f32_ws(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
+                    float *C, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    return run_bf16(M, N, K, A, B, C, stream, kDefaultWaitLimitNs, 0, 0, workspace,
+                    workspace_bytes);
+}
+
+int gemm_f16f32_ws(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
+                   float *C, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    return run_bf16(M, N, K, A, B, C, stream, kDefaultWaitLimitNs, 0, 1, workspace,
+                    workspace_bytes);
 }
 
 int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K, const uint16_t *A,

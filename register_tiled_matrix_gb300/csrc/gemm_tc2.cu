@@ -23,7 +23,13 @@
 //    accumulators are double-buffered (2 x 256 columns);
 //  * epilogue — in each CTA four warps read their CTA's accumulator rows
 //    with tcgen05.ld and store them; the eight epilogue warps of the pair hand
-//    the accumulator back to the even CTA.
+//    the accumulator back to the even CTA. Where C rows are 16-byte aligned
+//    (N % 4 == 0, C 16-byte aligned) each lane stores its row as float4;
+//    otherwise each warp turns its 32 x 32 block around in shared memory and
+//    stores it row by row, 32 consecutive floats per store instruction.
+//
+// The operands' row strides are parameters of the tensor maps, so the kernel
+// also runs on copies of A or B whose rows were padded to 16-byte multiples.
 //
 // Every mbarrier wait is bounded in time (see gemm_tc.cu); the cluster
 // barriers at start and end are reached on every path.
@@ -53,6 +59,9 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * PN;             // 512: two accumulators
 constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kEpiPitch = 33;                      // floats per row of an epilogue block
+constexpr uint32_t EPI_WARP_BYTES = 32 * kEpiPitch * 4;
+constexpr size_t SMEM_BYTES_SCALAR_C = SMEM_BYTES + 4 * EPI_WARP_BYTES;
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint16_t kEvenCta = 0x1;
 
@@ -96,7 +105,7 @@ __device__ __forceinline__ void give_up(int *err, volatile int *abort)
     *abort = 1;
 }
 
-template <bool F16>
+template <bool F16, bool C_VEC>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p)
@@ -261,33 +270,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int row = m0 + (int)rank * HM + quarter * 32 + lane;
-            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * PN;
-            float *crow = p.C + (size_t)row * p.N;
+            if constexpr (C_VEC) {
+                const int row = m0 + (int)rank * HM + quarter * 32 + lane;
+                const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * PN;
+                float *crow = p.C + (size_t)row * p.N;
 #pragma unroll 1
-            for (int c = 0; c < PN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, r);
-                tmem_wait_ld();
-                if (c == PN / 32 - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-                }
-                if (row < p.M) {
-                    const int col = n0 + c * 32;
+                for (int c = 0; c < PN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c * 32, r);
+                    tmem_wait_ld();
+                    if (c == PN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+                    }
+                    if (row < p.M) {
+                        const int col = n0 + c * 32;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        if (col + v * 4 < p.N) {
-                            float4 o;
-                            o.x = __uint_as_float(r[v * 4 + 0]);
-                            o.y = __uint_as_float(r[v * 4 + 1]);
-                            o.z = __uint_as_float(r[v * 4 + 2]);
-                            o.w = __uint_as_float(r[v * 4 + 3]);
-                            *reinterpret_cast<float4 *>(crow + col + v * 4) = o;
+                        for (int v = 0; v < 8; ++v) {
+                            if (col + v * 4 < p.N) {
+                                float4 o;
+                                o.x = __uint_as_float(r[v * 4 + 0]);
+                                o.y = __uint_as_float(r[v * 4 + 1]);
+                                o.z = __uint_as_float(r[v * 4 + 2]);
+                                o.w = __uint_as_float(r[v * 4 + 3]);
+                                *reinterpret_cast<float4 *>(crow + col + v * 4) = o;
+                            }
                         }
                     }
+                }
+            } else {
+                // Lane i holds row i of a 32 x 32 block: write it to shared memory
+                // as row i (pitch 33 floats, so the 32 lanes hit 32 banks), then
+                // read it back by columns so lane j stores column j of each row.
+                float *blk = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + 256 +
+                                                       quarter * EPI_WARP_BYTES);
+                const int row0 = m0 + (int)rank * HM + quarter * 32;
+                const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * PN;
+#pragma unroll 1
+                for (int c = 0; c < PN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c * 32, r);
+                    tmem_wait_ld();
+                    if (c == PN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+                    }
+#pragma unroll
+                    for (int v = 0; v < 32; ++v)
+                        blk[lane * kEpiPitch + v] = __uint_as_float(r[v]);
+                    __syncwarp();
+                    const int col = n0 + c * 32 + lane;
+                    const int rows = min(32, p.M - row0);
+                    if (col < p.N) {
+                        float *cp = p.C + (size_t)row0 * p.N + col;
+#pragma unroll 4
+                        for (int rr = 0; rr < rows; ++rr)
+                            cp[(size_t)rr * p.N] = blk[rr * kEpiPitch + lane];
+                    }
+                    __syncwarp();
                 }
             }
             if (++acc == 2) {
@@ -311,11 +355,13 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// rows x cols matrix of 2-byte values whose rows are `ld` values apart
+// (ld >= cols, ld * 2 a multiple of 16); columns past `cols` are never read.
 static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, uint64_t rows,
-                       uint64_t cols, uint32_t box_rows, bool f16)
+                       uint64_t cols, uint64_t ld, uint32_t box_rows, bool f16)
 {
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {ld * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
@@ -335,18 +381,23 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
         return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
     // A: M x K, boxes of 128 rows x 64 k; B: K x N, boxes of 64 k-rows x 64 n.
-    if (!encode_map(fn, &ta, L.A, (uint64_t)L.M, (uint64_t)L.K, HM, L.f16 != 0) ||
-        !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, BK, L.f16 != 0))
+    const uint64_t lda = L.lda > 0 ? (uint64_t)L.lda : (uint64_t)L.K;
+    const uint64_t ldb = L.ldb > 0 ? (uint64_t)L.ldb : (uint64_t)L.N;
+    if (!encode_map(fn, &ta, L.A, (uint64_t)L.M, (uint64_t)L.K, lda, HM, L.f16 != 0) ||
+        !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, ldb, BK, L.f16 != 0))
         return cudaErrorInvalidValue;
-    auto kernel = L.f16 ? gemm_tc2_kernel<true> : gemm_tc2_kernel<false>;
-    const int fi = L.f16 != 0;
-    static std::atomic<uint64_t> done[2] = {{0}, {0}};
-    cudaError_t e = set_smem_limit_once(kernel, (int)SMEM_BYTES, done[fi]);
+    const bool c_vec = (L.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0);
+    auto kernel = L.f16 ? (c_vec ? gemm_tc2_kernel<true, true> : gemm_tc2_kernel<true, false>)
+                        : (c_vec ? gemm_tc2_kernel<false, true> : gemm_tc2_kernel<false, false>);
+    const size_t smem_bytes = c_vec ? SMEM_BYTES : SMEM_BYTES_SCALAR_C;
+    const int fi = (L.f16 != 0 ? 1 : 0) + (c_vec ? 0 : 2);
+    static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
+    cudaError_t e = set_smem_limit_once(kernel, (int)smem_bytes, done[fi]);
     if (e != cudaSuccess)
         return e;
     // How many pairs can be resident at once (the persistent grid), cached
-    // per device; 0 means not yet known.
-    static std::atomic<int> max_clusters[2][64] = {};
+    // per device and kernel; 0 means not yet known.
+    static std::atomic<int> max_clusters[4][64] = {};
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -356,7 +407,7 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (L.sm_count / 2), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.dynamicSmemBytes = smem_bytes;
         if (cudaOccupancyMaxActiveClusters(&clusters_max, kernel, &cfg) != cudaSuccess ||
             clusters_max <= 0) {
             cudaGetLastError();
@@ -368,7 +419,7 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
     const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
     const int clusters = (int)(ntiles < clusters_max ? ntiles : clusters_max);
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};
-    kernel<<<2 * clusters, kThreads, SMEM_BYTES, stream>>>(ta, tb, p);
+    kernel<<<2 * clusters, kThreads, smem_bytes, stream>>>(ta, tb, p);
     return cudaGetLastError();
 }
 

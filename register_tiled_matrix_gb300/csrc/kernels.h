@@ -66,11 +66,22 @@ struct TcLaunch {
     int sm_count;
     void *encode_tiled;  // cuTensorMapEncodeTiled driver entry point
     int f16;             // 0: A and B are bf16; 1: A and B are fp16
+    int64_t lda = 0;     // row stride of A in elements (0: K); CTA-pair kernel only
+    int64_t ldb = 0;     // row stride of B in elements (0: N); CTA-pair kernel only
 };
 cudaError_t launch_gemm_bf16_tc(const TcLaunch &p, cudaStream_t stream);
 // The same product on CTA pairs (gemm_tc2.cu, tcgen05 cta_group::2, 256 x 256
-// tiles); used for M > 128, where a pair tile is not mostly empty.
+// tiles); used for M > 128, where a pair tile is not mostly empty. A and B
+// rows at lda / ldb elements (16-byte multiples, 16-byte aligned bases); any
+// 4-byte-aligned C and any N (float4 stores when C rows are 16-byte aligned).
 cudaError_t launch_gemm_tc_pair(const TcLaunch &p, cudaStream_t stream);
+
+// Copy a rows x cols matrix of 2-byte values (row-major, rows packed, `src`
+// 2-byte aligned) to `dst` with rows `ld` values apart (ld >= cols, ld % 8 ==
+// 0, dst 16-byte aligned), so that every row starts on a 16-byte boundary
+// (pack.cu). Values in columns cols .. ld-1 of dst are unspecified.
+cudaError_t launch_pack_rows_2b(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst,
+                                int64_t ld, int sm_count, cudaStream_t stream);
 // The same product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu):
 // operands loaded by producer warps instead of TMA. mute_producer unused.
 cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);

@@ -1,7 +1,7 @@
 """Seeded shape fuzz: every entry point on many random shapes against the full
 CPU oracle. Shapes mix tiny, ragged and tile-multiple sizes; for the tensor-
 core entry points they cover both the TMA path (K, N multiples of 8) and the
-load-and-swizzle path (anything else)."""
+load-and-swizzle or re-pitched path (anything else)."""
 
 import random
 
@@ -64,11 +64,19 @@ def _tc_shapes(seed, count):
     return out
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+TC_ENTRIES = {
+    "gemm_bf16f32": ("bf16", rtm.gemm_bf16f32),
+    "gemm_f16f32": ("f16", rtm.gemm_f16f32),
+    "gemm_bf16f32_ws": ("bf16", rtm.gemm_bf16f32_ws),
+    "gemm_f16f32_ws": ("f16", rtm.gemm_f16f32_ws),
+}
+
+
+@pytest.mark.parametrize("entry", list(TC_ENTRIES))
 @pytest.mark.parametrize("M,N,K", _tc_shapes(2025, 14))
-def test_fuzz_tensor_core(dtype, M, N, K):
+def test_fuzz_tensor_core(entry, M, N, K):
+    dtype, fn = TC_ENTRIES[entry]
     A, B = workloads.make_inputs(M, N, K, "normal", dtype, seed=M * 7919 + N * 31 + K)
-    fn = rtm.gemm_bf16f32 if dtype == "bf16" else rtm.gemm_f16f32
     C = fn(A.to(DEV), B.to(DEV))
     torch.cuda.synchronize()
     assert rtm.get_device_error() == 0

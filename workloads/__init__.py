@@ -70,6 +70,9 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("f32_4097x3001x1023", 4097, 3001, 1023, "f32", "uniform", _seed(4, 1), False),
         Workload("f32_8192x64x4096", 8192, 64, 4096, "f32", "uniform", _seed(4, 2), True),
         Workload("bf16_8192_normal", 8192, 8192, 8192, "bf16", "normal", _seed(5), False),
+        # The tensor-core case with K and N not multiples of 8: no row of A or
+        # B starts on a 16-byte boundary after the first.
+        Workload("bf16_8192x8190x8190", 8192, 8190, 8190, "bf16", "normal", _seed(5, 1), False),
     ]
 }
 
