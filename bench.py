@@ -577,7 +577,9 @@ def run_configs(args) -> Optional[Dict]:
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / args.steps
 
-    for name, w in workloads.WORKLOADS.items():
+    names = args.config_names.split(",") if args.config_names else list(workloads.WORKLOADS)
+    for name in names:
+        w = workloads.WORKLOADS[name]
         A, B = workloads.workload_inputs(w)
         A, B = A.cuda(), B.cuda()
         C = torch.empty(w.M, w.N, device="cuda")
@@ -634,6 +636,8 @@ def main(argv=None):
     p.add_argument("--ladder-size", type=int, default=4096)
     p.add_argument("--configs", action="store_true",
                    help="time every configuration's product (report only)")
+    p.add_argument("--config-names", default=None,
+                   help="comma-separated workload names for --configs (default: all)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

@@ -23,7 +23,8 @@ def test_exports_every_declared_symbol(lib):
     names = rtm.header_symbols()
     assert {"gemm_f32", "gemm_f32_ladder", "gemm_f32_ws", "gemm_f32_workspace_bytes",
             "gemm_f32_noalloc", "gemm_bf16f32", "gemm_f16f32", "gemm_get_device_error",
-            "gemm_bf16f32_selftest_timeout", "gemm_status_string"} <= set(names)
+            "gemm_bf16f32_selftest_timeout", "gemm_status_string", "gemm_bf16f32_ws",
+            "gemm_f16f32_ws", "gemm_bf16f32_workspace_bytes"} <= set(names)
     for name in names:
         assert hasattr(lib, name), f"{name} declared in gemm.h but not exported"
 
@@ -107,6 +108,34 @@ def test_workspace_entry_points_host_checks(lib):
     assert f(8, 8, 8, A, B, C, None, 64, None) == -1     # size without a buffer
     assert f(8, 8, 8, A, B, C, W + 2, 64, None) == -2    # misaligned workspace
     assert f(0, 8, 8, None, None, None, None, 0, None) == 0
+
+
+def _ceil256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_tensor_core_workspace_size(lib):
+    """Room for a copy of A and of B with rows padded to 8 values, each
+    rounded up to 256 bytes; none where no re-pitched product would run."""
+    f = lib.gemm_bf16f32_workspace_bytes
+    for M, N, K in [(300, 129, 77), (129, 1, 1), (8192, 8190, 8190), (4097, 3001, 1023),
+                    (256, 256, 256)]:
+        expect = _ceil256(M * ((K + 7) // 8 * 8) * 2) + _ceil256(K * ((N + 7) // 8 * 8) * 2)
+        assert f(M, N, K) == expect
+    assert f(128, 129, 77) == 0
+    assert f(300, 0, 77) == 0 and f(300, 129, 0) == 0 and f(0, 129, 77) == 0
+    assert f(-1, 8, 8) == -1 and f(300, 8, 1 << 31) == -1
+
+
+@pytest.mark.parametrize("fn", ["gemm_bf16f32_ws", "gemm_f16f32_ws"])
+def test_tensor_core_workspace_host_checks(lib, fn):
+    f = getattr(lib, fn)
+    A, B, C, W = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+    assert f(300, 129, 77, A, B, C, W, -4, None) == -1      # negative workspace size
+    assert f(300, 129, 77, A, B, C, None, 64, None) == -1   # size without a buffer
+    assert f(300, 129, 77, A + 1, B, C, W, 1 << 20, None) == -2
+    assert f(-3, 129, 77, A, B, C, W, 1 << 20, None) == -1
+    assert f(0, 129, 77, None, None, None, None, 0, None) == 0
 
 
 def test_selftest_limit_range(lib):
