@@ -58,8 +58,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     "gemm_f32": {"bytes": 396672000, "source_sha1": "2299e10d25cbcaf7b57126fe91dbd4897bc23c88",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
-    "gemm_bf16f32": {"bytes": 1287995648,
-                     "source_sha1": "c7fa824afef5857306ee21d823e7cc355ce0ffb1",
+    "gemm_bf16f32": {"bytes": 1304644608,
+                     "source_sha1": "6346158bc3e31af92e2aa816ba45f82d821f221b",
                      "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {

@@ -28,6 +28,13 @@ cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> 
     return e;
 }
 
+// Tiles of the SIMT FP32 product: 128 x 128 C tiles (128 x 64 for N <= 64,
+// where a 128-wide tile would be at least half empty), 32-deep K slices.
+namespace simt_tiles {
+constexpr int kTileM = 128, kTileN = 128, kSliceK = 32;
+constexpr int kNarrowN = 64;
+} // namespace simt_tiles
+
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
 // 4-byte-aligned pointers. 1 <= K; M, N >= 1.
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
@@ -41,7 +48,7 @@ struct SplitK {
     int splits;  // 1: no split (plain product)
     int kchunk;
 };
-SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count);
+SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count);  // sgemm_plan.cu
 // workspace: plan.splits * M * N floats. 1 <= K; M, N >= 1; plan.splits >= 2.
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
                                     const SplitK &plan, float *workspace, cudaStream_t stream);

@@ -372,10 +372,7 @@ cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, floa
 } // namespace simt
 
 namespace {
-constexpr int kTileM = 128, kTileN = 128, kSliceK = 32;
-// Products with N <= 64 use 128 x 64 tiles (8 x 4 per thread): a 128-wide
-// tile would be at least half empty.
-constexpr int kNarrowN = 64;
+using namespace simt_tiles;
 
 __global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restrict__ C,
                                      int64_t count, int splits)
@@ -414,46 +411,6 @@ cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B
     if (N <= kNarrowN)
         return simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
     return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
-}
-
-// Schedule model for the split: an SM retires CTA-slices (one BK-deep slice
-// of one tile) at about the same rate whether one or two CTAs are resident (a
-// lone CTA runs about twice as fast), so T equal CTAs of c slices each take
-// about ceil(T / SMs) * c slice-times. A split into s partial products adds a
-// reduction launch (about 2 slice-times) and, per partial product, writing and
-// re-reading M x N floats (about M * N / 2.1e6 slice-times at HBM bandwidth).
-// The plan minimises that estimate; a sweep of every split on GB300 (shapes
-// from 256^3 to 2048^2 x 8192) put its choice within 1.2 % of the fastest on
-// average. Products with more tiles than SMs are not split (every SM already
-// has work; the gain measured there was 4-9 % at most), nor are splits kept
-// that the model prices within 3 % of the plain product.
-SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count)
-{
-    SplitK p{1, K};
-    const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
-    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((N + tile_n - 1) / tile_n);
-    if (sm_count <= 0 || tiles > sm_count)
-        return p;
-    const long long kslices = (K + kSliceK - 1) / kSliceK;
-    const double slice_time = tile_n == kNarrowN ? 0.8 : 1.0;  // narrow tiles: less work per slice
-    const double per_partial = (double)M * N / 2.1e6;
-    const double plain = (double)((tiles + sm_count - 1) / sm_count) * kslices * slice_time;
-    double best = plain;
-    for (int s = 2; s <= 32; ++s) {
-        const long long chunk = (kslices + s - 1) / s;
-        const int splits = (int)((kslices + chunk - 1) / chunk);
-        if (splits < 2)
-            continue;
-        const double est = (double)((tiles * splits + sm_count - 1) / sm_count) * chunk * slice_time +
-                           2.0 + per_partial * splits;
-        if (est < best) {
-            best = est;
-            p = SplitK{splits, (int)(chunk * kSliceK)};
-        }
-    }
-    if (p.splits > 1 && best > 0.97 * plain)
-        p = SplitK{1, K};
-    return p;
 }
 
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
