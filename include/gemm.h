@@ -50,6 +50,14 @@
 
 #include <stdint.h>
 
+/* Only the entry points below are exported from the shared library; the
+   library is built with hidden default visibility. */
+#if defined(__GNUC__) || defined(__clang__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -79,8 +87,8 @@ typedef enum gemm_status {
  * tiling; the error against the exact sum is bounded by a small multiple of
  * K * 2^-24 * sum_k |A[i][k] B[k][j]|.
  */
-int gemm_f32(int64_t M, int64_t N, int64_t K,
-             const float *A, const float *B, float *C, void *stream);
+GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K,
+                      const float *A, const float *B, float *C, void *stream);
 
 /*
  * gemm_f32_workspace_bytes — bytes of scratch memory gemm_f32_ws uses for an
@@ -105,10 +113,10 @@ int gemm_f32(int64_t M, int64_t N, int64_t K,
  * ("寄存器Tiling跨架构解析", section 1.1: global tiling decides how much work
  * each block gets) and changes only the summation order.
  */
-int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K);
-int gemm_f32_ws(int64_t M, int64_t N, int64_t K,
-                const float *A, const float *B, float *C,
-                void *workspace, int64_t workspace_bytes, void *stream);
+GEMM_API int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K);
+GEMM_API int gemm_f32_ws(int64_t M, int64_t N, int64_t K,
+                         const float *A, const float *B, float *C,
+                         void *workspace, int64_t workspace_bytes, void *stream);
 
 /*
  * gemm_f32_noalloc — the gemm_f32_ws product for callers that cannot
@@ -131,8 +139,8 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K,
  * (a call writes every element it reads), and two calls whose work overlaps
  * on the GPU (for example on two streams) race on it.
  */
-int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
-                     const float *A, const float *B, float *C, void *stream);
+GEMM_API int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
+                              const float *A, const float *B, float *C, void *stream);
 
 /*
  * gemm_f32_ladder — the ablation ladder of the register-tiling page: the same
@@ -153,8 +161,8 @@ int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
  * when M exceeds what their grid can cover (65535 tiles along M: M > 1,048,560
  * for rung 0, 2,097,120 for rung 1, 4,194,240 for rung 2).
  */
-int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
-                    const float *A, const float *B, float *C, void *stream);
+GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
+                             const float *A, const float *B, float *C, void *stream);
 
 /*
  * gemm_bf16f32 — bfloat16 inputs, fp32 accumulation and output, on the
@@ -179,8 +187,8 @@ int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * the kernel records GEMM_ERR_TIMEOUT in the device error word and returns
  * instead of hanging. Read it with gemm_get_device_error.
  */
-int gemm_bf16f32(int64_t M, int64_t N, int64_t K,
-                 const uint16_t *A, const uint16_t *B, float *C, void *stream);
+GEMM_API int gemm_bf16f32(int64_t M, int64_t N, int64_t K,
+                          const uint16_t *A, const uint16_t *B, float *C, void *stream);
 
 /*
  * gemm_f16f32 — IEEE half-precision (fp16) inputs, fp32 accumulation and
@@ -190,8 +198,8 @@ int gemm_bf16f32(int64_t M, int64_t N, int64_t K,
  * raw fp16 bit patterns; every rule of gemm_bf16f32 applies (alignment,
  * the two staging paths, bounded waits).
  */
-int gemm_f16f32(int64_t M, int64_t N, int64_t K,
-                const uint16_t *A, const uint16_t *B, float *C, void *stream);
+GEMM_API int gemm_f16f32(int64_t M, int64_t N, int64_t K,
+                         const uint16_t *A, const uint16_t *B, float *C, void *stream);
 
 /*
  * gemm_bf16f32_workspace_bytes — bytes of scratch memory gemm_bf16f32_ws and
@@ -219,13 +227,13 @@ int gemm_f16f32(int64_t M, int64_t N, int64_t K,
  * share a workspace. A workspace that overlaps A, B or C returns
  * GEMM_ERR_INVALID_ARG.
  */
-int64_t gemm_bf16f32_workspace_bytes(int64_t M, int64_t N, int64_t K);
-int gemm_bf16f32_ws(int64_t M, int64_t N, int64_t K,
-                    const uint16_t *A, const uint16_t *B, float *C,
-                    void *workspace, int64_t workspace_bytes, void *stream);
-int gemm_f16f32_ws(int64_t M, int64_t N, int64_t K,
-                   const uint16_t *A, const uint16_t *B, float *C,
-                   void *workspace, int64_t workspace_bytes, void *stream);
+GEMM_API int64_t gemm_bf16f32_workspace_bytes(int64_t M, int64_t N, int64_t K);
+GEMM_API int gemm_bf16f32_ws(int64_t M, int64_t N, int64_t K,
+                             const uint16_t *A, const uint16_t *B, float *C,
+                             void *workspace, int64_t workspace_bytes, void *stream);
+GEMM_API int gemm_f16f32_ws(int64_t M, int64_t N, int64_t K,
+                            const uint16_t *A, const uint16_t *B, float *C,
+                            void *workspace, int64_t workspace_bytes, void *stream);
 
 /*
  * gemm_get_device_error — synchronises `stream`, then returns and clears the
@@ -233,7 +241,7 @@ int gemm_f16f32_ws(int64_t M, int64_t N, int64_t K,
  * in any kernel of this library on this device gave up since the last call.
  * Returns GEMM_ERR_LAUNCH if the synchronisation itself fails.
  */
-int gemm_get_device_error(void *stream);
+GEMM_API int gemm_get_device_error(void *stream);
 
 /*
  * gemm_bf16f32_selftest_timeout — failure-detection check for the bounded
@@ -247,12 +255,12 @@ int gemm_get_device_error(void *stream);
  * the TMA path (K % 8 == 0, N % 8 == 0, 16-byte-aligned pointers) else
  * GEMM_ERR_INVALID_ARG; wait_limit_ns must be in [1e6, 1e10].
  */
-int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K,
-                                  const uint16_t *A, const uint16_t *B, float *C,
-                                  int64_t wait_limit_ns, void *stream);
+GEMM_API int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K,
+                                           const uint16_t *A, const uint16_t *B, float *C,
+                                           int64_t wait_limit_ns, void *stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char *gemm_status_string(int status);
+GEMM_API const char *gemm_status_string(int status);
 
 #ifdef __cplusplus
 }

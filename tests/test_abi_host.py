@@ -3,6 +3,8 @@ symbol that include/gemm.h declares, and rejects bad arguments on the host
 before any CUDA call. No kernel is launched here (there is no GPU)."""
 
 import ctypes
+import shutil
+import subprocess
 
 import pytest
 
@@ -27,6 +29,20 @@ def test_exports_every_declared_symbol(lib):
             "gemm_f16f32_ws", "gemm_bf16f32_workspace_bytes"} <= set(names)
     for name in names:
         assert hasattr(lib, name), f"{name} declared in gemm.h but not exported"
+
+
+def test_exports_nothing_but_the_entry_points(lib):
+    """Built with hidden visibility: the dynamic symbol table holds exactly the
+    functions gemm.h declares, so internal C++ names cannot clash with another
+    library's in the same process."""
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", rtm.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines()
+                if len(line.split()) == 3 and line.split()[1] in "TWVui"}
+    assert exported == set(rtm.header_symbols())
 
 
 def test_status_strings(lib):
