@@ -24,9 +24,12 @@
 //  * epilogue — in each CTA four warps read their CTA's accumulator rows
 //    with tcgen05.ld and store them; the eight epilogue warps of the pair hand
 //    the accumulator back to the even CTA. Where C rows are 16-byte aligned
-//    (N % 4 == 0, C 16-byte aligned) each lane stores its row as float4;
-//    otherwise each warp turns its 32 x 32 block around in shared memory and
-//    stores it row by row, 32 consecutive floats per store instruction.
+//    (N % 4 == 0, C 16-byte aligned) each warp stages its 32 x 32 blocks in
+//    128-byte-swizzled shared memory and the TMA unit stores them (a float4
+//    per lane and row before: 0.605 ms at 8192^3, 0.111 ms at 8192^2 x 64;
+//    TMA stores: 0.582 and 0.054); otherwise each warp turns its 32 x 32 block
+//    around in shared memory and stores it row by row, 32 consecutive floats
+//    per store instruction.
 //
 // The operands' row strides are parameters of the tensor maps, so the kernel
 // also runs on copies of A or B whose rows were padded to 16-byte multiples.
@@ -34,6 +37,7 @@
 // Every mbarrier wait is bounded in time (see gemm_tc.cu); the cluster
 // barriers at start and end are reached on every path.
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -62,6 +66,14 @@ constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barr
 constexpr int kEpiPitch = 33;                      // floats per row of an epilogue block
 constexpr uint32_t EPI_WARP_BYTES = 32 * kEpiPitch * 4;
 constexpr size_t SMEM_BYTES_SCALAR_C = SMEM_BYTES + 4 * EPI_WARP_BYTES;
+// TMA-store epilogue: per epilogue warp two 32 x 32 fp32 boxes (4 KB each,
+// 128-byte swizzled, 1024-byte aligned) after a 1 KB block for the barriers.
+constexpr uint32_t EPI_BOX_BYTES = 32 * 32 * 4;
+constexpr size_t SMEM_BYTES_TMA_C = SMEM_BYTES + 1024 + 4 * 2 * EPI_BOX_BYTES;
+// Epilogue variants: C rows 16-byte aligned (N % 4 == 0, C 16-byte aligned),
+// TMA stores of 32 x 32 boxes; any other C, row-by-row stores through shared
+// memory.
+enum { kEpiRowByRow = 1, kEpiTmaStore = 2 };
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint16_t kEvenCta = 0x1;
 
@@ -105,10 +117,11 @@ __device__ __forceinline__ void give_up(int *err, volatile int *abort)
     *abort = 1;
 }
 
-template <bool F16, bool C_VEC>
+template <bool F16, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const Params p)
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -142,6 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_mbarrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (EPI == kEpiTmaStore)
+            tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -270,37 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            if constexpr (C_VEC) {
-                const int row = m0 + (int)rank * HM + quarter * 32 + lane;
-                const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * PN;
-                float *crow = p.C + (size_t)row * p.N;
-#pragma unroll 1
-                for (int c = 0; c < PN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_row + c * 32, r);
-                    tmem_wait_ld();
-                    if (c == PN / 32 - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-                    }
-                    if (row < p.M) {
-                        const int col = n0 + c * 32;
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            if (col + v * 4 < p.N) {
-                                float4 o;
-                                o.x = __uint_as_float(r[v * 4 + 0]);
-                                o.y = __uint_as_float(r[v * 4 + 1]);
-                                o.z = __uint_as_float(r[v * 4 + 2]);
-                                o.w = __uint_as_float(r[v * 4 + 3]);
-                                *reinterpret_cast<float4 *>(crow + col + v * 4) = o;
-                            }
-                        }
-                    }
-                }
-            } else {
+            if constexpr (EPI == kEpiRowByRow) {
                 // Lane i holds row i of a 32 x 32 block: write it to shared memory
                 // as row i (pitch 33 floats, so the 32 lanes hit 32 banks), then
                 // read it back by columns so lane j stores column j of each row.
@@ -333,11 +318,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 }
+            } else {
+                // Lane i writes row i of each 32 x 32 block into a 128-byte-
+                // swizzled box (16-byte chunk q of row i at q ^ (i mod 8):
+                // 8 lanes cover all 32 banks), then one lane hands the box to
+                // the TMA unit, which stores it and clips rows and columns
+                // outside M x N. Two boxes per warp alternate; a box is
+                // rewritten only after the store issued from it has read it.
+                uint8_t *boxes = smem + STAGES * STAGE_BYTES + 1024 + quarter * 2 * EPI_BOX_BYTES;
+                const int row0 = m0 + (int)rank * HM + quarter * 32;
+                const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * PN;
+#pragma unroll 1
+                for (int c = 0; c < PN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c * 32, r);
+                    tmem_wait_ld();
+                    if (c == PN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+                    }
+                    const int col = n0 + c * 32;
+                    if (row0 >= p.M || col >= p.N)
+                        continue;  // the whole box lies outside C
+                    uint8_t *box = boxes + (c & 1) * EPI_BOX_BYTES;
+                    if (lane == 0)
+                        bulk_wait_group_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<uint4 *>(box + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                            make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, smem_u32(box), col, row0);
+                        bulk_commit_group();
+                    }
+                }
             }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1;
             }
+        }
+        if constexpr (EPI == kEpiTmaStore) {
+            if (lane == 0)
+                bulk_wait_group<0>();  // every store done before the CTA leaves
         }
     }
 
@@ -371,6 +399,21 @@ static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, uin
     return r == CUDA_SUCCESS;
 }
 
+// C (M x N fp32, rows N * 4 bytes apart, N % 4 == 0, 16-byte aligned) as
+// 32 x 32 boxes with the 128-byte swizzle of the epilogue's staging boxes.
+static bool encode_c_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, uint64_t rows,
+                         uint64_t cols)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 } // namespace tc2
 
 cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
@@ -387,9 +430,15 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
         !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, ldb, BK, L.f16 != 0))
         return cudaErrorInvalidValue;
     const bool c_vec = (L.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0);
-    auto kernel = L.f16 ? (c_vec ? gemm_tc2_kernel<true, true> : gemm_tc2_kernel<true, false>)
-                        : (c_vec ? gemm_tc2_kernel<false, true> : gemm_tc2_kernel<false, false>);
-    const size_t smem_bytes = c_vec ? SMEM_BYTES : SMEM_BYTES_SCALAR_C;
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
+    if (c_vec && !encode_c_map(fn, &tc, L.C, (uint64_t)L.M, (uint64_t)L.N))
+        return cudaErrorInvalidValue;
+    auto kernel = L.f16 ? (c_vec ? gemm_tc2_kernel<true, kEpiTmaStore>
+                                 : gemm_tc2_kernel<true, kEpiRowByRow>)
+                        : (c_vec ? gemm_tc2_kernel<false, kEpiTmaStore>
+                                 : gemm_tc2_kernel<false, kEpiRowByRow>);
+    const size_t smem_bytes = c_vec ? SMEM_BYTES_TMA_C : SMEM_BYTES_SCALAR_C;
     const int fi = (L.f16 != 0 ? 1 : 0) + (c_vec ? 0 : 2);
     static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
     cudaError_t e = set_smem_limit_once(kernel, (int)smem_bytes, done[fi]);
@@ -419,7 +468,7 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
     const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
     const int clusters = (int)(ntiles < clusters_max ? ntiles : clusters_max);
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};
-    kernel<<<2 * clusters, kThreads, smem_bytes, stream>>>(ta, tb, p);
+    kernel<<<2 * clusters, kThreads, smem_bytes, stream>>>(ta, tb, tc, p);
     return cudaGetLastError();
 }
 
