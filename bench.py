@@ -58,8 +58,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     "gemm_f32": {"bytes": 395282688, "source_sha1": "3ca6f7fb3b5080ee587b00398e89ee873ce70dd2",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
-    "gemm_bf16f32": {"bytes": 1304644608,
-                     "source_sha1": "6346158bc3e31af92e2aa816ba45f82d821f221b",
+    "gemm_bf16f32": {"bytes": 1322460672,
+                     "source_sha1": "c783e511080729e042138d66e9ba9af5dfda2306",
                      "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {
