@@ -513,7 +513,7 @@ def run_reference(args) -> Optional[Dict]:
 
 
 def run_ladder(args) -> Optional[Dict]:
-    """Time the page's ablation ladder (gemm_f32_ladder rungs 0-3) on one square size."""
+    """Time the page's ablation ladder (gemm_f32_ladder rungs 0-6) on one square size."""
     import register_tiled_matrix_gb300 as rtm
     from oracle import tiling_model
 
@@ -526,11 +526,12 @@ def run_ladder(args) -> Optional[Dict]:
     C = torch.empty(n, n, device="cuda")
     flops = 2.0 * n ** 3
     # Model of shared reads per output per k for each rung (counting model of
-    # the page's loops): naive 0, shared-tiled 2, 4x4 register 0.5, 8x8 0.25.
-    model = {0: 0.0, 1: 2.0, 2: tiling_model.predicted_shared_reads_per_output_per_k(4, 4),
-             3: tiling_model.predicted_shared_reads_per_output_per_k(8, 8)}
+    # the page's loops): naive 0, shared-tiled 2, T x T register tile 2/T.
+    reads = tiling_model.predicted_shared_reads_per_output_per_k
+    model = {0: 0.0, 1: 2.0, 2: reads(4, 4), 3: reads(8, 8), 4: reads(1, 1), 5: reads(2, 2),
+             6: reads(8, 8)}
     rungs = []
-    for rung in range(4):
+    for rung in range(7):
         for _ in range(args.warmup):
             rtm.gemm_f32_ladder(rung, A, B, out=C)
         torch.cuda.synchronize()

@@ -156,10 +156,19 @@ GEMM_API int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
  *           outputs per thread (0.5 shared reads per output per k);
  *   rung 3  gemm_f32 itself (8 x 8 per thread, 0.25).
  *
+ * Rungs 4-6 are the page's extreme-tile experiment ("寄存器Tiling跨架构解析",
+ * section 7.4): rung 2's kernel with only the per-thread tile changed, T x T
+ * outputs on the same 16 x 16 threads (a 16T x 16T block, 2/T shared reads
+ * per output per k):
+ *
+ *   rung 4  T = 1 (16 x 16 block);   rung 5  T = 2 (32 x 32 block);
+ *   rung 6  T = 8 (128 x 128 block); rung 2 is T = 4.
+ *
  * Same layout, ownership, degenerate-shape and error rules as gemm_f32; any
- * shape. Rungs 0-2 also return GEMM_ERR_INVALID_ARG for a rung outside 0..3 or
- * when M exceeds what their grid can cover (65535 tiles along M: M > 1,048,560
- * for rung 0, 2,097,120 for rung 1, 4,194,240 for rung 2).
+ * shape. GEMM_ERR_INVALID_ARG for a rung outside 0..6, or when M exceeds what
+ * the rung's grid can cover (65535 tiles along M: M > 1,048,560 for rungs 0
+ * and 4, 2,097,120 for rungs 1 and 5, 4,194,240 for rung 2, 8,388,480 for
+ * rung 6).
  */
 GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
                              const float *A, const float *B, float *C, void *stream);

@@ -164,7 +164,10 @@ def gemm_f32_ws(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = 
 
 
 LADDER = {0: "naive", 1: "shared-tiled 32x32", 2: "register-tiled 64x64, 4x4/thread",
-          3: "register-tiled 128x128, 8x8/thread (gemm_f32)"}
+          3: "register-tiled 128x128, 8x8/thread (gemm_f32)",
+          4: "register-tiled 16x16, 1x1/thread (rung 2's kernel, T=1)",
+          5: "register-tiled 32x32, 2x2/thread (rung 2's kernel, T=2)",
+          6: "register-tiled 128x128, 8x8/thread (rung 2's kernel, T=8)"}
 
 
 def gemm_f32_ladder(rung: int, A: torch.Tensor, B: torch.Tensor,

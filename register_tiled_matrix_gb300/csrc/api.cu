@@ -321,7 +321,7 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
 int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K, const float *A, const float *B,
                     float *C, void *stream)
 {
-    if (rung < 0 || rung > 3)
+    if (rung < 0 || rung > 6)
         return GEMM_ERR_INVALID_ARG;
     if (rung == 3)
         return gemm_f32(M, N, K, A, B, C, stream);

@@ -6,14 +6,17 @@
 // cores the per-thread register tile becomes the matrix instruction's
 // accumulator fragment):
 //
-//  * global tiling — a persistent CTA per SM walks 128 x 256 C tiles in
-//    grouped order (GROUP_M tile-rows at a time) for L2 reuse;
+//  * global tiling — a persistent CTA per SM walks 128 x BN C tiles in
+//    grouped order (GROUP_M tile-rows at a time) for L2 reuse; BN is 256, or
+//    128 / 64 for short, wide products (M <= 128), where 256-wide tiles
+//    would leave most SMs idle (N / 256 tiles);
 //  * shared tiling — one TMA producer warp streams 64-deep K-slices of A
-//    (128 x 64, K-major) and B (64 x 256, N-major) into a 4-stage ring of
-//    128-byte-swizzled shared-memory buffers, zero-filled past M, N, K;
-//  * accumulator tiling — one thread issues tcgen05.mma (M=128, N=256, K=16,
-//    four per K-slice) into a 128 x 256 fp32 accumulator in tensor memory
-//    (TMEM), double-buffered (2 x 256 columns) so the epilogue of one tile
+//    (128 x 64, K-major) and B (64 x BN, N-major) into a ring of
+//    128-byte-swizzled shared-memory buffers (4, 6 or 8 stages, about 192 KB),
+//    zero-filled past M, N, K;
+//  * accumulator tiling — one thread issues tcgen05.mma (M=128, N=BN, K=16,
+//    four per K-slice) into a 128 x BN fp32 accumulator in tensor memory
+//    (TMEM), double-buffered (2 x BN columns) so the epilogue of one tile
 //    overlaps the MMAs of the next;
 //  * epilogue — four warps read the accumulator with tcgen05.ld (one TMEM
 //    lane = one row of C per thread) and store fp32 rows with masks.
@@ -35,22 +38,26 @@ namespace rtm {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;                 // 64 16-bit values = 128 bytes = one swizzle row
-constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kGroupM = 16;
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;            // 16 KB
 constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;             // 8 KB: 64 k-rows x 64 n
-constexpr uint32_t B_STAGE_BYTES = BK * BN * 2;            // 32 KB
-constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr uint32_t TMEM_COLS = 2 * BN;                     // 512: two accumulators
-constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+// Sizes that follow from the tile width BN (256, 128 or 64).
+template <int BN>
+struct Tile {
+    static constexpr uint32_t B_STAGE_BYTES = BK * BN * 2;  // 32, 16 or 8 KB
+    static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : BN == 128 ? 6 : 8;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;           // two accumulators
+    static constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
 
 // Instruction descriptor, kind::f16: D fp32, A and B both bf16 (format 1) or
-// both fp16 (format 0), A K-major, B MN-major, N = 256, M = 128.
-template <bool F16>
+// both fp16 (format 0), A K-major, B MN-major, N = BN, M = 128.
+template <bool F16, int BN>
 __host__ __device__ constexpr uint32_t idesc()
 {
     return (1u << 4)                               // D format: f32
@@ -78,6 +85,7 @@ struct Params {
     int mute_producer;
 };
 
+template <int BN>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &n0)
 {
     const int group_size = kGroupM * tiles_n;
@@ -95,11 +103,14 @@ __device__ __forceinline__ void give_up(int *err, volatile int *abort)
     *abort = 1;
 }
 
-template <bool F16>
+template <bool F16, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const Params p)
+                   const __grid_constant__ CUtensorMap tmB, const Params p)
 {
+    constexpr int STAGES = Tile<BN>::STAGES;
+    constexpr uint32_t STAGE_BYTES = Tile<BN>::STAGE_BYTES;
+    constexpr uint32_t TMEM_COLS = Tile<BN>::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -151,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks
             for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
                 int m0, n0;
-                tile_coords(t, tiles_m, tiles_n, m0, n0);
+                tile_coords<BN>(t, tiles_m, tiles_n, m0, n0);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1, limit, abort)) {
                         give_up(p.err, abort);
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t adesc = sdesc_sw128(sa + kk * UMMA_K * 2, 16, 1024);
                         const uint64_t bdesc =
                             sdesc_sw128(sb + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
-                        umma_f16(d_tmem, adesc, bdesc, idesc<F16>(), (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16(d_tmem, adesc, bdesc, idesc<F16, BN>(), (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
                     umma_commit(&empty[stage]);  // frees the stage when these MMAs finish
@@ -245,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc = 0, acc_phase = 0;
         for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
             int m0, n0;
-            tile_coords(t, tiles_m, tiles_n, m0, n0);
+            tile_coords<BN>(t, tiles_m, tiles_n, m0, n0);
             if (!mbar_wait_bounded(&tfull[acc], acc_phase, limit, abort)) {
                 give_up(p.err, abort);
                 break;
@@ -317,11 +328,9 @@ static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, uin
     return r == CUDA_SUCCESS;
 }
 
-} // namespace tc
-
-cudaError_t launch_gemm_bf16_tc(const TcLaunch &L, cudaStream_t stream)
+template <int BN>
+cudaError_t launch_bn(const TcLaunch &L, cudaStream_t stream)
 {
-    using namespace tc;
     auto fn = reinterpret_cast<EncodeTiledFn>(L.encode_tiled);
     if (!fn)
         return cudaErrorInvalidValue;
@@ -332,16 +341,38 @@ cudaError_t launch_gemm_bf16_tc(const TcLaunch &L, cudaStream_t stream)
         !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, BK, L.f16 != 0))
         return cudaErrorInvalidValue;
 
-    auto kernel = L.f16 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+    auto kernel = L.f16 ? gemm_tc_kernel<true, BN> : gemm_tc_kernel<false, BN>;
     static std::atomic<uint64_t> done[2] = {{0}, {0}};
-    const cudaError_t e = set_smem_limit_once(kernel, (int)SMEM_BYTES, done[L.f16 != 0]);
+    const size_t smem_bytes = Tile<BN>::SMEM_BYTES;
+    const cudaError_t e = set_smem_limit_once(kernel, (int)smem_bytes, done[L.f16 != 0]);
     if (e != cudaSuccess)
         return e;
     const long long ntiles = (long long)((L.M + BM - 1) / BM) * ((L.N + BN - 1) / BN);
     const int grid = (int)(ntiles < L.sm_count ? ntiles : L.sm_count);
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};
-    kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(ta, tb, p);
+    kernel<<<grid, kThreads, smem_bytes, stream>>>(ta, tb, p);
     return cudaGetLastError();
+}
+
+} // namespace tc
+
+cudaError_t launch_gemm_bf16_tc(const TcLaunch &L, cudaStream_t stream)
+{
+    return launch_gemm_bf16_tc_bn(L, 256, stream);
+}
+
+cudaError_t launch_gemm_bf16_tc_bn(const TcLaunch &L, int bn, cudaStream_t stream)
+{
+    switch (bn) {
+    case 256:
+        return tc::launch_bn<256>(L, stream);
+    case 128:
+        return tc::launch_bn<128>(L, stream);
+    case 64:
+        return tc::launch_bn<64>(L, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 } // namespace rtm

@@ -15,6 +15,17 @@
 //           reads per output per k); BK = 16.
 //
 // Rung 3 is the tuned kernel of sgemm_simt.cu (8 x 8 per thread, 0.25).
+//
+// Rungs 4-6 are the page's extreme-tile experiment ("寄存器Tiling跨架构解析",
+// section 7.4: time the kernel with a 1x1 and with a large tile to see how much
+// register tiling contributes): rung 2's kernel, unchanged but for the size of
+// the per-thread tile T x T, on the same 16 x 16 threads and BK = 16, so the
+// block is 16T x 16T and a thread reads 2T values from shared memory for T^2
+// FMA (2/T shared reads per output per k):
+//   rung 4  T = 1 (16 x 16 block, 2 reads per output per k);
+//   rung 5  T = 2 (32 x 32 block, 1);
+//   rung 2  T = 4 (64 x 64 block, 0.5);
+//   rung 6  T = 8 (128 x 128 block, 0.25).
 // All rungs handle ragged M, N, K: out-of-range loads read zeros, stores are
 // masked.
 #include <cstdint>
@@ -64,15 +75,17 @@ __global__ void __launch_bounds__(TILE *TILE)
 }
 
 constexpr int RT = 16;       // threads per side
-constexpr int TM = 4, TN = 4;
-constexpr int BM = RT * TM;  // 64
-constexpr int BN = RT * TN;  // 64
 constexpr int BK = 16;
 
+// T x T outputs per thread (the page's kernel has T = 4: a 64 x 64 block).
+template <int T>
 __global__ void __launch_bounds__(RT *RT)
     register_tiled_kernel(int M, int N, int K, const float *__restrict__ A,
                           const float *__restrict__ B, float *__restrict__ C)
 {
+    constexpr int TM = T, TN = T;
+    constexpr int BM = RT * TM;
+    constexpr int BN = RT * TN;
     __shared__ float sA[BM][BK];
     __shared__ float sB[BK][BN];
     const int ty = threadIdx.y, tx = threadIdx.x;
@@ -134,7 +147,10 @@ cudaError_t launch_sgemm_ladder(int rung, int M, int N, int K, const float *A, c
 {
     using namespace ladder;
     // Grids are (N / tile) x (M / tile); the y extent is limited to 65535.
-    const int tile = rung == 0 ? 16 : rung == 1 ? TILE : BM;
+    static const int kTile[7] = {16, TILE, RT * 4, 0, RT * 1, RT * 2, RT * 8};
+    if (rung < 0 || rung > 6 || rung == 3)
+        return cudaErrorInvalidValue;
+    const int tile = kTile[rung];
     if ((M + tile - 1) / tile > 65535)
         return cudaErrorInvalidValue;
     switch (rung) {
@@ -148,9 +164,19 @@ cudaError_t launch_sgemm_ladder(int rung, int M, int N, int K, const float *A, c
         shared_tiled_kernel<<<grid, dim3(TILE, TILE), 0, stream>>>(M, N, K, A, B, C);
         break;
     }
-    case 2: {
-        dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-        register_tiled_kernel<<<grid, dim3(RT, RT), 0, stream>>>(M, N, K, A, B, C);
+    case 2:
+    case 4:
+    case 5:
+    case 6: {
+        dim3 grid((N + tile - 1) / tile, (M + tile - 1) / tile);
+        if (rung == 2)
+            register_tiled_kernel<4><<<grid, dim3(RT, RT), 0, stream>>>(M, N, K, A, B, C);
+        else if (rung == 4)
+            register_tiled_kernel<1><<<grid, dim3(RT, RT), 0, stream>>>(M, N, K, A, B, C);
+        else if (rung == 5)
+            register_tiled_kernel<2><<<grid, dim3(RT, RT), 0, stream>>>(M, N, K, A, B, C);
+        else
+            register_tiled_kernel<8><<<grid, dim3(RT, RT), 0, stream>>>(M, N, K, A, B, C);
         break;
     }
     default:

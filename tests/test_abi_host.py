@@ -108,7 +108,7 @@ def test_f32_alignment_rule(lib):
 def test_ladder_rung_range(lib):
     f = lib.gemm_f32_ladder
     assert f(-1, 8, 8, 8, FAKE, FAKE, FAKE * 4, None) == -1
-    assert f(4, 8, 8, 8, FAKE, FAKE, FAKE * 4, None) == -1
+    assert f(7, 8, 8, 8, FAKE, FAKE, FAKE * 4, None) == -1
     assert f(1, -8, 8, 8, FAKE, FAKE, FAKE * 4, None) == -1
     assert f(2, 0, 8, 8, None, None, None, None) == 0
 

@@ -1,4 +1,4 @@
-"""GPU parity tests of the ablation ladder (gemm_f32_ladder rungs 0-3) against
+"""GPU parity tests of the ablation ladder (gemm_f32_ladder rungs 0-6) against
 the CPU oracle, through the C ABI."""
 
 import pytest
@@ -25,7 +25,7 @@ def run(rung, A, B):
     return C
 
 
-@pytest.mark.parametrize("rung", [0, 1, 2, 3])
+@pytest.mark.parametrize("rung", [0, 1, 2, 3, 4, 5, 6])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (1000, 1000, 999), (67, 130, 33), (1, 1, 1),
                                    (129, 65, 300)])
 def test_ladder_parity(rung, M, N, K):
@@ -33,13 +33,13 @@ def test_ladder_parity(rung, M, N, K):
     assert_close_to_oracle(run(rung, A, B), A, B, "f32")
 
 
-@pytest.mark.parametrize("rung", [0, 1, 2, 3])
+@pytest.mark.parametrize("rung", [0, 1, 2, 3, 4, 5, 6])
 def test_ladder_small_integer_bit_exact(rung):
     A, B = small_int_inputs(97, 131, 77, seed=5 + rung)
     assert_bit_exact(run(rung, A, B), (A.to(torch.int64) @ B.to(torch.int64)).numpy())
 
 
-@pytest.mark.parametrize("rung", [0, 1, 2])
+@pytest.mark.parametrize("rung", [0, 1, 2, 4, 5, 6])
 def test_ladder_k_zero(rung):
     C = torch.full((9, 7), 1.0, device=DEV)
     rtm.gemm_f32_ladder(rung, torch.empty(9, 0, device=DEV), torch.empty(0, 7, device=DEV), out=C)
@@ -51,5 +51,5 @@ def test_ladder_1024_workload_all_rungs_agree_with_oracle():
     w = workloads.WORKLOADS["f32_1024_uniform"]
     A, B = workloads.workload_inputs(w)
     C0, S = oracle.gemm(A, B)
-    for rung in range(4):
+    for rung in range(7):
         assert_close_to_oracle(run(rung, A, B), A, B, "f32")
