@@ -227,10 +227,26 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
         }
         return finish(rtm::launch_gemm_tc_any(L, s));
     }
-    // One CTA per 128 x 256 tile.
+    // One CTA per 128 x BN tile. With M <= 128 there is one row of tiles, so
+    // the widest BN that still gives 60 % of the SMs a tile is used (a sweep
+    // of BN 256/128/64 over N = 1K..32K, K = 1K..8K on GB300 found it within
+    // 1 % of the best width; 128 x 8192 x 8192: 56.0 us at BN 256, 41.5 at 64),
+    // but with at most 16 CTAs per row of A: every CTA reads all of A, and
+    // more CTAs on one 128-byte line per K-slice queue at its L2 slice
+    // (x 8192 x 8192 at BN 64: M = 1 63.1 us, against 52.6 at BN 256;
+    // M = 4 53.6 us; M = 8 and up 42 us).
     if (!tma_ok)
         return finish(rtm::launch_gemm_tc_any(L, s));
-    return finish(rtm::launch_gemm_bf16_tc(L, s));
+    int bn = 64;
+    for (int w : {256, 128}) {
+        if ((N + w - 1) / w * 10 >= (int64_t)d.sms * 6) {
+            bn = w;
+            break;
+        }
+    }
+    while (bn < 256 && (N + bn - 1) / bn > 16 * M)
+        bn *= 2;
+    return finish(rtm::launch_gemm_bf16_tc_bn(L, bn, s));
 }
 
 } // namespace

@@ -356,11 +356,6 @@ cudaError_t launch_bn(const TcLaunch &L, cudaStream_t stream)
 
 } // namespace tc
 
-cudaError_t launch_gemm_bf16_tc(const TcLaunch &L, cudaStream_t stream)
-{
-    return launch_gemm_bf16_tc_bn(L, 256, stream);
-}
-
 cudaError_t launch_gemm_bf16_tc_bn(const TcLaunch &L, int bn, cudaStream_t stream)
 {
     switch (bn) {

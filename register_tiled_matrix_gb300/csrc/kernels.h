@@ -76,9 +76,8 @@ struct TcLaunch {
     int64_t lda = 0;     // row stride of A in elements (0: K); CTA-pair kernel only
     int64_t ldb = 0;     // row stride of B in elements (0: N); CTA-pair kernel only
 };
-cudaError_t launch_gemm_bf16_tc(const TcLaunch &p, cudaStream_t stream);
-// The same single-CTA kernel with 128 x bn tiles, bn in {256, 128, 64}
-// (narrower tiles give short, wide products more CTAs).
+// The single-CTA kernel with 128 x bn tiles, bn in {256, 128, 64} (narrower
+// tiles give short, wide products more CTAs).
 cudaError_t launch_gemm_bf16_tc_bn(const TcLaunch &p, int bn, cudaStream_t stream);
 // The same product on CTA pairs (gemm_tc2.cu, tcgen05 cta_group::2, 256 x 256
 // tiles); used for M > 128, where a pair tile is not mostly empty. A and B

@@ -177,3 +177,24 @@ def test_single_cta_and_pair_boundary(M, N, K):
     """M <= 128 runs the single-CTA kernel, M > 128 the CTA pair: both near the switch."""
     A, B = bf16_inputs(M, N, K, seed=M * N)
     assert_close_to_oracle(run(A, B), A, B, "bf16")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 2048, 1024), (1, 8192, 512), (2, 8192, 256),
+                                   (77, 16384, 256), (128, 32768, 128), (16, 2056, 520)])
+def test_short_wide_tile_widths(M, N, K):
+    """M <= 128: the single-CTA kernel with 128 x 64, 128 x 128 or 128 x 256
+    tiles depending on N and M (64, 256, 256, 128, 256 and 64 here on a
+    152-SM GPU)."""
+    A, B = bf16_inputs(M, N, K, seed=M + N + 3 * K)
+    full = M * N * K <= (1 << 31)
+    assert_close_to_oracle(run(A, B), A, B, "bf16", full=full, seed=N)
+
+
+@pytest.mark.parametrize("M,N,K", [(100, 2056, 136), (128, 16392, 64)])
+def test_short_wide_guard_band(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=48)
+    buf, C = guarded_output(M, N, DEV, pad=4096)
+    rtm.gemm_bf16f32(A.to(DEV), B.to(DEV), out=C)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N)
+    assert_close_to_oracle(C, A, B, "bf16", full=M * N * K <= (1 << 31), seed=K)
