@@ -44,6 +44,13 @@
  * only library state is a per-device cache (SM count, driver entry point,
  * kernel attributes) and one device error word per device, both set up on
  * first use.
+ *
+ * CUDA graphs. After a first call of the same kind on the device (which fills
+ * that cache), calls of gemm_f32, gemm_f32_ws, gemm_bf16f32, gemm_f16f32,
+ * gemm_bf16f32_ws and gemm_f16f32_ws only enqueue kernels on `stream`: they
+ * can be recorded by stream capture and replayed; the pointers, sizes and
+ * workspace are fixed at capture. gemm_get_device_error synchronises and
+ * must not be called while its stream is being captured.
  */
 #ifndef REGISTER_TILED_GEMM_H
 #define REGISTER_TILED_GEMM_H
