@@ -187,7 +187,10 @@ GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * register tile; "寄存器Tiling跨架构解析", sections 2.1 and 6). For M > 128 a
  * cluster of two CTAs computes each 256 x 256 tile with the two-SM MMA
  * (each SM stages half of A and half of B); for M <= 128 one CTA per
- * 128 x 256 tile.
+ * 128 x 256, 128 x 128 or 128 x 64 tile, or, when K >= 2048, the transposed
+ * product C^T = B^T.A^T with K split over the CTAs of a cluster (the long
+ * operand B on the MMA's 128-row side; the partial sums are added in a fixed
+ * order, so results repeat exactly from call to call).
  *
  * A and B hold raw bfloat16 bit patterns (uint16_t), 2-byte aligned; C is
  * 4-byte aligned (else GEMM_ERR_ALIGNMENT). Any M, N, K. When the rows of A

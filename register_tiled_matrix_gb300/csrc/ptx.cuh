@@ -259,6 +259,18 @@ __device__ __forceinline__ void cluster_sync()
                      : "memory");
 }
 
+// 16-byte load from the shared memory of a CTA of this cluster
+// (shared::cluster address, e.g. from mapa_shared).
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank)
 {

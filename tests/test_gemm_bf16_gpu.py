@@ -198,3 +198,67 @@ def test_short_wide_guard_band(M, N, K):
     torch.cuda.synchronize()
     assert guard_intact(buf, M, N)
     assert_close_to_oracle(C, A, B, "bf16", full=M * N * K <= (1 << 31), seed=K)
+
+
+# M <= 128, K >= 2048, at most one 128-column tile per SM: C^T = B^T.A^T on the
+# tensor cores, K split over S CTAs of a cluster (S for a 152-SM GPU noted).
+@pytest.mark.parametrize("M,N,K", [(1, 8192, 4096),      # S = 2
+                                   (8, 1024, 8192),      # S = 8
+                                   (33, 4096, 2048),     # S = 2
+                                   (64, 2056, 2048),     # S = 2, ragged N
+                                   (100, 1000, 8200),    # S = 8, ragged N and K
+                                   (128, 8192, 2048),    # S = 2
+                                   (97, 19456, 2048)])   # S = 1, 152 tiles
+def test_transposed_short_wide(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=M * 13 + N + K)
+    full = M * N * K <= (1 << 31)
+    assert_close_to_oracle(run(A, B), A, B, "bf16", full=full, seed=M + K)
+
+
+def test_transposed_full_size_sampled():
+    M, N, K = 128, 8192, 8192
+    A, B = bf16_inputs(M, N, K, seed=49)
+    assert_close_to_oracle(run(A, B), A, B, "bf16", full=False, seed=49)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 1024, 4096), (128, 2048, 2048)])
+def test_transposed_small_integer_bit_exact(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "int", "f32", seed=M + N + K)
+    C = run(A.to(torch.bfloat16), B.to(torch.bfloat16))
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_transposed_guard_band_and_repeatability():
+    M, N, K = 50, 1000, 4096
+    A, B = bf16_inputs(M, N, K, seed=50)
+    buf, C = guarded_output(M, N, DEV, pad=4096)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    rtm.gemm_bf16f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_bf16f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N)
+    assert torch.equal(C, C2), "the cluster's rank-ordered sum is the same on every call"
+    assert_close_to_oracle(C, A, B, "bf16")
+
+
+def test_transposed_f16():
+    M, N, K = 32, 2048, 4096
+    A, B = workloads.make_inputs(M, N, K, "normal", "f16", seed=51)
+    C = rtm.gemm_f16f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "bf16")
+
+
+def test_transposed_bounded_wait_gives_up_and_context_survives():
+    """64 x 4096 x 4096 runs the transposed kernel with K split over clusters
+    of four CTAs; with the loads muted every CTA's waits run out, every thread
+    still reaches both cluster barriers, and the next product is correct."""
+    A, B = bf16_inputs(64, 4096, 4096, seed=52)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = torch.empty(64, 4096, device=DEV)
+    assert rtm.get_device_error() == 0
+    rtm.gemm_bf16f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
+    assert rtm.get_device_error() == -4
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(run(A, B), A, B, "bf16", full=False, seed=52)
