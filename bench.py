@@ -578,9 +578,19 @@ def run_configs(args) -> Optional[Dict]:
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / args.steps
 
-    names = args.config_names.split(",") if args.config_names else list(workloads.WORKLOADS)
-    for name in names:
-        w = workloads.WORKLOADS[name]
+    if args.shapes:
+        todo = []
+        for i, spec in enumerate(args.shapes.split(",")):
+            dims, _, dt = spec.partition(":")
+            M, N, K = (int(x) for x in dims.split("x"))
+            dt = dt or "f32"
+            todo.append(workloads.Workload(f"{dt}_{M}x{N}x{K}", M, N, K, dt, "normal",
+                                           workloads.SEED_BASE + 1000 + i, False))
+    else:
+        names = args.config_names.split(",") if args.config_names else list(workloads.WORKLOADS)
+        todo = [workloads.WORKLOADS[name] for name in names]
+    for w in todo:
+        name = w.name
         A, B = workloads.workload_inputs(w)
         A, B = A.cuda(), B.cuda()
         C = torch.empty(w.M, w.N, device="cuda")
@@ -639,6 +649,8 @@ def main(argv=None):
                    help="time every configuration's product (report only)")
     p.add_argument("--config-names", default=None,
                    help="comma-separated workload names for --configs (default: all)")
+    p.add_argument("--shapes", default=None,
+                   help="--configs on these products instead, e.g. 16x8192x8192:bf16,4096x4096x4096:f32")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
