@@ -197,6 +197,15 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
         // and B rows must start on 16-byte boundaries, directly or in copies.
         const int64_t need = (a_rows16 ? 0 : padded_copy_bytes(M, K)) +
                              (b_rows16 ? 0 : padded_copy_bytes(K, N));
+        // Tall and narrow (N <= 256) with long K: A streams through 128-row
+        // tiles with K split over a cluster, as for short, wide products.
+        const int64_t s_tiles = (M + 127) / 128 * ((N + rtm::tcs_cols((int)N) - 1) / rtm::tcs_cols((int)N));
+        if (need == 0 && N <= 256 && K >= 2048 && s_tiles <= d.sms) {
+            int splits = 1;
+            while (splits < 8 && s_tiles * splits * 2 <= d.sms && K / (splits * 2) >= 1024)
+                splits *= 2;
+            return finish(rtm::launch_gemm_tc_t(L, splits, false, s));
+        }
         if (need == 0)
             return finish(rtm::launch_gemm_tc_pair(L, s));
         uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -248,7 +257,7 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
         int splits = 1;
         while (splits < 8 && t_tiles * splits * 2 <= d.sms && K / (splits * 2) >= 1024)
             splits *= 2;
-        return finish(rtm::launch_gemm_tc_t(L, splits, s));
+        return finish(rtm::launch_gemm_tc_t(L, splits, true, s));
     }
     int bn = 64;
     for (int w : {256, 128}) {

@@ -29,6 +29,13 @@
 //    the sum is the same on every run), and stores them; a second cluster
 //    barrier keeps every partial alive until all have been read.
 //
+// The same kernel without the swap (SWAP = false) serves tall, narrow
+// products (many rows of A, N <= 256): A fills the MMA's 128-row side
+// (K-major), B the N side (MN = 64 or 128 columns, MN-major; 256 columns
+// are two tiles, which measured the same as one 256-wide tile with half the
+// stages), TMEM lane i is row m0 + i of C, and K is split over a cluster the
+// same way.
+//
 // Every mbarrier wait is bounded in time; a warp that gives up records
 // GEMM_ERR_TIMEOUT in the device error word and every thread still reaches
 // both cluster barriers.
@@ -42,16 +49,16 @@
 namespace rtm {
 namespace tct {
 
-constexpr int BNT = 128;  // columns of C per CTA (the MMA's M)
+constexpr int BNT = 128;  // the MMA's M: columns of C per CTA (SWAP) or rows (no swap)
 constexpr int BK = 64;    // 64 16-bit values = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr uint32_t B_ATOM_BYTES = 64 * BK * 2;     // 8 KB: 64 k-rows x 64 n
-constexpr uint32_t BT_BYTES = BNT * BK * 2;        // 16 KB of B per stage
+constexpr uint32_t BT_BYTES = BNT * BK * 2;        // 16 KB per stage on the MMA's 128-row side
 
 template <int MN>
 struct Cfg {
-    static constexpr uint32_t AT_BYTES = MN * BK * 2;  // 4, 8 or 16 KB of A per stage
+    static constexpr uint32_t AT_BYTES = MN * BK * 2;  // 4, 8 or 16 KB per stage on the N side
     static constexpr uint32_t STAGE_BYTES = BT_BYTES + AT_BYTES;
     static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;  // 10, 8 or 6
     static constexpr int PITCH = MN + 4;  // floats per row of a partial tile in shared memory
@@ -61,13 +68,15 @@ struct Cfg {
     static_assert(PART_BYTES <= STAGES * STAGE_BYTES, "partial tile must fit the stage ring");
 };
 
-// kind::f16: D fp32, A and B both bf16 (1) or both fp16 (0), A (= B^T)
-// MN-major, B (= A^T) K-major, N = MN, M = 128.
-template <bool F16, int MN>
+// kind::f16: D fp32, A and B both bf16 (1) or both fp16 (0), N = MN, M = 128.
+// SWAP: the MMA's A (= B^T) MN-major, its B (= A^T) K-major; otherwise A
+// K-major and B MN-major.
+template <bool F16, int MN, bool SWAP>
 __host__ __device__ constexpr uint32_t idesc()
 {
-    return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) | (1u << 15) |
-           (0u << 16) | ((uint32_t)(MN >> 3) << 17) | ((uint32_t)(BNT >> 4) << 24);
+    return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) |
+           ((SWAP ? 1u : 0u) << 15) | ((SWAP ? 0u : 1u) << 16) | ((uint32_t)(MN >> 3) << 17) |
+           ((uint32_t)(BNT >> 4) << 24);
 }
 
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
@@ -83,6 +92,7 @@ struct Params {
     unsigned long long limit_ns;
     int splits;         // CTAs per cluster, each summing one K-range
     int mute_producer;  // failure-detection self-test: issue no loads
+    int c_vec;          // C rows 16-byte aligned (float4 row stores without the swap)
 };
 
 __device__ __forceinline__ void give_up(int *err, volatile int *abort)
@@ -91,7 +101,7 @@ __device__ __forceinline__ void give_up(int *err, volatile int *abort)
     *abort = 1;
 }
 
-template <bool F16, int MN>
+template <bool F16, int MN, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tct_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p)
@@ -112,9 +122,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = p.splits;
     const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
     const int unit = blockIdx.x / S;
-    const int tiles_n = (p.N + BNT - 1) / BNT;
-    const int n0 = (unit % tiles_n) * BNT;
-    const int m0 = (unit / tiles_n) * MN;
+    int m0, n0;
+    if constexpr (SWAP) {
+        const int tiles_n = (p.N + BNT - 1) / BNT;
+        n0 = (unit % tiles_n) * BNT;
+        m0 = (unit / tiles_n) * MN;
+    } else {
+        const int tiles_m = (p.M + BNT - 1) / BNT;
+        m0 = (unit % tiles_m) * BNT;
+        n0 = (unit / tiles_m) * MN;
+    }
     const int kblocks = (p.K + BK - 1) / BK;
     const int per = (kblocks + S - 1) / S;
     const int kb_begin = min(kblocks, (int)rank * per);
@@ -151,12 +168,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     give_up(p.err, abort);
                     break;
                 }
-                const uint32_t sbt = smem_u32(smem + stage * Cf::STAGE_BYTES);
-                const uint32_t sat = sbt + BT_BYTES;
+                const uint32_t sbig = smem_u32(smem + stage * Cf::STAGE_BYTES);
+                const uint32_t ssmall = sbig + BT_BYTES;
                 mbar_arrive_expect_tx(&full[stage], Cf::STAGE_BYTES);
-                tma_load_2d(sbt, &tmB, &full[stage], n0, kb * BK);
-                tma_load_2d(sbt + B_ATOM_BYTES, &tmB, &full[stage], n0 + 64, kb * BK);
-                tma_load_2d(sat, &tmA, &full[stage], kb * BK, m0);
+                if constexpr (SWAP) {
+                    tma_load_2d(sbig, &tmB, &full[stage], n0, kb * BK);
+                    tma_load_2d(sbig + B_ATOM_BYTES, &tmB, &full[stage], n0 + 64, kb * BK);
+                    tma_load_2d(ssmall, &tmA, &full[stage], kb * BK, m0);
+                } else {
+                    tma_load_2d(sbig, &tmA, &full[stage], kb * BK, m0);
+#pragma unroll
+                    for (int j = 0; j < MN / 64; ++j)
+                        tma_load_2d(ssmall + j * B_ATOM_BYTES, &tmB, &full[stage], n0 + 64 * j,
+                                    kb * BK);
+                }
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) {
@@ -183,15 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sbt = smem_u32(smem + stage * Cf::STAGE_BYTES);
-                const uint32_t sat = sbt + BT_BYTES;
+                const uint32_t sbig = smem_u32(smem + stage * Cf::STAGE_BYTES);
+                const uint32_t ssmall = sbig + BT_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                    // A = B^T: N-major, 64-wide atoms B_ATOM_BYTES apart, 16 k-rows per step.
-                    // B = A^T: K-major rows of 128 B, 8-row groups 1024 B apart, 32 B per step.
-                    const uint64_t adesc = sdesc_sw128(sbt + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
-                    const uint64_t bdesc = sdesc_sw128(sat + kk * UMMA_K * 2, 16, 1024);
-                    umma_f16(tmem_base, adesc, bdesc, idesc<F16, MN>(),
+                    // MN-major side: 64-wide atoms B_ATOM_BYTES apart, 16 k-rows per step.
+                    // K-major side: rows of 128 B, 8-row groups 1024 B apart, 32 B per step.
+                    uint64_t adesc, bdesc;
+                    if constexpr (SWAP) {
+                        adesc = sdesc_sw128(sbig + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
+                        bdesc = sdesc_sw128(ssmall + kk * UMMA_K * 2, 16, 1024);
+                    } else {
+                        adesc = sdesc_sw128(sbig + kk * UMMA_K * 2, 16, 1024);
+                        bdesc = sdesc_sw128(ssmall + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
+                    }
+                    umma_f16(tmem_base, adesc, bdesc, idesc<F16, MN, SWAP>(),
                              (kb != kb_begin || kk != 0) ? 1u : 0u);
                 }
                 issued_any = true;
@@ -211,8 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;  // TMEM lane = column n0 + row of C
-        const int gn = n0 + row;
+        const int row = quarter * 32 + lane;  // TMEM lane: column n0 + row (SWAP) or row m0 + row of C
         const bool have = kb_end > kb_begin;
         bool ok = true;
         if (have && !mbar_wait_bounded(done, 0, limit, abort)) {
@@ -228,13 +258,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, r);
                     tmem_wait_ld();
-                    const int rows = min(32, p.M - (m0 + c * 32));
-                    if (gn < p.N) {
-                        float *cp = p.C + (size_t)(m0 + c * 32) * p.N + gn;
+                    if constexpr (SWAP) {
+                        const int gn = n0 + row;
+                        const int rows = min(32, p.M - (m0 + c * 32));
+                        if (gn < p.N) {
+                            float *cp = p.C + (size_t)(m0 + c * 32) * p.N + gn;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < rows)
-                                cp[(size_t)j * p.N] = __uint_as_float(r[j]);
+                            for (int j = 0; j < 32; ++j)
+                                if (j < rows)
+                                    cp[(size_t)j * p.N] = __uint_as_float(r[j]);
+                        }
+                    } else {
+                        const int gm = m0 + row;
+                        const int col = n0 + c * 32;
+                        if (gm < p.M) {
+                            float *cp = p.C + (size_t)gm * p.N + col;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                if (p.c_vec && col + 4 * v + 3 < p.N) {
+                                    *reinterpret_cast<float4 *>(cp + 4 * v) = make_float4(
+                                        __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if (col + 4 * v + e < p.N)
+                                            cp[4 * v + e] = __uint_as_float(r[4 * v + e]);
+                                }
+                            }
+                        }
                     }
                 }
             }
@@ -263,7 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // every partial tile of the cluster is in shared memory
         if (warp >= 2) {
             const int row = (warp & 3) * 32 + lane;
-            const int gn = n0 + row;
             const int cols = MN / S;
             const int c0 = (int)rank * cols;
             const uint32_t mine = smem_u32(smem) + (uint32_t)(row * Cf::PITCH) * 4u;
@@ -277,13 +328,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc.z += v.z;
                     acc.w += v.w;
                 }
-                const int gm = m0 + c0 + cc;
-                if (gn < p.N) {
-                    float *cp = p.C + (size_t)gm * p.N + gn;
-                    if (gm + 0 < p.M) cp[0] = acc.x;
-                    if (gm + 1 < p.M) cp[(size_t)p.N] = acc.y;
-                    if (gm + 2 < p.M) cp[(size_t)2 * p.N] = acc.z;
-                    if (gm + 3 < p.M) cp[(size_t)3 * p.N] = acc.w;
+                if constexpr (SWAP) {
+                    const int gn = n0 + row;
+                    const int gm = m0 + c0 + cc;
+                    if (gn < p.N) {
+                        float *cp = p.C + (size_t)gm * p.N + gn;
+                        if (gm + 0 < p.M) cp[0] = acc.x;
+                        if (gm + 1 < p.M) cp[(size_t)p.N] = acc.y;
+                        if (gm + 2 < p.M) cp[(size_t)2 * p.N] = acc.z;
+                        if (gm + 3 < p.M) cp[(size_t)3 * p.N] = acc.w;
+                    }
+                } else {
+                    const int gm = m0 + row;
+                    const int gn = n0 + c0 + cc;
+                    if (gm < p.M) {
+                        float *cp = p.C + (size_t)gm * p.N + gn;
+                        if (p.c_vec && gn + 3 < p.N) {
+                            *reinterpret_cast<float4 *>(cp) = acc;
+                        } else {
+                            if (gn + 0 < p.N) cp[0] = acc.x;
+                            if (gn + 1 < p.N) cp[1] = acc.y;
+                            if (gn + 2 < p.N) cp[2] = acc.z;
+                            if (gn + 3 < p.N) cp[3] = acc.w;
+                        }
+                    }
                 }
             }
         }
@@ -317,7 +385,7 @@ static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, uin
     return r == CUDA_SUCCESS;
 }
 
-template <bool F16, int MN>
+template <bool F16, int MN, bool SWAP>
 static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
 {
     using Cf = Cfg<MN>;
@@ -325,19 +393,20 @@ static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
     if (!fn)
         return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
-    // A: M x K, boxes of MN rows x 64 k; B: K x N, boxes of 64 k-rows x 64 n.
-    if (!encode_map(fn, &ta, L.A, (uint64_t)L.M, (uint64_t)L.K, MN, F16) ||
+    // A: M x K, boxes of 64 k x (MN rows with the swap, 128 without);
+    // B: K x N, boxes of 64 k-rows x 64 n.
+    if (!encode_map(fn, &ta, L.A, (uint64_t)L.M, (uint64_t)L.K, SWAP ? MN : BNT, F16) ||
         !encode_map(fn, &tb, L.B, (uint64_t)L.K, (uint64_t)L.N, BK, F16))
         return cudaErrorInvalidValue;
-    auto kernel = gemm_tct_kernel<F16, MN>;
+    auto kernel = gemm_tct_kernel<F16, MN, SWAP>;
     static std::atomic<uint64_t> done{0};
     cudaError_t e = set_smem_limit_once(kernel, (int)Cf::SMEM_BYTES, done);
     if (e != cudaSuccess)
         return e;
-    const long long units =
-        (long long)((L.N + BNT - 1) / BNT) * ((L.M + MN - 1) / MN) * (long long)splits;
+    const long long tiles = SWAP ? (long long)((L.N + BNT - 1) / BNT) * ((L.M + MN - 1) / MN)
+                                 : (long long)((L.M + BNT - 1) / BNT) * ((L.N + MN - 1) / MN);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)units, 1, 1);
+    cfg.gridDim = dim3((unsigned)(tiles * splits), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
     cfg.stream = stream;
@@ -348,8 +417,9 @@ static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const int c_vec = (L.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0);
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, splits,
-             L.mute_producer};
+             L.mute_producer, c_vec};
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
 }
 
@@ -360,19 +430,32 @@ int tct_rows(int M)
     return M <= 32 ? 32 : M <= 64 ? 64 : 128;
 }
 
-cudaError_t launch_gemm_tc_t(const TcLaunch &L, int splits, cudaStream_t stream)
+int tcs_cols(int N)
+{
+    return N <= 64 ? 64 : 128;
+}
+
+cudaError_t launch_gemm_tc_t(const TcLaunch &L, int splits, bool swap, cudaStream_t stream)
 {
     using namespace tct;
     if (splits != 1 && splits != 2 && splits != 4 && splits != 8)
         return cudaErrorInvalidValue;
-    const int mn = tct_rows(L.M);
+    if (swap) {
+        const int mn = tct_rows(L.M);
+        if (L.f16)
+            return mn == 32 ? launch_mn<true, 32, true>(L, splits, stream)
+                   : mn == 64 ? launch_mn<true, 64, true>(L, splits, stream)
+                              : launch_mn<true, 128, true>(L, splits, stream);
+        return mn == 32 ? launch_mn<false, 32, true>(L, splits, stream)
+               : mn == 64 ? launch_mn<false, 64, true>(L, splits, stream)
+                          : launch_mn<false, 128, true>(L, splits, stream);
+    }
+    const int mn = tcs_cols(L.N);
     if (L.f16)
-        return mn == 32 ? launch_mn<true, 32>(L, splits, stream)
-               : mn == 64 ? launch_mn<true, 64>(L, splits, stream)
-                          : launch_mn<true, 128>(L, splits, stream);
-    return mn == 32 ? launch_mn<false, 32>(L, splits, stream)
-           : mn == 64 ? launch_mn<false, 64>(L, splits, stream)
-                      : launch_mn<false, 128>(L, splits, stream);
+        return mn == 64 ? launch_mn<true, 64, false>(L, splits, stream)
+                        : launch_mn<true, 128, false>(L, splits, stream);
+    return mn == 64 ? launch_mn<false, 64, false>(L, splits, stream)
+                    : launch_mn<false, 128, false>(L, splits, stream);
 }
 
 } // namespace rtm

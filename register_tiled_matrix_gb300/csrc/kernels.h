@@ -91,12 +91,15 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &p, cudaStream_t stream);
 // (pack.cu). Values in columns cols .. ld-1 of dst are unspecified.
 cudaError_t launch_pack_rows_2b(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst,
                                 int64_t ld, int sm_count, cudaStream_t stream);
-// Short, wide products as C^T = B^T.A^T (gemm_tc_t.cu): CTAs own 128 columns
-// of C and tct_rows(M) (32, 64 or 128) rows; `splits` (1, 2, 4 or 8) CTAs of
-// a cluster split K and sum their partial tiles in rank order. Same operand
-// rules as launch_gemm_bf16_tc_bn (rows on 16-byte boundaries).
+// Products with one short side and K split over CTA clusters (gemm_tc_t.cu).
+// swap: short, wide products as C^T = B^T.A^T, CTAs own 128 columns of C and
+// tct_rows(M) (32, 64 or 128) rows. No swap: tall, narrow products, CTAs own
+// 128 rows and tcs_cols(N) (64 or 128) columns. `splits` (1, 2, 4 or 8)
+// CTAs of a cluster split K and sum their partial tiles in rank order. Same
+// operand rules as launch_gemm_bf16_tc_bn (rows on 16-byte boundaries).
 int tct_rows(int M);
-cudaError_t launch_gemm_tc_t(const TcLaunch &p, int splits, cudaStream_t stream);
+int tcs_cols(int N);
+cudaError_t launch_gemm_tc_t(const TcLaunch &p, int splits, bool swap, cudaStream_t stream);
 // The same product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu):
 // operands loaded by producer warps instead of TMA. mute_producer unused.
 cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);

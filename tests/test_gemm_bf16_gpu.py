@@ -262,3 +262,47 @@ def test_transposed_bounded_wait_gives_up_and_context_survives():
     assert rtm.get_device_error() == -4
     assert rtm.get_device_error() == 0
     assert_close_to_oracle(run(A, B), A, B, "bf16", full=False, seed=52)
+
+
+# M > 128, N <= 256, K >= 2048: A on the MMA's 128-row side, B (64, 128 or 256
+# columns) on its N side, K split over S CTAs of a cluster (S for 152 SMs).
+@pytest.mark.parametrize("M,N,K", [(8192, 64, 4096),    # S = 2
+                                   (4096, 100, 8192),   # S = 4, ragged N, scalar C rows
+                                   (2000, 256, 2048),   # S = 2, 256 columns
+                                   (300, 8, 4096),      # S = 4
+                                   (19456, 200, 2048),  # S = 1, 152 tiles
+                                   (1000, 136, 8200)])  # S = 8, ragged K
+def test_tall_narrow(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=M + 5 * N + K)
+    full = M * N * K <= (1 << 31)
+    assert_close_to_oracle(run(A, B), A, B, "bf16", full=full, seed=N + K)
+
+
+def test_tall_narrow_small_integer_bit_exact():
+    A, B = workloads.make_inputs(1024, 64, 4096, "int", "f32", seed=53)
+    C = run(A.to(torch.bfloat16), B.to(torch.bfloat16))
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_tall_narrow_guard_band_and_repeatability():
+    M, N, K = 500, 72, 4096
+    A, B = bf16_inputs(M, N, K, seed=54)
+    buf, C = guarded_output(M, N, DEV, pad=4096)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    rtm.gemm_bf16f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_bf16f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N)
+    assert torch.equal(C, C2)
+    assert_close_to_oracle(C, A, B, "bf16")
+
+
+def test_tall_narrow_bounded_wait_gives_up_and_context_survives():
+    A, B = bf16_inputs(2048, 128, 4096, seed=55)  # clusters of four CTAs
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = torch.empty(2048, 128, device=DEV)
+    assert rtm.get_device_error() == 0
+    rtm.gemm_bf16f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
+    assert rtm.get_device_error() == -4
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(run(A, B), A, B, "bf16", full=False, seed=55)
