@@ -81,3 +81,29 @@ def test_fuzz_tensor_core(entry, M, N, K):
     torch.cuda.synchronize()
     assert rtm.get_device_error() == 0
     assert_close_to_oracle(C, A, B, "bf16")
+
+
+def _long_k_shapes(seed, count):
+    """Long K (2048..3072, a multiple of 8) with one short side: the kernel that
+    splits K over a cluster, in both orientations."""
+    rng = random.Random(seed)
+    out = []
+    for i in range(count):
+        K = 8 * rng.randint(256, 384)
+        if i % 2 == 0:   # short, wide
+            M, N = rng.randint(1, 128), 8 * rng.randint(1, 256)
+        else:            # tall, narrow
+            M, N = rng.randint(129, 1500), 8 * rng.randint(1, 32)
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", _long_k_shapes(2026, 8))
+def test_fuzz_long_k_one_short_side(dtype, M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "normal", dtype, seed=M * 131 + N * 7 + K)
+    fn = rtm.gemm_bf16f32 if dtype == "bf16" else rtm.gemm_f16f32
+    C = fn(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "bf16")
