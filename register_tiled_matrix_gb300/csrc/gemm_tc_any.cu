@@ -13,6 +13,11 @@
 // outside M, N, K. Each producer thread then makes its shared-memory writes
 // visible to the tensor core (fence.proxy.async) and arrives on the stage's
 // barrier. The epilogue stores scalars where C rows are not 16-byte aligned.
+//
+// Loads and stores move V consecutive values at once (V = 1, 2 or 4: 2-, 4-
+// or 8-byte accesses), the largest V for which every row of A and B starts on
+// a 2V-byte boundary (K and N multiples of V, A and B 2V-byte aligned), so a
+// vector never straddles a row end or a 16-byte swizzle chunk.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -87,7 +92,32 @@ __device__ __forceinline__ uint32_t swz(int row, int col)
            ((uint32_t)col & 7u) * 2u;
 }
 
-template <bool F16, bool C_VEC>
+// V consecutive 16-bit values (V = 1, 2 or 4) as one register-sized word.
+template <int V>
+struct Vec;
+template <>
+struct Vec<1> {
+    using T = uint16_t;
+};
+template <>
+struct Vec<2> {
+    using T = uint32_t;
+};
+template <>
+struct Vec<4> {
+    using T = uint2;
+};
+
+template <int V>
+__device__ __forceinline__ typename Vec<V>::T vzero()
+{
+    if constexpr (V == 4)
+        return make_uint2(0u, 0u);
+    else
+        return typename Vec<V>::T(0);
+}
+
+template <bool F16, bool C_VEC, int V>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -149,48 +179,86 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p
                 const int k0 = kb * BK;
                 uint8_t *sA = smem + stage * STAGE_BYTES;
                 uint8_t *sB = sA + A_STAGE_BYTES;
-                // All of this lane's loads for the slice are issued before any
-                // store, so the slice costs one round trip to L2, not dozens.
-                // A: 128 rows x 64 k; warp w fills rows 16w .. 16w+15, lanes run along k.
-                // B: 64 k-rows x 256 n in four 64-column atoms; warp w fills k-rows
-                // 8w .. 8w+7, lanes run along n.
-                constexpr int AR = BM / kProducerWarps, AE = BK / 32;
-                constexpr int BR = BK / kProducerWarps, BE = BN / 32;
-                uint16_t va[AR][AE], vb[BR][BE];
-#pragma unroll
-                for (int rr = 0; rr < AR; ++rr) {
-                    const int gm = m0 + warp * AR + rr;
-#pragma unroll
-                    for (int e = 0; e < AE; ++e) {
-                        const int gk = k0 + e * 32 + lane;
-                        va[rr][e] =
-                            (gm < M && gk < K) ? __ldg(p.A + (size_t)gm * K + gk) : (uint16_t)0;
+                if constexpr (V == 1) {
+                    // All of this lane's loads for the slice are issued before any
+                    // store, so the slice costs one round trip to L2, not dozens.
+                    // A: 128 rows x 64 k; warp w fills rows 16w .. 16w+15, lanes run along k.
+                    // B: 64 k-rows x 256 n in four 64-column atoms; warp w fills k-rows
+                    // 8w .. 8w+7, lanes run along n.
+                    constexpr int AR = BM / kProducerWarps, AE = BK / 32;
+                    constexpr int BR = BK / kProducerWarps, BE = BN / 32;
+                    uint16_t va[AR][AE], vb[BR][BE];
+    #pragma unroll
+                    for (int rr = 0; rr < AR; ++rr) {
+                        const int gm = m0 + warp * AR + rr;
+    #pragma unroll
+                        for (int e = 0; e < AE; ++e) {
+                            const int gk = k0 + e * 32 + lane;
+                            va[rr][e] =
+                                (gm < M && gk < K) ? __ldg(p.A + (size_t)gm * K + gk) : (uint16_t)0;
+                        }
                     }
+    #pragma unroll
+                    for (int kr = 0; kr < BR; ++kr) {
+                        const int gk = k0 + warp * BR + kr;
+    #pragma unroll
+                        for (int e = 0; e < BE; ++e) {
+                            const int gn = n0 + e * 32 + lane;
+                            vb[kr][e] =
+                                (gk < K && gn < N) ? __ldg(p.B + (size_t)gk * N + gn) : (uint16_t)0;
+                        }
+                    }
+    #pragma unroll
+                    for (int rr = 0; rr < AR; ++rr)
+    #pragma unroll
+                        for (int e = 0; e < AE; ++e)
+                            *reinterpret_cast<uint16_t *>(sA + swz(warp * AR + rr, e * 32 + lane)) =
+                                va[rr][e];
+    #pragma unroll
+                    for (int kr = 0; kr < BR; ++kr)
+    #pragma unroll
+                        for (int e = 0; e < BE; ++e) {
+                            const int n = e * 32 + lane;
+                            *reinterpret_cast<uint16_t *>(sB + (n >> 6) * B_ATOM_BYTES +
+                                                          swz(warp * BR + kr, n & 63)) = vb[kr][e];
+                        }
+                } else {
+                    // The same with V values per access: consecutive producer
+                    // threads take consecutive vectors along a row; a thread's
+                    // vectors share one column and step down the rows by a fixed
+                    // stride, so one base pointer per operand serves all.
+                    using W = typename Vec<V>::T;
+                    constexpr int A_ROW = BK / V, A_PER = BM * A_ROW / kProducerThreads;
+                    constexpr int A_STEP = kProducerThreads / A_ROW;  // rows between a thread's vectors
+                    constexpr int B_ROW = BN / V, B_PER = BK * B_ROW / kProducerThreads;
+                    constexpr int B_STEP = kProducerThreads / B_ROW;
+                    const int tid = threadIdx.x;  // 0 .. 255 among the producer warps
+                    const int ar = tid / A_ROW, ac = (tid % A_ROW) * V;
+                    const int br = tid / B_ROW, bc = (tid % B_ROW) * V;
+                    const int gka = k0 + ac, gnb = n0 + bc;
+                    const uint16_t *pa = p.A + (size_t)(m0 + ar) * K + gka;
+                    const uint16_t *pb = p.B + (size_t)(k0 + br) * N + gnb;
+                    W va[A_PER], vb[B_PER];
+    #pragma unroll
+                    for (int j = 0; j < A_PER; ++j) {
+                        const bool in = m0 + ar + j * A_STEP < M && gka < K;
+                        va[j] = in ? __ldg(reinterpret_cast<const W *>(pa + (size_t)j * A_STEP * K))
+                                   : vzero<V>();
+                    }
+    #pragma unroll
+                    for (int j = 0; j < B_PER; ++j) {
+                        const bool in = k0 + br + j * B_STEP < K && gnb < N;
+                        vb[j] = in ? __ldg(reinterpret_cast<const W *>(pb + (size_t)j * B_STEP * N))
+                                   : vzero<V>();
+                    }
+    #pragma unroll
+                    for (int j = 0; j < A_PER; ++j)
+                        *reinterpret_cast<W *>(sA + swz(ar + j * A_STEP, ac)) = va[j];
+    #pragma unroll
+                    for (int j = 0; j < B_PER; ++j)
+                        *reinterpret_cast<W *>(sB + (bc >> 6) * B_ATOM_BYTES + swz(br + j * B_STEP, bc & 63)) =
+                            vb[j];
                 }
-#pragma unroll
-                for (int kr = 0; kr < BR; ++kr) {
-                    const int gk = k0 + warp * BR + kr;
-#pragma unroll
-                    for (int e = 0; e < BE; ++e) {
-                        const int gn = n0 + e * 32 + lane;
-                        vb[kr][e] =
-                            (gk < K && gn < N) ? __ldg(p.B + (size_t)gk * N + gn) : (uint16_t)0;
-                    }
-                }
-#pragma unroll
-                for (int rr = 0; rr < AR; ++rr)
-#pragma unroll
-                    for (int e = 0; e < AE; ++e)
-                        *reinterpret_cast<uint16_t *>(sA + swz(warp * AR + rr, e * 32 + lane)) =
-                            va[rr][e];
-#pragma unroll
-                for (int kr = 0; kr < BR; ++kr)
-#pragma unroll
-                    for (int e = 0; e < BE; ++e) {
-                        const int n = e * 32 + lane;
-                        *reinterpret_cast<uint16_t *>(sB + (n >> 6) * B_ATOM_BYTES +
-                                                      swz(warp * BR + kr, n & 63)) = vb[kr][e];
-                    }
                 fence_proxy_async_shared();
                 mbar_arrive(&full[stage]);
                 if (++stage == STAGES) {
@@ -315,10 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p
     }
 }
 
-template <bool F16, bool C_VEC>
+template <bool F16, bool C_VEC, int V>
 static cudaError_t launch(const TcLaunch &L, cudaStream_t stream)
 {
-    auto kernel = gemm_tc_any_kernel<F16, C_VEC>;
+    auto kernel = gemm_tc_any_kernel<F16, C_VEC, V>;
     static std::atomic<uint64_t> done{0};  // per instantiation
     const cudaError_t e = set_smem_limit_once(kernel, (int)SMEM_BYTES, done);
     if (e != cudaSuccess)
@@ -330,15 +398,28 @@ static cudaError_t launch(const TcLaunch &L, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+template <bool F16, bool C_VEC>
+static cudaError_t launch_v(const TcLaunch &L, int v, cudaStream_t stream)
+{
+    return v == 4 ? launch<F16, C_VEC, 4>(L, stream)
+           : v == 2 ? launch<F16, C_VEC, 2>(L, stream)
+                    : launch<F16, C_VEC, 1>(L, stream);
+}
+
 } // namespace tcany
 
 cudaError_t launch_gemm_tc_any(const TcLaunch &L, cudaStream_t stream)
 {
     using namespace tcany;
     const bool c_vec = (L.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0);
+    // Widest access that keeps every row of A and B aligned to it.
+    const uintptr_t a = reinterpret_cast<uintptr_t>(L.A), b = reinterpret_cast<uintptr_t>(L.B);
+    int v = 4;
+    while (v > 1 && (L.K % v != 0 || L.N % v != 0 || (a % (2 * v)) != 0 || (b % (2 * v)) != 0))
+        v /= 2;
     if (L.f16)
-        return c_vec ? launch<true, true>(L, stream) : launch<true, false>(L, stream);
-    return c_vec ? launch<false, true>(L, stream) : launch<false, false>(L, stream);
+        return c_vec ? launch_v<true, true>(L, v, stream) : launch_v<true, false>(L, v, stream);
+    return c_vec ? launch_v<false, true>(L, v, stream) : launch_v<false, false>(L, v, stream);
 }
 
 } // namespace rtm
