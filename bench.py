@@ -563,6 +563,7 @@ def run_configs(args) -> Optional[Dict]:
     peaks = load_peaks()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * float(peaks.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    hbm = float(peaks.get("hbm_gbs") or 6800.0)
     rows = []
 
     def timed(fn):
@@ -614,9 +615,17 @@ def run_configs(args) -> Optional[Dict]:
         for entry, fn, peak in entries:
             ms = timed(fn)
             tf = w.flops / ms / 1e9
+            # Binding roofline of this product: the larger of its compute time
+            # at the peak and its algorithmic bytes at the measured copy bandwidth.
+            alg_bytes = w.in_bytes + w.out_bytes
+            t_compute = w.flops / (peak * 1e12) * 1e3
+            t_memory = alg_bytes / (hbm * 1e9) * 1e3
+            roof_ms = max(t_compute, t_memory)
             rows.append({"config": name, "M": w.M, "N": w.N, "K": w.K, "entry": entry,
                          "ms": round(ms, 4), "tflops": round(tf, 2),
-                         "frac_of_peak": round(tf / peak, 4)})
+                         "frac_of_peak": round(tf / peak, 4),
+                         "bound": "compute" if t_compute >= t_memory else "hbm",
+                         "roof_ms": round(roof_ms, 4), "frac_of_roofline": round(roof_ms / ms, 4)})
         del A, B, C
         torch.cuda.empty_cache()
     if rtm.get_device_error() != 0:
@@ -624,7 +633,7 @@ def run_configs(args) -> Optional[Dict]:
     return {"metric": "GEMM TFLOP/s per configuration (report only)", "unit": UNIT,
             "steps": args.steps, "warmup": args.warmup,
             "peaks": {"fp32_simt_tflops": round(fp32_peak, 2),
-                      "bf16_tflops_burst": float(peaks["bf16_tflops"])},
+                      "bf16_tflops_burst": float(peaks["bf16_tflops"]), "hbm_gbs": hbm},
             "l2": "back-to-back launches (L2-warm for the smaller configs)", "configs": rows}
 
 
