@@ -92,7 +92,10 @@ typedef enum gemm_status {
  * Any M, N, K >= 0 and any 4-byte-aligned pointers. Each output is a sum of
  * K fp32 products formed with fused multiply-add in an order fixed by the
  * tiling; the error against the exact sum is bounded by a small multiple of
- * K * 2^-24 * sum_k |A[i][k] B[k][j]|.
+ * K * 2^-24 * sum_k |A[i][k] B[k][j]|. Products with M <= 32 use a kernel
+ * whose threads keep a column strip of C in registers and, where that leaves
+ * SMs idle, split K over the CTAs of a cluster, adding the partial sums in a
+ * fixed order (results repeat exactly from call to call); no workspace.
  */
 GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K,
                       const float *A, const float *B, float *C, void *stream);

@@ -147,6 +147,17 @@ bool rows_on_16_bytes(const void *base, int64_t cols)
 // Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
 // CTA-pair kernel run on re-pitched copies of operands whose rows do not start
 // on 16-byte boundaries.
+// The fp32 product without a workspace: column strips for short, wide
+// products (M <= 32, where 128 x 128 tiles would be mostly empty), the
+// register-tiled 128 x 128 (128 x 64) kernel otherwise. K >= 1.
+cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, float *C, int sms,
+                          cudaStream_t s)
+{
+    if (M <= rtm::kShortMaxM)
+        return rtm::launch_sgemm_short(M, N, K, A, B, C, rtm::sgemm_short_splits(M, N, K, sms), s);
+    return rtm::launch_sgemm_f32(M, N, K, A, B, C, s);
+}
+
 int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
              void *stream, uint64_t wait_limit_ns, int mute_producer, int f16 = 0,
              void *workspace = nullptr, int64_t workspace_bytes = 0)
@@ -306,7 +317,7 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B, fl
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return finish(rtm::launch_zero_fill(C, M * N, s));
-    return finish(rtm::launch_sgemm_f32((int)M, (int)N, (int)K, A, B, C, s));
+    return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d.sms, s));
 }
 
 int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
@@ -320,6 +331,8 @@ int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
     const int st = current_device(&d);
     if (st != GEMM_OK)
         return st;
+    if (M <= rtm::kShortMaxM)
+        return 0;  // short, wide products split K without a workspace
     const rtm::SplitK plan = rtm::sgemm_splitk_plan((int)M, (int)N, (int)K, d.sms);
     return plan.splits > 1 ? (int64_t)plan.splits * M * N * (int64_t)sizeof(float) : 0;
 }
@@ -345,6 +358,8 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return finish(rtm::launch_zero_fill(C, M * N, s));
+    if (M <= rtm::kShortMaxM)
+        return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d.sms, s));
     const rtm::SplitK plan = rtm::sgemm_splitk_plan((int)M, (int)N, (int)K, d.sms);
     const int64_t need = plan.splits > 1 ? (int64_t)plan.splits * M * N * 4 : 0;
     if (need == 0 || workspace_bytes < need)

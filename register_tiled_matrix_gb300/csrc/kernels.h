@@ -40,6 +40,15 @@ constexpr int kNarrowN = 64;
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
                              cudaStream_t stream);
 
+// SIMT FP32 product for short, wide shapes (sgemm_short.cu): M <= kShortMaxM,
+// any N and K >= 1, 4-byte-aligned pointers. Each thread keeps one column of
+// C in registers; `splits` (1, 2, 4 or 8, from sgemm_short_splits) CTAs of a
+// cluster split K and add their partials in rank order. No workspace.
+constexpr int kShortMaxM = 32;
+int sgemm_short_splits(int M, int N, int K, int sm_count);
+cudaError_t launch_sgemm_short(int M, int N, int K, const float *A, const float *B, float *C,
+                               int splits, cudaStream_t stream);
+
 // Split-K schedule of the SIMT product for shapes with too few C tiles to
 // fill the GPU: `splits` CTA rows each sum `kchunk` of K (a multiple of the
 // 32-deep slice) into their own M x N slab of a workspace, then a reduction

@@ -114,6 +114,10 @@ extern "C" int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
     cudaError_t e;
     if (K == 0) {
         e = rtm::launch_zero_fill(C, M * N, s);
+    } else if (M <= rtm::kShortMaxM) {
+        // Short, wide products split K over CTA clusters and need no scratch.
+        e = rtm::launch_sgemm_short((int)M, (int)N, (int)K, A, B, C,
+                                    rtm::sgemm_short_splits((int)M, (int)N, (int)K, sc.sms), s);
     } else {
         const rtm::SplitK plan = rtm::sgemm_splitk_plan((int)M, (int)N, (int)K, sc.sms);
         if (plan.splits <= 1) {

@@ -271,6 +271,23 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr)
     return v;
 }
 
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_shared_cluster_v2(uint32_t cluster_addr)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                 : "=f"(v.x), "=f"(v.y)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank)
 {

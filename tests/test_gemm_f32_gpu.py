@@ -174,3 +174,42 @@ def test_narrow_tile_boundary(N):
     assert_close_to_oracle(run(A, B), A, B, "f32")
     Ai, Bi = small_int_inputs(M, N, K, seed=N + 1)
     assert_bit_exact(run(Ai, Bi), (Ai.to(torch.int64) @ Bi.to(torch.int64)).numpy())
+
+
+# M <= 32: one column of C per thread, K split over S CTAs of a cluster
+# (S for a 152-SM GPU noted); no workspace in any fp32 entry point.
+@pytest.mark.parametrize("M,N,K", [(1, 8192, 4096),    # S = 4
+                                   (7, 1000, 999),     # S = 1
+                                   (16, 257, 3000),    # S = 4, 4-byte B copies
+                                   (32, 4096, 8192),   # S = 8
+                                   (17, 64, 33),       # 32 accumulators, one CTA
+                                   (1, 1, 1),
+                                   (9, 8190, 2048),    # S = 4, 4-byte B copies
+                                   (32, 2048, 8192)])  # S = 8: clusters of 8
+def test_short_wide_parity(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M * 31 + N + K)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+def test_short_wide_small_integer_bit_exact():
+    A, B = small_int_inputs(24, 1000, 4096, seed=81)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_short_wide_guard_band_repeatability_and_entry_points():
+    M, N, K = 20, 300, 2000
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=82)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf, C = guarded_output(M, N, DEV, pad=4096)
+    rtm.gemm_f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_f32(Ad, Bd)
+    assert rtm.gemm_f32_workspace_bytes(M, N, K) == 0
+    C3 = rtm.gemm_f32_ws(Ad, Bd)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N)
+    assert torch.equal(C, C2) and torch.equal(C, C3)
+    assert_close_to_oracle(C, A, B, "f32")
