@@ -28,11 +28,13 @@ cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> 
     return e;
 }
 
-// Tiles of the SIMT FP32 product: 128 x 128 C tiles (128 x 64 for N <= 64,
-// where a 128-wide tile would be at least half empty), 32-deep K slices.
+// Tiles of the SIMT FP32 product: 128 x 128 C tiles, with 64 columns for
+// N <= 64 and 64 rows for M <= 64 (where 128 would be at least half empty),
+// 32-deep K slices.
 namespace simt_tiles {
 constexpr int kTileM = 128, kTileN = 128, kSliceK = 32;
 constexpr int kNarrowN = 64;
+constexpr int kShortTileM = 64;
 } // namespace simt_tiles
 
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and

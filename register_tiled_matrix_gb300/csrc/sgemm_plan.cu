@@ -22,11 +22,13 @@ SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count)
 {
     SplitK p{1, K};
     const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
-    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((N + tile_n - 1) / tile_n);
+    const int tile_m = M <= kShortTileM ? kShortTileM : kTileM;
+    const long long tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
     if (sm_count <= 0 || tiles > sm_count)
         return p;
     const long long kslices = (K + kSliceK - 1) / kSliceK;
-    const double slice_time = tile_n == kNarrowN ? 0.8 : 1.0;  // narrow tiles: less work per slice
+    // Tiles of half the area: less work per slice.
+    const double slice_time = (tile_n == kNarrowN || tile_m == kShortTileM) ? 0.8 : 1.0;
     const double per_partial = (double)M * N / 2.1e6;
     const double plain = (double)((tiles + sm_count - 1) / sm_count) * kslices * slice_time;
     double best = plain;

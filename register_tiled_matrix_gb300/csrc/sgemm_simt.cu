@@ -408,6 +408,11 @@ __global__ void splitk_reduce4_kernel(const float4 *__restrict__ W, float4 *__re
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
                              cudaStream_t stream)
 {
+    if (M <= kShortTileM) {  // 64-row tiles: 128-row tiles would be at least half empty
+        if (N <= kNarrowN)
+            return simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
+        return simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
+    }
     if (N <= kNarrowN)
         return simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
     return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
@@ -416,12 +421,19 @@ cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
                                     const SplitK &plan, float *workspace, cudaStream_t stream)
 {
-    cudaError_t e =
-        N <= kNarrowN
-            ? simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, true>(
-                  M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk)
-            : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, true>(
-                  M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
+    cudaError_t e;
+    if (M <= kShortTileM)
+        e = N <= kNarrowN
+                ? simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, true>(
+                      M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk)
+                : simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1, true>(
+                      M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
+    else
+        e = N <= kNarrowN
+                ? simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, true>(
+                      M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk)
+                : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, true>(
+                      M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
     if (e != cudaSuccess)
         return e;
     const int64_t count = (int64_t)M * N;

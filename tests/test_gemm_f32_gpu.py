@@ -213,3 +213,30 @@ def test_short_wide_guard_band_repeatability_and_entry_points():
     assert guard_intact(buf, M, N)
     assert torch.equal(C, C2) and torch.equal(C, C3)
     assert_close_to_oracle(C, A, B, "f32")
+
+
+# 32 < M <= 64: 64-row tiles (64 x 128, or 64 x 64 for N <= 64), plain and
+# with K split over a workspace.
+@pytest.mark.parametrize("M,N,K", [(33, 8192, 4096), (64, 1000, 999), (48, 64, 1000),
+                                   (40, 130, 77), (64, 257, 2048)])
+def test_64_row_tiles_parity(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M * 17 + N + K)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = rtm.gemm_f32(Ad, Bd)
+    Cw = rtm.gemm_f32_ws(Ad, Bd)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(C, A, B, "f32")
+    assert_close_to_oracle(Cw, A, B, "f32")
+
+
+def test_64_row_tiles_sampled_and_bit_exact():
+    M, N, K = 64, 8192, 8192
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=83)
+    assert rtm.gemm_f32_workspace_bytes(M, N, K) > 0
+    C = rtm.gemm_f32_ws(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert_close_to_oracle(C, A, B, "f32", full=False, seed=83)
+    Ai, Bi = small_int_inputs(50, 300, 4096, seed=84)
+    Ci = rtm.gemm_f32_ws(Ai.to(DEV), Bi.to(DEV))
+    torch.cuda.synchronize()
+    assert_bit_exact(Ci, (Ai.to(torch.int64) @ Bi.to(torch.int64)).numpy())
