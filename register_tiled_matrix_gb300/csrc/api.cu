@@ -144,12 +144,10 @@ bool rows_on_16_bytes(const void *base, int64_t cols)
     return cols % 8 == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0;
 }
 
-// Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
-// CTA-pair kernel run on re-pitched copies of operands whose rows do not start
-// on 16-byte boundaries.
 // The fp32 product without a workspace: column strips for short, wide
-// products (M <= 32, where 128 x 128 tiles would be mostly empty), the
-// register-tiled 128 x 128 (128 x 64) kernel otherwise. K >= 1.
+// products (M <= 32, where 128-row tiles would be mostly empty), the
+// register-tiled kernel with 128 x 128 tiles otherwise (64 columns for
+// N <= 64, 64 rows for M <= 64). K >= 1.
 cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, float *C, int sms,
                           cudaStream_t s)
 {
@@ -158,6 +156,9 @@ cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, f
     return rtm::launch_sgemm_f32(M, N, K, A, B, C, s);
 }
 
+// Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
+// CTA-pair kernel run on re-pitched copies of operands whose rows do not start
+// on 16-byte boundaries.
 int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
              void *stream, uint64_t wait_limit_ns, int mute_producer, int f16 = 0,
              void *workspace = nullptr, int64_t workspace_bytes = 0)
@@ -247,14 +248,6 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
         }
         return finish(rtm::launch_gemm_tc_any(L, s));
     }
-    // One CTA per 128 x BN tile. With M <= 128 there is one row of tiles, so
-    // the widest BN that still gives 60 % of the SMs a tile is used (a sweep
-    // of BN 256/128/64 over N = 1K..32K, K = 1K..8K on GB300 found it within
-    // 1 % of the best width; 128 x 8192 x 8192: 56.0 us at BN 256, 41.5 at 64),
-    // but with at most 16 CTAs per row of A: every CTA reads all of A, and
-    // more CTAs on one 128-byte line per K-slice queue at its L2 slice
-    // (x 8192 x 8192 at BN 64: M = 1 63.1 us, against 52.6 at BN 256;
-    // M = 4 53.6 us; M = 8 and up 42 us).
     if (!tma_ok)
         return finish(rtm::launch_gemm_tc_any(L, s));
     // Long K with at most one 128-column tile per SM: the product streams B
@@ -270,6 +263,14 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
             splits *= 2;
         return finish(rtm::launch_gemm_tc_t(L, splits, true, s));
     }
+    // One CTA per 128 x BN tile. With M <= 128 there is one row of tiles, so
+    // the widest BN that still gives 60 % of the SMs a tile is used (a sweep
+    // of BN 256/128/64 over N = 1K..32K, K = 1K..8K on GB300 found it within
+    // 1 % of the best width; 128 x 8192 x 8192: 56.0 us at BN 256, 41.5 at 64),
+    // but with at most 16 CTAs per row of A: every CTA reads all of A, and
+    // more CTAs on one 128-byte line per K-slice queue at its L2 slice
+    // (x 8192 x 8192 at BN 64: M = 1 63.1 us, against 52.6 at BN 256;
+    // M = 4 53.6 us; M = 8 and up 42 us).
     int bn = 64;
     for (int w : {256, 128}) {
         if ((N + w - 1) / w * 10 >= (int64_t)d.sms * 6) {

@@ -405,6 +405,16 @@ static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
         return e;
     const long long tiles = SWAP ? (long long)((L.N + BNT - 1) / BNT) * ((L.M + MN - 1) / MN)
                                  : (long long)((L.M + BNT - 1) / BNT) * ((L.N + MN - 1) / MN);
+    // Every cluster resident at once (CTAs wait for their cluster's partials):
+    // halve the split while more clusters would be launched than fit.
+    static std::atomic<int> resident[4][64] = {};  // clusters of 1, 2, 4, 8
+    while (splits > 1) {
+        const int slot = splits == 2 ? 1 : splits == 4 ? 2 : 3;
+        const int fit = resident_clusters(kernel, splits, kThreads, Cf::SMEM_BYTES, resident[slot]);
+        if (fit <= 0 || tiles <= fit)
+            break;
+        splits /= 2;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles * splits), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);

@@ -37,6 +37,43 @@ constexpr int kNarrowN = 64;
 constexpr int kShortTileM = 64;
 } // namespace simt_tiles
 
+// How many clusters of `cluster_size` CTAs of `kernel` (`threads` threads,
+// `smem` bytes of dynamic shared memory, attribute already set) can be
+// resident at once on the current device; cached in `cache` (one slot per
+// device). 0 if the query fails. Kernels whose CTAs wait for each other at a
+// cluster barrier use it to launch no more clusters than fit at once: a
+// cluster that must wait for another to finish doubles the time.
+template <typename Kernel>
+int resident_clusters(Kernel kernel, int cluster_size, int threads, size_t smem,
+                      std::atomic<int> (&cache)[64])
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 0;
+    }
+    int n = cache[dev].load();
+    if (n > 0)
+        return n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster_size, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster_size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev].store(n);
+    return n;
+}
+
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
 // 4-byte-aligned pointers. 1 <= K; M, N >= 1.
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,

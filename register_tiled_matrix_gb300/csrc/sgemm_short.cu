@@ -239,38 +239,14 @@ static cudaError_t launch_b(int M, int N, int K, const float *A, const float *B,
 // current device (cached; 0 if unknown).
 static int resident_clusters_of_8()
 {
-    static std::atomic<int> cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        cudaGetLastError();
-        return 0;
-    }
-    int n = cached[dev].load();
-    if (n > 0)
-        return n;
     auto kernel = sshort::sgemm_short_kernel<32, 2, true>;
     static std::atomic<uint64_t> done{0};
     if (set_smem_limit_once(kernel, (int)sshort::Cfg<32>::SMEM_BYTES, done) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(8, 1, 1);
-    cfg.blockDim = dim3(sshort::BN / 2, 1, 1);
-    cfg.dynamicSmemBytes = sshort::Cfg<32>::SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 8;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        return 0;
-    }
-    cached[dev].store(n);
-    return n;
+    static std::atomic<int> cache[64] = {};
+    return resident_clusters(kernel, 8, sshort::BN / 2, sshort::Cfg<32>::SMEM_BYTES, cache);
 }
 
 int sgemm_short_splits(int M, int N, int K, int sm_count)

@@ -208,7 +208,8 @@ def test_short_wide_guard_band(M, N, K):
                                    (64, 2056, 2048),     # S = 2, ragged N
                                    (100, 1000, 8200),    # S = 8, ragged N and K
                                    (128, 8192, 2048),    # S = 2
-                                   (97, 19456, 2048)])   # S = 1, 152 tiles
+                                   (97, 19456, 2048),    # S = 1, 152 tiles
+                                   (64, 2048, 8192)])    # 16 tiles: S = 8 only if 16 clusters of 8 fit
 def test_transposed_short_wide(M, N, K):
     A, B = bf16_inputs(M, N, K, seed=M * 13 + N + K)
     full = M * N * K <= (1 << 31)
@@ -271,7 +272,8 @@ def test_transposed_bounded_wait_gives_up_and_context_survives():
                                    (2000, 256, 2048),   # S = 2, 256 columns
                                    (300, 8, 4096),      # S = 4
                                    (19456, 200, 2048),  # S = 1, 152 tiles
-                                   (1000, 136, 8200)])  # S = 8, ragged K
+                                   (1000, 136, 8200),   # S = 8, ragged K
+                                   (2048, 64, 8192)])   # 16 tiles: S = 8 only if they all fit
 def test_tall_narrow(M, N, K):
     A, B = bf16_inputs(M, N, K, seed=M + 5 * N + K)
     full = M * N * K <= (1 << 31)
