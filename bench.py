@@ -597,7 +597,9 @@ def run_configs(args) -> Optional[Dict]:
         C = torch.empty(w.M, w.N, device="cuda")
         entries = []
         if w.dtype == "f32":
-            entries.append(("gemm_f32", lambda: rtm.gemm_f32(A, B, out=C), fp32_peak))
+            kind, splits = rtm.gemm_f32_schedule(w.M, w.N, w.K)
+            label = "gemm_f32" if kind == "tiles" else f"gemm_f32 ({kind} x{splits})"
+            entries.append((label, lambda: rtm.gemm_f32(A, B, out=C), fp32_peak))
             need = rtm.gemm_f32_workspace_bytes(w.M, w.N, w.K)
             if need > 0:
                 ws = torch.empty(need // 4, device="cuda")

@@ -96,15 +96,44 @@ typedef enum gemm_status {
  * whose threads keep a column strip of C in registers and, where that leaves
  * SMs idle, split K over the CTAs of a cluster, adding the partial sums in a
  * fixed order (results repeat exactly from call to call); no workspace.
+ * Larger products with too few C tiles to fill the GPU split K the same way:
+ * the 2, 4 or 8 CTAs that share a C tile form a thread-block cluster, park
+ * their partial tiles in shared memory and add them through distributed
+ * shared memory in rank order (gemm_f32_schedule reports the choice).
  */
 GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K,
                       const float *A, const float *B, float *C, void *stream);
 
 /*
+ * gemm_f32_schedule — how an M x N x K fp32 product would be computed on the
+ * current device: by gemm_f32 when use_workspace == 0, by gemm_f32_ws with a
+ * workspace of gemm_f32_workspace_bytes (and by gemm_f32_noalloc) when
+ * use_workspace != 0. Launches nothing. Writes *kind (one of the values
+ * below) and *splits (the number of K chunks; 1 when K is not split); either
+ * pointer may be null. Returns GEMM_OK, GEMM_ERR_INVALID_ARG for sizes the
+ * entry points reject, or GEMM_ERR_LAUNCH / GEMM_ERR_DEVICE when no usable
+ * device is current. Products with M == 0, N == 0 or K == 0 report
+ * GEMM_F32_NO_KERNEL.
+ */
+typedef enum gemm_f32_kind {
+    GEMM_F32_NO_KERNEL = 0,        /* nothing to multiply (zero fill or no-op) */
+    GEMM_F32_TILES = 1,            /* register-tiled kernel, one CTA per C tile */
+    GEMM_F32_TILES_CLUSTER = 2,    /* the same, K split over the CTAs of a cluster */
+    GEMM_F32_TILES_WORKSPACE = 3,  /* the same, K split through a workspace + reduction */
+    GEMM_F32_COLUMN_STRIPS = 4     /* M <= 32: column strips (K split over a cluster
+                                      when splits > 1) */
+} gemm_f32_kind;
+GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace,
+                               int *kind, int *splits);
+
+/*
  * gemm_f32_workspace_bytes — bytes of scratch memory gemm_f32_ws uses for an
  * M x N x K product on the current device: 0 when the product has enough C
- * tiles to fill the GPU (gemm_f32_ws then needs no workspace), otherwise
- * splits * M * N * 4 for the split-K schedule described below. Returns a
+ * tiles to fill the GPU, or when splitting K over cluster CTAs (which needs
+ * no workspace, see gemm_f32) is estimated to be at least as fast (gemm_f32_ws
+ * then runs what gemm_f32 runs), otherwise splits * M * N * 4 for the
+ * split-K schedule described below. The workspace split can cut K into up to
+ * 32 chunks against a cluster's 8, so it wins for long K over few tiles. Returns a
  * negative status on invalid sizes (GEMM_ERR_INVALID_ARG) or when no usable
  * device is current (GEMM_ERR_LAUNCH, GEMM_ERR_DEVICE).
  *

@@ -12,7 +12,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
-from typing import List, Optional
+from typing import List, Optional, Tuple
 
 import torch
 
@@ -57,6 +57,9 @@ def load_library() -> ctypes.CDLL:
             f.restype = ctypes.c_int
         lib.gemm_f32_workspace_bytes.argtypes = [i64, i64, i64]
         lib.gemm_f32_workspace_bytes.restype = ctypes.c_int64
+        lib.gemm_f32_schedule.argtypes = [i64, i64, i64, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+        lib.gemm_f32_schedule.restype = ctypes.c_int
         lib.gemm_f32_ws.argtypes = [i64, i64, i64, p, p, p, p, i64, p]
         lib.gemm_f32_ws.restype = ctypes.c_int
         lib.gemm_bf16f32_workspace_bytes.argtypes = [i64, i64, i64]
@@ -132,6 +135,19 @@ def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = Non
         _check(load_library().gemm_f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                        _stream_handle(stream)))
     return C
+
+
+F32_KINDS = {0: "none", 1: "tiles", 2: "tiles+cluster-split", 3: "tiles+workspace-split",
+             4: "column-strips"}
+
+
+def gemm_f32_schedule(M: int, N: int, K: int, workspace: bool = False) -> Tuple[str, int]:
+    """(kind, splits): how gemm_f32 (or gemm_f32_ws, workspace=True) computes this
+    shape on the current device; kind is a value of F32_KINDS."""
+    kind, splits = ctypes.c_int(-1), ctypes.c_int(0)
+    _check(load_library().gemm_f32_schedule(int(M), int(N), int(K), 1 if workspace else 0,
+                                            ctypes.byref(kind), ctypes.byref(splits)))
+    return F32_KINDS[kind.value], splits.value
 
 
 def gemm_f32_workspace_bytes(M: int, N: int, K: int) -> int:

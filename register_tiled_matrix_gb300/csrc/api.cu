@@ -139,6 +139,16 @@ int64_t padded_copy_bytes(int64_t rows, int64_t cols)
     return (rows * ((cols + 7) / 8 * 8) * 2 + 255) / 256 * 256;
 }
 
+// The register-tiled fp32 product, K split over cluster CTAs when
+// cluster.splits > 1.
+cudaError_t run_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
+                          const rtm::SplitK &cluster, cudaStream_t s)
+{
+    if (cluster.splits > 1)
+        return rtm::launch_sgemm_f32_cluster(M, N, K, A, B, C, cluster, s);
+    return rtm::launch_sgemm_f32(M, N, K, A, B, C, s);
+}
+
 bool rows_on_16_bytes(const void *base, int64_t cols)
 {
     return cols % 8 == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0;
@@ -147,13 +157,14 @@ bool rows_on_16_bytes(const void *base, int64_t cols)
 // The fp32 product without a workspace: column strips for short, wide
 // products (M <= 32, where 128-row tiles would be mostly empty), the
 // register-tiled kernel with 128 x 128 tiles otherwise (64 columns for
-// N <= 64, 64 rows for M <= 64). K >= 1.
+// N <= 64, 64 rows for M <= 64), with K split over the CTAs of a cluster
+// when the product has too few tiles to fill the GPU. K >= 1.
 cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, float *C, int sms,
                           cudaStream_t s)
 {
     if (M <= rtm::kShortMaxM)
         return rtm::launch_sgemm_short(M, N, K, A, B, C, rtm::sgemm_short_splits(M, N, K, sms), s);
-    return rtm::launch_sgemm_f32(M, N, K, A, B, C, s);
+    return run_f32_tiles(M, N, K, A, B, C, rtm::sgemm_cluster_schedule(M, N, K, sms), s);
 }
 
 // Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
@@ -321,6 +332,45 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B, fl
     return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d.sms, s));
 }
 
+int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace, int *kind, int *splits)
+{
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim ||
+        M * N > (int64_t)1 << 52 || M * K > (int64_t)1 << 52 || K * N > (int64_t)1 << 52)
+        return GEMM_ERR_INVALID_ARG;
+    int k = GEMM_F32_NO_KERNEL, s = 1;
+    if (M > 0 && N > 0 && K > 0) {
+        DeviceInfo d;
+        const int st = current_device(&d);
+        if (st != GEMM_OK)
+            return st;
+        if (M <= rtm::kShortMaxM) {
+            k = GEMM_F32_COLUMN_STRIPS;
+            s = rtm::sgemm_short_splits((int)M, (int)N, (int)K, d.sms);
+        } else {
+            rtm::SplitK cluster;
+            if (use_workspace) {
+                const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
+                cluster = f.cluster;
+                if (f.workspace.splits > 1) {
+                    k = GEMM_F32_TILES_WORKSPACE;
+                    s = f.workspace.splits;
+                }
+            } else {
+                cluster = rtm::sgemm_cluster_schedule((int)M, (int)N, (int)K, d.sms);
+            }
+            if (k == GEMM_F32_NO_KERNEL) {
+                k = cluster.splits > 1 ? GEMM_F32_TILES_CLUSTER : GEMM_F32_TILES;
+                s = cluster.splits;
+            }
+        }
+    }
+    if (kind)
+        *kind = k;
+    if (splits)
+        *splits = s;
+    return GEMM_OK;
+}
+
 int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim ||
@@ -334,7 +384,7 @@ int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
         return st;
     if (M <= rtm::kShortMaxM)
         return 0;  // short, wide products split K without a workspace
-    const rtm::SplitK plan = rtm::sgemm_splitk_plan((int)M, (int)N, (int)K, d.sms);
+    const rtm::SplitK plan = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms).workspace;
     return plan.splits > 1 ? (int64_t)plan.splits * M * N * (int64_t)sizeof(float) : 0;
 }
 
@@ -361,10 +411,11 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
         return finish(rtm::launch_zero_fill(C, M * N, s));
     if (M <= rtm::kShortMaxM)
         return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d.sms, s));
-    const rtm::SplitK plan = rtm::sgemm_splitk_plan((int)M, (int)N, (int)K, d.sms);
+    const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
+    const rtm::SplitK &plan = f.workspace;
     const int64_t need = plan.splits > 1 ? (int64_t)plan.splits * M * N * 4 : 0;
     if (need == 0 || workspace_bytes < need)
-        return finish(rtm::launch_sgemm_f32((int)M, (int)N, (int)K, A, B, C, s));
+        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, s));
     if (overlaps(workspace, need, A, M * K * 4) || overlaps(workspace, need, B, K * N * 4) ||
         overlaps(workspace, need, C, M * N * 4))
         return GEMM_ERR_INVALID_ARG;

@@ -95,11 +95,35 @@ cudaError_t launch_sgemm_short(int M, int N, int K, const float *A, const float 
 struct SplitK {
     int splits;  // 1: no split (plain product)
     int kchunk;
+    bool spread = false;  // cluster split: one CTA per SM (see sgemm_cluster_plan)
 };
 SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count);  // sgemm_plan.cu
+// The plan's run time in the slice-time units of sgemm_cluster_plan's
+// estimate, for choosing between the two splits (1e300 when not split).
+double sgemm_workspace_estimate(int M, int N, int K, int sm_count, const SplitK &plan);
 // workspace: plan.splits * M * N floats. 1 <= K; M, N >= 1; plan.splits >= 2.
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
                                     const SplitK &plan, float *workspace, cudaStream_t stream);
+// Split-K without a workspace: the plan.splits (2, 4 or 8) CTAs that share a C
+// tile form one cluster and add their partial tiles through distributed shared
+// memory in rank order (deterministic). plan.splits == 1 is the plain product.
+// resident_spread[i]: clusters of 2 << i CTAs that fit at once with one CTA
+// per SM (sgemm_cluster_resident_spread; 0 if unknown).
+SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&resident_spread)[3],
+                          double *est = nullptr);  // sgemm_plan.cu
+int sgemm_cluster_resident_spread(int cluster_size);
+// sgemm_cluster_plan with the current device's cluster residency.
+SplitK sgemm_cluster_schedule(int M, int N, int K, int sm_count, double *est = nullptr);
+// How gemm_f32_ws (and gemm_f32_noalloc) schedule a product with M > kShortMaxM:
+// the workspace split when the model prices it below the cluster split (ties
+// go to the workspace), else the cluster split or the plain product.
+struct F32Schedule {
+    SplitK workspace;  // splits > 1: split-K through a workspace of splits * M * N floats
+    SplitK cluster;    // used when workspace.splits == 1
+};
+F32Schedule sgemm_ws_schedule(int M, int N, int K, int sm_count);
+cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const float *B, float *C,
+                                     const SplitK &plan, cudaStream_t stream);
 
 // The page's ablation ladder (sgemm_ladder.cu): rung 0 naive, 1 shared-memory
 // tiled (TILE 32), 2 register tiled (64 x 64 block, 4 x 4 per thread).

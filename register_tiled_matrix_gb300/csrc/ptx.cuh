@@ -244,6 +244,29 @@ __device__ __forceinline__ void tmem_wait_ld()
 }
 
 // ---------------------------------------------------------------- clusters
+// Special registers read with a volatile move: the compiler cannot reuse an
+// earlier read, so the value need not stay live in a register until then.
+__device__ __forceinline__ uint32_t special_tid_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%tid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t special_ctaid_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t special_ctaid_y()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
     uint32_t r;

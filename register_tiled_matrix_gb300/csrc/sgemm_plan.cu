@@ -49,4 +49,94 @@ SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count)
     return p;
 }
 
+namespace {
+
+// Comparable run-time estimates (in slice-times) for the split schedules,
+// fitted to a sweep of 18 shapes on GB300 (256^3 to 64 x 8192 x 8192, every
+// cluster size and the workspace plan): each wave of CTAs costs its chunk plus
+// kCtaOverhead slice-times (start-up, pipeline fill, epilogue); two CTAs
+// sharing an SM finish a wave in kPackedRate x twice a lone CTA's time.
+constexpr double kCtaOverhead = 0.7;
+constexpr double kPackedRate = 0.9;
+constexpr double kClusterReduce = 1.0;  // per wave: partials parked, cluster barriers, DSMEM adds
+
+struct ShapeCost {
+    long long tiles, kslices;
+    double slice_time;
+};
+
+ShapeCost shape_cost(int M, int N, int K)
+{
+    const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
+    const int tile_m = M <= kShortTileM ? kShortTileM : kTileM;
+    ShapeCost c;
+    c.tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
+    c.kslices = (K + kSliceK - 1) / kSliceK;
+    c.slice_time = (tile_n == kNarrowN || tile_m == kShortTileM) ? 0.8 : 1.0;  // half-area tiles
+    return c;
+}
+
+// `ctas` CTAs of `chunk` slices each; `alone`: every CTA has an SM to itself.
+double waves_time(const ShapeCost &c, long long ctas, long long chunk, int sms, bool alone,
+                  double per_wave)
+{
+    const double waves = alone ? 1.0 : kPackedRate * (double)((ctas + sms - 1) / sms < 2
+                                                                  ? 2
+                                                                  : (ctas + sms - 1) / sms);
+    return waves * ((chunk + kCtaOverhead) * c.slice_time + per_wave);
+}
+
+} // namespace
+
+double sgemm_workspace_estimate(int M, int N, int K, int sm_count, const SplitK &plan)
+{
+    const ShapeCost c = shape_cost(M, N, K);
+    if (plan.splits <= 1 || sm_count <= 0)
+        return 1e300;
+    const long long chunk = (plan.kchunk + kSliceK - 1) / kSliceK;
+    const long long ctas = c.tiles * plan.splits;
+    return waves_time(c, ctas, chunk, sm_count, ctas <= sm_count, 0.0) + 2.0 +
+           (double)M * N / 2.1e6 * plan.splits;
+}
+
+// The split over one cluster's CTAs: S in {2, 4, 8} (S must divide the tile
+// height), no reduction launch and no partial products in HBM; the partial
+// tiles are added through distributed shared memory. Left to itself the GPU
+// places the CTAs of a cluster of 8 two to an SM (measured on GB300: 512 x
+// 512 x 8192 at S = 8 ran each slice 1.9x slower than at S = 4), so when every
+// CTA can have an SM of its own the plan asks for one CTA per SM (`spread`),
+// provided all the clusters fit at once that way; otherwise it prices the
+// split as packed two to an SM.
+SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&resident_spread)[3],
+                          double *est_out)
+{
+    SplitK p{1, K};
+    if (est_out)
+        *est_out = 1e300;
+    const ShapeCost c = shape_cost(M, N, K);
+    if (sm_count <= 0 || c.tiles > sm_count)
+        return p;
+    const double plain = waves_time(c, c.tiles, c.kslices, sm_count, true, 0.0);
+    double best = plain;
+    for (int i = 0, s = 2; s <= 8; ++i, s *= 2) {
+        const long long chunk = (c.kslices + s - 1) / s;
+        if ((long long)s * chunk - c.kslices >= chunk)
+            break;  // a chunk would be empty: K too short for this many
+        const long long ctas = c.tiles * s;
+        // Clusters of 2 and 4 land one CTA per SM by themselves when they fit.
+        const bool spread = ctas <= sm_count && c.tiles <= resident_spread[i];
+        const bool alone = ctas <= sm_count && (spread || s < 8);
+        const double est = waves_time(c, ctas, chunk, sm_count, alone, kClusterReduce);
+        if (est < best) {
+            best = est;
+            p = SplitK{s, (int)(chunk * kSliceK), spread && s == 8};
+        }
+    }
+    if (p.splits > 1 && best > 0.97 * plain)
+        p = SplitK{1, K};
+    if (est_out)
+        *est_out = p.splits > 1 ? best : plain;
+    return p;
+}
+
 } // namespace rtm

@@ -49,6 +49,14 @@ namespace simt {
 constexpr int kThreads = 256;  // 16 x 16 threads
 constexpr int kGroupM = 8;     // tile-rows per L2 group
 
+// How K is split (one CTA per K chunk and C tile; the chunk index is blockIdx.y).
+enum SplitMode : int {
+    kPlain = 0,           // no split: gridDim.y == 1
+    kSplitWorkspace = 1,  // each chunk writes its partial tile to its own slab of a workspace
+    kSplitCluster = 2,    // the chunks of one tile are one cluster and add their partial
+                          // tiles through distributed shared memory
+};
+
 template <int BM, int BN, int BK, int STAGES>
 struct Cfg {
     static constexpr int JROWS = BM / 32;   // A copies per thread per 8-deep k group
@@ -71,6 +79,12 @@ struct Cfg {
     static_assert(BK * BN % (4 * kThreads) == 0, "B loader coverage");
     static constexpr int FAST_COPIES = A_PER_THREAD + B4_PER_THREAD;
     static constexpr int COPIES_PER_K = (FAST_COPIES + BK - 1) / BK;  // spread over the k loop
+    // kSplitCluster: the partial tile parked in shared memory after the k loop,
+    // rows padded by 4 floats (a quarter-warp's 128-bit stores, 2 rows 4 apart
+    // x 64 bytes, then fall in distinct banks).
+    static constexpr int PART_PITCH = BN + 4;
+    static constexpr size_t PART_BYTES = (size_t)BM * PART_PITCH * sizeof(float);
+    static constexpr size_t CLUSTER_SMEM_BYTES = SMEM_BYTES > PART_BYTES ? SMEM_BYTES : PART_BYTES;
 };
 
 __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n, int &tile_m,
@@ -85,28 +99,75 @@ __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n,
     tile_n = in_group / rows;
 }
 
+// kSplitCluster, after the cluster barrier: CTA r of the S = gridDim.y CTAs of
+// a cluster adds rows [r * BM / S, +BM / S) of the S partial tiles parked in
+// the cluster's shared memory (row pitch PITCH), reading them through
+// distributed shared memory in rank order, and stores the sums to C with the
+// same masks as the plain epilogue. Kept out of line: inlined, it cost the k
+// loop of the 4-byte-copy variant spilled registers.
+template <int BM, int BN, int PITCH, bool C_VEC>
+__device__ __noinline__ void cluster_add_partials(const float *part, int M, int N, float *C)
+{
+    int tile_m, tile_n;
+    tile_of_block((int)blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tile_m, tile_n);
+    const int m0 = tile_m * BM, n0 = tile_n * BN;
+    const uint32_t S = gridDim.y;  // cluster of (1, S, 1): rank == blockIdx.y
+    const uint32_t rank = blockIdx.y;
+    const int rows = BM / (int)S;
+    const int count4 = rows * (BN / 4);
+    for (int f = (int)threadIdx.x; f < count4; f += (int)blockDim.x) {
+        const int r = (int)rank * rows + f / (BN / 4);
+        const int c = (f % (BN / 4)) * 4;
+        const uint32_t local = smem_u32(part + r * PITCH + c);
+        float4 sum = ld_shared_cluster_v4(mapa_shared(local, 0));
+        for (uint32_t q = 1; q < S; ++q) {
+            const float4 v = ld_shared_cluster_v4(mapa_shared(local, q));
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+        }
+        const int gm = m0 + r, gn = n0 + c;
+        if (gm < M) {
+            float *crow = C + (size_t)gm * N;
+            if constexpr (C_VEC) {
+                if (gn < N)
+                    *reinterpret_cast<float4 *>(crow + gn) = sum;
+            } else {
+                const float w[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gn + j < N)
+                        crow[gn + j] = w[j];
+            }
+        }
+    }
+}
+
 // ORDER 0: accumulator tile walked row by row; 1: serpentine (odd rows walk
 // the columns backwards, so the B operand of a row's last FFMA is the first of
 // the next row's and can be reused by the operand cache).
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC,
-          bool SPLIT>
+          int SPLIT>
 __global__ void __launch_bounds__(kThreads, MINB)
     sgemm_rt_kernel(int M, int N, int K_total, int kchunk, const float *__restrict__ A,
                     const float *__restrict__ B, float *__restrict__ C, size_t c_split_stride)
 {
-    // Split-K (SPLIT): CTA row blockIdx.y of the grid sums k in
-    // [y * kchunk, +kchunk) and writes its partial tile to C + y * c_split_stride;
-    // A keeps its full row stride K_total. Without SPLIT the kernel is the plain
-    // product, compiled without any of this (the extra runtime offsets changed
+    // Split-K: CTA row blockIdx.y of the grid sums k in [y * kchunk, +kchunk);
+    // A keeps its full row stride K_total. kSplitWorkspace writes the partial
+    // tile to C + y * c_split_stride; kSplitCluster adds the partial tiles of
+    // the cluster's CTAs (the K chunks of one tile) after the k loop. The plain
+    // product is compiled without any of this (the extra runtime offsets changed
     // the register allocation of the FFMA loop and cost 6 % on GB300).
     int lda = K_total;
     int K = K_total;
-    if constexpr (SPLIT) {
+    if constexpr (SPLIT != kPlain) {
         const int k_begin = blockIdx.y * kchunk;
         K = min(kchunk, K_total - k_begin);
         A += k_begin;
         B += (size_t)k_begin * N;
-        C += blockIdx.y * c_split_stride;
+        if constexpr (SPLIT == kSplitWorkspace)
+            C += blockIdx.y * c_split_stride;
     }
 
     using G = Cfg<BM, BN, BK, STAGES>;
@@ -299,61 +360,123 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     cp_async_wait<0>();
 
-    // Epilogue: masked stores, 128-bit where the row allows it.
+    if constexpr (SPLIT == kSplitCluster) {
+        // Every CTA parks its partial tile in its own (now idle) shared memory;
+        // after a cluster barrier CTA r adds rows [r * BM / S, +BM / S) of the S
+        // partial tiles, read through distributed shared memory in rank order
+        // (so the sum is the same on every call), and stores them. The second
+        // barrier keeps each CTA's partial alive until every CTA has read it.
+        constexpr int PITCH = G::PART_PITCH;
+        // The thread and tile coordinates are read again from the special
+        // registers rather than kept live across the k loop, where the
+        // 128-register budget has no room for them.
+        const int tid2 = (int)special_tid_x();
+        const int warp2 = tid2 >> 5, lane2 = tid2 & 31;
+        const int tm2 = (warp2 >> 1) * 4 + (((lane2 >> 2) & 1) | ((lane2 >> 3) & 2));
+        const int tn2 = (warp2 & 1) * 8 + ((lane2 & 3) | ((lane2 >> 1) & 4));
+        __syncthreads();  // every warp has finished reading the last K-slice
 #pragma unroll
-    for (int q = 0; q < QM; ++q) {
+        for (int q = 0; q < QM; ++q)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int gm = m0 + q * SUBM + tm * 4 + i;
-            if (gm >= M)
-                continue;
-            float *crow = C + (size_t)gm * N;
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int p = 0; p < QN; ++p) {
-                const int gn = n0 + p * SUBN + tn * 4;
-                const float *v = &acc[q * 4 + i][p * 4];
-                if constexpr (C_VEC) {
-                    if (gn < N)
-                        *reinterpret_cast<float4 *>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
-                } else {
+                for (int p = 0; p < QN; ++p) {
+                    const float *v = &acc[q * 4 + i][p * 4];
+                    *reinterpret_cast<float4 *>(smem + (q * SUBM + tm2 * 4 + i) * PITCH +
+                                                p * SUBN + tn2 * 4) =
+                        make_float4(v[0], v[1], v[2], v[3]);
+                }
+        cluster_sync();
+        cluster_add_partials<BM, BN, PITCH, C_VEC>(smem, M, N, C);
+        cluster_sync();
+    } else {
+        // Epilogue: masked stores, 128-bit where the row allows it.
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (gn + j < N)
-                            crow[gn + j] = v[j];
+        for (int q = 0; q < QM; ++q) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int gm = m0 + q * SUBM + tm * 4 + i;
+                if (gm >= M)
+                    continue;
+                float *crow = C + (size_t)gm * N;
+#pragma unroll
+                for (int p = 0; p < QN; ++p) {
+                    const int gn = n0 + p * SUBN + tn * 4;
+                    const float *v = &acc[q * 4 + i][p * 4];
+                    if constexpr (C_VEC) {
+                        if (gn < N)
+                            *reinterpret_cast<float4 *>(crow + gn) =
+                                make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (gn + j < N)
+                                crow[gn + j] = v[j];
+                    }
                 }
             }
         }
     }
 }
 
+// Shared memory a cluster-split CTA reserves to have an SM to itself: more
+// than half of the 228 KB an SM holds.
+constexpr size_t kSpreadSmemBytes = 120 * 1024;
+
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC,
-          bool SPLIT>
+          int SPLIT>
 cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, float *C,
-                       cudaStream_t stream, int splits = 1, int kchunk = 0)
+                       cudaStream_t stream, int splits = 1, int kchunk = 0, bool spread = false)
 {
+    static_assert(Cfg<BM, BN, BK, STAGES>::CLUSTER_SMEM_BYTES <= kSpreadSmemBytes,
+                  "the spread reservation holds the pipeline and the partial tile");
     using G = Cfg<BM, BN, BK, STAGES>;
     auto kernel = sgemm_rt_kernel<BM, BN, BK, STAGES, MINB, ORDER, B_VEC, C_VEC, SPLIT>;
-    if (G::SMEM_BYTES > 48 * 1024) {
+    // A cluster split may ask for one CTA per SM (spread): it then reserves
+    // more shared memory than two CTAs of an SM could hold.
+    constexpr size_t smem_max = SPLIT == kSplitCluster ? kSpreadSmemBytes : G::SMEM_BYTES;
+    const size_t smem = SPLIT != kSplitCluster ? G::SMEM_BYTES
+                        : spread               ? kSpreadSmemBytes
+                                               : G::CLUSTER_SMEM_BYTES;
+    if (smem_max > 48 * 1024) {
         static std::atomic<uint64_t> done{0};  // per instantiation
-        const cudaError_t e = set_smem_limit_once(kernel, (int)G::SMEM_BYTES, done);
+        const cudaError_t e = set_smem_limit_once(kernel, (int)smem_max, done);
         if (e != cudaSuccess)
             return e;
     }
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     if (tiles > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    if (splits < 1 || splits > 65535 || (!SPLIT && splits != 1))
+    if (splits < 1 || splits > 65535 || (SPLIT == kPlain && splits != 1))
         return cudaErrorInvalidValue;
     if (splits == 1)
         kchunk = K;
-    kernel<<<dim3((unsigned)tiles, (unsigned)splits), kThreads, G::SMEM_BYTES, stream>>>(
+    if constexpr (SPLIT == kSplitCluster) {
+        // S = splits CTAs per cluster, S dividing BM (S in 1, 2, 4, 8).
+        if (splits > 8 || BM % splits != 0)
+            return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)tiles, (unsigned)splits, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)splits;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, M, N, K, kchunk, A, B, C, (size_t)M * N);
+    }
+    kernel<<<dim3((unsigned)tiles, (unsigned)splits), kThreads, smem, stream>>>(
         M, N, K, kchunk, A, B, C, (size_t)M * N);
     return cudaGetLastError();
 }
 
-template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool SPLIT = false>
+template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, int SPLIT = kPlain>
 cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, float *C,
-                       cudaStream_t stream, int splits = 1, int kchunk = 0)
+                       cudaStream_t stream, int splits = 1, int kchunk = 0, bool spread = false)
 {
     const bool b_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(B) & 15) == 0);
     const bool c_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
@@ -361,12 +484,12 @@ cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, floa
     // takes the 4-byte C stores.
     if (b_vec && c_vec)
         return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, true, SPLIT>(
-            M, N, K, A, B, C, stream, splits, kchunk);
+            M, N, K, A, B, C, stream, splits, kchunk, spread);
     if (b_vec)
         return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, false, SPLIT>(
-            M, N, K, A, B, C, stream, splits, kchunk);
+            M, N, K, A, B, C, stream, splits, kchunk, spread);
     return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, false, false, SPLIT>(
-        M, N, K, A, B, C, stream, splits, kchunk);
+        M, N, K, A, B, C, stream, splits, kchunk, spread);
 }
 
 } // namespace simt
@@ -421,18 +544,19 @@ cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
                                     const SplitK &plan, float *workspace, cudaStream_t stream)
 {
+    using simt::kSplitWorkspace;
     cudaError_t e;
     if (M <= kShortTileM)
         e = N <= kNarrowN
-                ? simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, true>(
+                ? simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitWorkspace>(
                       M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk)
-                : simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1, true>(
+                : simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1, kSplitWorkspace>(
                       M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
     else
         e = N <= kNarrowN
-                ? simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, true>(
+                ? simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitWorkspace>(
                       M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk)
-                : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, true>(
+                : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, kSplitWorkspace>(
                       M, N, K, A, B, workspace, stream, plan.splits, plan.kchunk);
     if (e != cudaSuccess)
         return e;
@@ -451,6 +575,66 @@ cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const f
         splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(workspace, C, count,
                                                                   plan.splits);
     return cudaGetLastError();
+}
+
+int sgemm_cluster_resident_spread(int cluster_size)
+{
+    // Every cluster-split instantiation has the same footprint when spread
+    // (256 threads, at most 128 registers, kSpreadSmemBytes), so one of them
+    // stands for all in the occupancy query.
+    auto kernel = simt::sgemm_rt_kernel<kTileM, kTileN, kSliceK, 2, 2, 1, true, true,
+                                        simt::kSplitCluster>;
+    static std::atomic<uint64_t> done{0};
+    if (set_smem_limit_once(kernel, (int)simt::kSpreadSmemBytes, done) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cluster_size != 2 && cluster_size != 4 && cluster_size != 8)
+        return 0;
+    static std::atomic<int> cache2[64] = {}, cache4[64] = {}, cache8[64] = {};
+    auto &cache = cluster_size == 2 ? cache2 : cluster_size == 4 ? cache4 : cache8;
+    return resident_clusters(kernel, cluster_size, simt::kThreads, simt::kSpreadSmemBytes, cache);
+}
+
+SplitK sgemm_cluster_schedule(int M, int N, int K, int sm_count, double *est)
+{
+    const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
+    const int tile_m = M <= kShortTileM ? kShortTileM : kTileM;
+    const long long tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
+    int resident[3] = {0, 0, 0};
+    if (tiles <= sm_count)  // only then is a split considered
+        for (int i = 0; i < 3; ++i)
+            resident[i] = sgemm_cluster_resident_spread(2 << i);
+    return sgemm_cluster_plan(M, N, K, sm_count, resident, est);
+}
+
+F32Schedule sgemm_ws_schedule(int M, int N, int K, int sm_count)
+{
+    double cluster_est = 0;
+    F32Schedule f;
+    f.workspace = sgemm_splitk_plan(M, N, K, sm_count);
+    f.cluster = sgemm_cluster_schedule(M, N, K, sm_count, &cluster_est);
+    if (f.workspace.splits > 1 &&
+        cluster_est < sgemm_workspace_estimate(M, N, K, sm_count, f.workspace))
+        f.workspace = SplitK{1, K};
+    return f;
+}
+
+cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const float *B, float *C,
+                                     const SplitK &plan, cudaStream_t stream)
+{
+    using simt::kSplitCluster;
+    if (M <= kShortTileM)
+        return N <= kNarrowN
+                   ? simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitCluster>(
+                         M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread)
+                   : simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
+                         M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread);
+    return N <= kNarrowN
+               ? simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitCluster>(
+                     M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread)
+               : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
+                     M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread);
 }
 
 } // namespace rtm

@@ -126,6 +126,16 @@ def test_workspace_entry_points_host_checks(lib):
     assert f(0, 8, 8, None, None, None, None, 0, None) == 0
 
 
+def test_f32_schedule_host_checks(lib):
+    kind, splits = ctypes.c_int(-1), ctypes.c_int(-1)
+    f = lib.gemm_f32_schedule
+    assert f(-1, 8, 8, 0, ctypes.byref(kind), ctypes.byref(splits)) == -1
+    assert f(8, 8, 1 << 31, 1, None, None) == -1
+    assert f(0, 8, 8, 0, ctypes.byref(kind), ctypes.byref(splits)) == 0
+    assert (kind.value, splits.value) == (0, 1)  # GEMM_F32_NO_KERNEL
+    assert f(8, 8, 0, 1, ctypes.byref(kind), None) == 0 and kind.value == 0
+
+
 def _ceil256(x):
     return (x + 255) // 256 * 256
 

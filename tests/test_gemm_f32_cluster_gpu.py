@@ -1,0 +1,113 @@
+"""GPU tests of the fp32 split-K over thread-block clusters: products with too
+few C tiles to fill the GPU, run through gemm_f32 (no workspace), split K over
+2, 4 or 8 CTAs of one cluster, which add their partial tiles through
+distributed shared memory in rank order. Each shape below was chosen so the
+schedule on a 152-SM GB300 takes the variant named beside it (cluster size,
+one CTA per SM or two, tile shape, 16-byte or 4-byte paths); every one is
+checked against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import register_tiled_matrix_gb300 as rtm
+import workloads
+from tests.parity import (assert_bit_exact, assert_close_to_oracle, guard_intact,
+                          guarded_output, small_int_inputs)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rtm.build()
+    rtm.load_library()
+
+
+SHAPES = [
+    (300, 260, 129),     # 2 per cluster
+    (1024, 1024, 1024),  # 4 per cluster, two CTAs per SM
+    (1000, 1000, 999),   # the same, ragged in M, N and K
+    (512, 512, 512),     # 4 per cluster, one CTA per SM
+    (640, 520, 384),     # 4 per cluster, ragged N, three slices per chunk
+    (256, 256, 256),     # 8 per cluster spread one CTA per SM, one slice per chunk
+    (300, 200, 1024),    # 8 per cluster spread, ragged tiles
+    (129, 65, 999),      # 8 per cluster spread, one spare row and column tile
+    (2000, 60, 2000),    # 128 x 64 tiles, 8 per cluster, two CTAs per SM
+    (8192, 64, 4096),    # 128 x 64 tiles, 4 per cluster
+    (60, 3000, 2000),    # 64 x 128 tiles, 8 per cluster
+    (64, 8, 4096),       # 64 x 64 tiles, 8 per cluster spread
+    (48, 64, 1000),      # 64 x 64 tiles, 8 per cluster spread, partial last chunk
+    (300, 201, 1024),    # N % 4 != 0: 4-byte copies of B and stores of C
+    (1200, 1300, 700),   # 4 per cluster, three waves of CTAs
+    (2048, 640, 2048),   # 8 per cluster, five waves of CTAs
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_cluster_split_parity(M, N, K):
+    kind, splits = rtm.gemm_f32_schedule(M, N, K)
+    assert kind == "tiles+cluster-split" and splits in (2, 4, 8), (kind, splits)
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M * 31 + N * 7 + K)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (1000, 1000, 999), (48, 64, 1000),
+                                   (2048, 640, 2048)])
+def test_cluster_split_small_integer_bit_exact(M, N, K):
+    A, B = small_int_inputs(M, N, K, seed=M + N + K)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 200, 1024), (129, 65, 999), (1000, 1000, 999)])
+def test_cluster_split_guard_band_and_repeatability(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "normal", "f32", seed=K)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf, C = guarded_output(M, N, DEV)
+    rtm.gemm_f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N), "a store landed outside C"
+    assert torch.equal(C, C2), "the rank-ordered sum repeats exactly"
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+def test_cluster_split_unaligned_output():
+    # C starts 4 bytes past a 16-byte boundary: the 4-byte store path.
+    M, N, K = 640, 520, 384
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=5)
+    buf = torch.full((M * N + 4,), float("nan"), device=DEV)
+    C = buf[1:1 + M * N].view(M, N)
+    rtm.gemm_f32(A.to(DEV), B.to(DEV), out=C)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[0]) and torch.isnan(buf[1 + M * N:]).all()
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+def test_workspace_entry_takes_the_cheaper_split():
+    # 1024^3 splits over clusters (no workspace); 512 x 512 x 8192 needs more
+    # chunks than a cluster holds and keeps the workspace split. Both agree
+    # with the oracle through both entry points.
+    assert rtm.gemm_f32_workspace_bytes(1024, 1024, 1024) == 0
+    assert rtm.gemm_f32_schedule(1024, 1024, 1024, workspace=True)[0] == "tiles+cluster-split"
+    assert rtm.gemm_f32_workspace_bytes(512, 512, 8192) > 0
+    assert rtm.gemm_f32_schedule(512, 512, 8192, workspace=True)[0] == "tiles+workspace-split"
+    assert rtm.gemm_f32_schedule(512, 512, 8192)[0] == "tiles+cluster-split"
+    assert rtm.gemm_f32_schedule(4096, 4096, 4096) == ("tiles", 1)
+    assert rtm.gemm_f32_schedule(16, 8192, 8192)[0] == "column-strips"
+    for M, N, K in [(1024, 1024, 1024), (512, 512, 8192)]:
+        A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M + K)
+        Ad, Bd = A.to(DEV), B.to(DEV)
+        Cw = rtm.gemm_f32_ws(Ad, Bd)
+        C = rtm.gemm_f32(Ad, Bd)
+        torch.cuda.synchronize()
+        assert_close_to_oracle(Cw, A, B, "f32")
+        assert_close_to_oracle(C, A, B, "f32")
+        if M == 1024:
+            assert torch.equal(C, Cw), "no workspace needed: both entries run the same schedule"

@@ -1,5 +1,6 @@
 """The product entry points can be captured into a CUDA graph once they have
-run on the device (the per-device caches are then filled): a replay with new
+run on the device (the per-device caches, including the cluster occupancy
+queries of the split schedules, are then filled): a replay with new
 inputs written into the captured buffers gives bit for bit what an eager call
 gives, and agrees with the oracle."""
 
@@ -32,6 +33,8 @@ def _ws_2byte(M, N, K):
 CASES = {
     # name: (dtype, M, N, K, call(A, B, C, workspace))
     "gemm_f32": ("f32", 640, 520, 384, lambda A, B, C, W: rtm.gemm_f32(A, B, out=C)),
+    "gemm_f32 cluster split-K": ("f32", 1000, 1000, 999,
+                                 lambda A, B, C, W: rtm.gemm_f32(A, B, out=C)),
     "gemm_f32_ws split-K": ("f32", 512, 64, 2048,
                             lambda A, B, C, W: rtm.gemm_f32_ws(A, B, out=C, workspace=W)),
     "gemm_bf16f32 CTA pairs": ("bf16", 512, 512, 256,
