@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
     const int ktiles = (K + BK - 1) / BK;
     // K-slices that lie wholly inside K; with the tile wholly inside M x N
-    // (and the 16-byte B path) they are loaded without any predicate.
-    const bool interior = B_VEC && (m0 + BM <= M) && (n0 + BN <= N);
+    // they are loaded without any predicate.
+    const bool interior = (m0 + BM <= M) && (n0 + BN <= N);
     const int kfull = interior ? K / BK : 0;
 
     // A loader: copy (j, h) of this thread moves A[m0 + a_m + 4j][k0 + 8h + a_k]
@@ -227,14 +227,24 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
     // Unpredicated copies of K-slice kt into `stage` (interior tiles, full
     // slices), one per call so they can be spread over the FMA loop: copies
-    // 0 .. A_PER_THREAD-1 are A elements, the rest B vectors.
-    constexpr int FAST_COPIES = G::FAST_COPIES;
+    // 0 .. A_PER_THREAD-1 are A elements, the rest B vectors (16-byte path) or
+    // B elements (4-byte path, rows of B not on 16-byte boundaries).
+    constexpr int FAST_COPIES =
+        B_VEC ? G::FAST_COPIES : G::A_PER_THREAD + G::B1_PER_THREAD;
+    constexpr int COPIES_PER_K = (FAST_COPIES + BK - 1) / BK;  // spread over the k loop
     auto fast_copy = [&](int c, uint32_t stage, int kt) {
         const int k0 = kt * BK;
         if (c < G::A_PER_THREAD) {
             const int h = c / JROWS, j = c % JROWS;
             cp_async_4_full(a_dst0 + stage * A_STAGE_BYTES + (uint32_t)((8 * h * LDA + 4 * j) * 4),
                             a_src + (size_t)(4 * j) * lda + (k0 + 8 * h));
+        } else if constexpr (!B_VEC) {
+            // copy i moves B[k0 + i * (256 / BN) + tid / BN][n0 + tid % BN]
+            const int i = c - G::A_PER_THREAD;
+            const int k = i * (kThreads / BN) + tid / BN;
+            const int n = tid % BN;
+            cp_async_4_full(smem_u32(sB + stage * (BK * BN) + k * BN + n),
+                            B + (size_t)(k0 + k) * N + (n0 + n));
         } else {
             const int i = c - G::A_PER_THREAD;
             const int krow = i * (kThreads / (BN / 4));
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     };
 
     auto load_tile = [&](uint32_t stage, int kt) {
-        if (B_VEC && kt < kfull) {
+        if (kt < kfull) {
 #pragma unroll
             for (int c = 0; c < FAST_COPIES; ++c)
                 fast_copy(c, stage, kt);
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         cp_async_wait<STAGES - 2>();
         __syncthreads();  // slice kt visible to all; the stage read at kt-1 is free
         const int nt = kt + STAGES - 1;
-        const bool fast = B_VEC && nt < kfull;  // copies spread over the FMA loop below
+        const bool fast = nt < kfull;  // copies spread over the FMA loop below
         if (!fast && nt < ktiles)
             load_pred(write_stage, nt);
         const uint32_t fill_stage = write_stage;
@@ -352,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
                 }
 #pragma unroll
-            for (int q = 0; q < G::COPIES_PER_K; ++q)
-                if (fast && k * G::COPIES_PER_K + q < FAST_COPIES)
-                    fast_copy(k * G::COPIES_PER_K + q, fill_stage, nt);
+            for (int q = 0; q < COPIES_PER_K; ++q)
+                if (fast && k * COPIES_PER_K + q < FAST_COPIES)
+                    fast_copy(k * COPIES_PER_K + q, fill_stage, nt);
         }
         cp_async_commit();
     }
