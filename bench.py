@@ -56,7 +56,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
 # reported as null once the source changes. See profiles/.
 TRAFFIC = {
-    "gemm_f32": {"bytes": 393601536, "source_sha1": "4a3ee780ba9e61fea5560e949508663de5938b33",
+    "gemm_f32": {"bytes": 383779072, "source_sha1": "f2f1b5e280af84d759853c1bb420f8f929f52fed",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
     "gemm_bf16f32": {"bytes": 1322460672,
                      "source_sha1": "c783e511080729e042138d66e9ba9af5dfda2306",
