@@ -41,6 +41,13 @@ __global__ void zero_fill_kernel(float *C, int64_t count)
         C[i] = 0.0f;
 }
 
+__global__ void zero_fill4_kernel(float4 *C, int64_t count4)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count4; i += stride)
+        C[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // Current device's cached info; GEMM_OK or an error status.
 int current_device(DeviceInfo *out)
 {
@@ -301,10 +308,16 @@ cudaError_t launch_zero_fill(float *C, int64_t count, cudaStream_t stream)
 {
     if (count <= 0)
         return cudaSuccess;
-    int64_t blocks = (count + 255) / 256;
+    const bool vec = count % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+    const int64_t items = vec ? count / 4 : count;
+    int64_t blocks = (items + 255) / 256;
     if (blocks > 4096)
         blocks = 4096;
-    zero_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(C, count);
+    if (vec)
+        zero_fill4_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<float4 *>(C),
+                                                                items);
+    else
+        zero_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(C, count);
     return cudaGetLastError();
 }
 } // namespace rtm

@@ -34,6 +34,13 @@
 // The operands' row strides are parameters of the tensor maps, so the kernel
 // also runs on copies of A or B whose rows were padded to 16-byte multiples.
 //
+// Products whose tiles would occupy at most half the pairs (256 x 8192 x 8192:
+// 32 tiles for 76 pairs) split K in two: the persistent loop walks (tile, K
+// half) units, C is zero-filled first, and the epilogue adds each half's tile
+// into C with TMA reduce-adds. With exactly two partials the sum 0 + a + b is
+// the same in either order (IEEE addition is commutative), so results still
+// repeat exactly from call to call.
+//
 // Every mbarrier wait is bounded in time (see gemm_tc.cu); the cluster
 // barriers at start and end are reached on every path.
 #include <cstdint>
@@ -98,7 +105,19 @@ struct Params {
     int *err;
     unsigned long long limit_ns;
     int mute_producer;
+    int splits;  // 1, or 2: K halves added into a zeroed C (TMA-store epilogue only)
 };
+
+// Work unit u of the persistent loop: tile u / splits, K-blocks
+// [kb_begin, kb_end) of its split u % splits (every split non-empty: the host
+// splits only K of at least two blocks).
+__device__ __forceinline__ void unit_kblocks(int u, int splits, int kblocks, int &kb_begin,
+                                             int &kb_end)
+{
+    const int per = (kblocks + splits - 1) / splits;
+    kb_begin = (u % splits) * per;
+    kb_end = min(kblocks, kb_begin + per);
+}
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &n0)
 {
@@ -170,7 +189,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const int tiles_m = (p.M + PM - 1) / PM;
     const int tiles_n = (p.N + PN - 1) / PN;
-    const int ntiles = tiles_m * tiles_n;
+    const int splits = p.splits;
+    const int nunits = tiles_m * tiles_n * splits;
     const int kblocks = (p.K + BK - 1) / BK;
     const uint64_t limit = p.limit_ns;
 
@@ -179,12 +199,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0 && !p.mute_producer) {
             uint32_t stage = 0, phase = 0;
             uint32_t issued = 0, issued_parity = 0;
-            for (int t = cluster_id; t < ntiles && !*abort; t += num_clusters) {
-                int m0, n0;
-                tile_coords(t, tiles_m, tiles_n, m0, n0);
+            for (int u = cluster_id; u < nunits && !*abort; u += num_clusters) {
+                int m0, n0, kb_begin, kb_end;
+                tile_coords(u / splits, tiles_m, tiles_n, m0, n0);
+                unit_kblocks(u, splits, kblocks, kb_begin, kb_end);
                 const int row0 = m0 + (int)rank * HM;
                 const int col0 = n0 + (int)rank * HN;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1, limit, abort)) {
                         give_up(p.err, abort);
                         break;
@@ -227,7 +248,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool issued_any = false;
-            for (int t = cluster_id; t < ntiles && !*abort; t += num_clusters) {
+            for (int u = cluster_id; u < nunits && !*abort; u += num_clusters) {
+                int kb_begin, kb_end;
+                unit_kblocks(u, splits, kblocks, kb_begin, kb_end);
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, limit, abort)) {
                     give_up(p.err, abort);
                     break;
@@ -235,7 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * PN;
                 bool ok = true;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait_bounded(&full[stage], phase, limit, abort)) {
                         give_up(p.err, abort);
                         ok = false;
@@ -249,7 +272,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint64_t adesc = sdesc_sw128(sa + kk * UMMA_K * 2, 16, 1024);
                         const uint64_t bdesc =
                             sdesc_sw128(sb + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
-                        umma_f16_pair(d_tmem, adesc, bdesc, idesc<F16>(), (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16_pair(d_tmem, adesc, bdesc, idesc<F16>(),
+                                      (kb > kb_begin || kk > 0) ? 1u : 0u);
                     }
                     issued_any = true;
                     umma_commit_pair_multicast(&empty[stage], kBothCtas);
@@ -277,9 +301,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
         uint32_t acc = 0, acc_phase = 0;
-        for (int t = cluster_id; t < ntiles && !*abort; t += num_clusters) {
+        for (int u = cluster_id; u < nunits && !*abort; u += num_clusters) {
             int m0, n0;
-            tile_coords(t, tiles_m, tiles_n, m0, n0);
+            tile_coords(u / splits, tiles_m, tiles_n, m0, n0);
             if (!mbar_wait_bounded(&tfull[acc], acc_phase, limit, abort)) {
                 give_up(p.err, abort);
                 break;
@@ -353,7 +377,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, smem_u32(box), col, row0);
+                        if (splits > 1)
+                            tma_reduce_add_2d(&tmC, smem_u32(box), col, row0);
+                        else
+                            tma_store_2d(&tmC, smem_u32(box), col, row0);
                         bulk_commit_group();
                     }
                 }
@@ -418,6 +445,11 @@ static bool encode_c_map(EncodeTiledFn fn, CUtensorMap *map, const void *base, u
 
 cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
 {
+    return launch_gemm_tc_pair_split(L, 0, stream);
+}
+
+cudaError_t launch_gemm_tc_pair_split(const TcLaunch &L, int splits, cudaStream_t stream)
+{
     using namespace tc2;
     auto fn = reinterpret_cast<EncodeTiledFn>(L.encode_tiled);
     if (!fn)
@@ -466,8 +498,24 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &L, cudaStream_t stream)
             max_clusters[fi][dev].store(clusters_max);
     }
     const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
-    const int clusters = (int)(ntiles < clusters_max ? ntiles : clusters_max);
-    Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer};
+    // splits == 0: choose. Products whose tiles fill at most half the pairs
+    // split K in two (each half adds its tile into a zeroed C with TMA
+    // reduce-adds; 0 + a + b is the same in either order, so the result still
+    // repeats exactly), when both halves keep at least 32 K-blocks.
+    const int kblocks = (L.K + BK - 1) / BK;
+    if (splits == 0)
+        splits = (c_vec && 2 * ntiles <= clusters_max && kblocks >= 64) ? 2 : 1;
+    if (splits != 1 && (splits != 2 || !c_vec || kblocks < 2))
+        return cudaErrorInvalidValue;
+    const long long nunits = ntiles * splits;
+    const int clusters = (int)(nunits < clusters_max ? nunits : clusters_max);
+    if (splits > 1) {
+        e = launch_zero_fill(L.C, (int64_t)L.M * L.N, stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer,
+             splits};
     kernel<<<2 * clusters, kThreads, smem_bytes, stream>>>(ta, tb, tc, p);
     return cudaGetLastError();
 }

@@ -156,6 +156,9 @@ cudaError_t launch_gemm_bf16_tc_bn(const TcLaunch &p, int bn, cudaStream_t strea
 // rows at lda / ldb elements (16-byte multiples, 16-byte aligned bases); any
 // 4-byte-aligned C and any N (float4 stores when C rows are 16-byte aligned).
 cudaError_t launch_gemm_tc_pair(const TcLaunch &p, cudaStream_t stream);
+// splits 1 or 2 (2: C zero-filled, then each K half reduce-added; C rows must be
+// 16-byte aligned); 0 lets the launcher choose (launch_gemm_tc_pair).
+cudaError_t launch_gemm_tc_pair_split(const TcLaunch &p, int splits, cudaStream_t stream);
 
 // Copy a rows x cols matrix of 2-byte values (row-major, rows packed, `src`
 // 2-byte aligned) to `dst` with rows `ld` values apart (ld >= cols, ld % 8 ==

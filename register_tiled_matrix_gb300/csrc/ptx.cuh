@@ -150,6 +150,18 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int
                  : "memory");
 }
 
+// The same box added element by element into global memory (fp32 add at the
+// L2, tracked in bulk async-groups like a store).
+__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, uint32_t src, int32_t c0,
+                                                  int32_t c1)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], "
+        "[%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

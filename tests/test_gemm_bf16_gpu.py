@@ -155,12 +155,14 @@ def test_repeated_calls_identical():
     assert torch.equal(C1, C2)
 
 
-@pytest.mark.parametrize("M", [256, 128], ids=["cta_pair", "single_cta"])
-def test_bounded_wait_gives_up_and_context_survives(M):
+@pytest.mark.parametrize("M,K", [(256, 256), (128, 256), (256, 4096)],
+                         ids=["cta_pair", "single_cta", "cta_pair_k_split"])
+def test_bounded_wait_gives_up_and_context_survives(M, K):
     """With the loads muted, every wait runs out after 50 ms; the kernel records
     a timeout and returns, and the next product on the same context is correct.
-    M = 256 runs the CTA-pair kernel, M = 128 the single-CTA kernel."""
-    A, B = bf16_inputs(M, 512, 256, seed=45)
+    M = 256 runs the CTA-pair kernel (with K = 4096 split in two), M = 128 the
+    single-CTA kernel."""
+    A, B = bf16_inputs(M, 512, K, seed=45)
     Ad, Bd = A.to(DEV), B.to(DEV)
     C = torch.empty(M, 512, device=DEV)
     assert rtm.get_device_error() == 0
@@ -308,3 +310,53 @@ def test_tall_narrow_bounded_wait_gives_up_and_context_survives():
     assert rtm.get_device_error() == -4
     assert rtm.get_device_error() == 0
     assert_close_to_oracle(run(A, B), A, B, "bf16", full=False, seed=55)
+
+
+# CTA pairs with K split in two: products whose 256 x 256 tiles fill at most
+# half the pairs, with K >= 4096 and C rows on 16-byte boundaries. C is
+# zero-filled, then each K half adds its tile into C with TMA reduce-adds.
+@pytest.mark.parametrize("M,N,K", [(256, 8192, 4096), (130, 264, 4096), (300, 1000, 4104),
+                                   (640, 512, 8192), (512, 2048, 4160)])
+def test_pair_k_split_parity(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=M + N * 3 + K)
+    C = run(A, B)
+    full = M * N * K <= (1 << 31)
+    assert_close_to_oracle(C, A, B, "bf16", full=full, seed=M + K)
+
+
+def test_pair_k_split_small_integer_bit_exact():
+    M, N, K = 384, 520, 4096
+    A, B = workloads.make_inputs(M, N, K, "int", "f32", seed=46)
+    C = run(A.to(torch.bfloat16), B.to(torch.bfloat16))
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_pair_k_split_guard_band_and_repeatability():
+    """The reduce-adds stay inside C, and the two halves' sum repeats exactly."""
+    M, N, K = 300, 1000, 4104
+    A, B = bf16_inputs(M, N, K, seed=47)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf, C = guarded_output(M, N, DEV)
+    rtm.gemm_bf16f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_bf16f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert guard_intact(buf, M, N), "a reduce-add landed outside C"
+    assert torch.equal(C, C2)
+    assert_close_to_oracle(C, A, B, "bf16")
+
+
+def test_pair_k_split_f16_and_workspace_path():
+    """fp16 operands, and operands re-pitched into a workspace (K, N not
+    multiples of 8), through the split CTA-pair kernel."""
+    M, N, K = 256, 1024, 4096
+    A, B = workloads.make_inputs(M, N, K, "normal", "f16", seed=48)
+    C = rtm.gemm_f16f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert_close_to_oracle(C, A, B, "bf16")
+    M, N, K = 300, 132, 4097
+    A, B = bf16_inputs(M, N, K, seed=49)
+    C = rtm.gemm_bf16f32_ws(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "bf16")
