@@ -338,6 +338,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
                  : "memory");
 }
 
+// Arrive on a peer's mbarrier to say "this thread's tensor-memory reads are
+// done" (after tcgen05.wait::ld and tcgen05.fence::before_thread_sync): the
+// waiter needs no memory written by this thread, so CTA scope suffices; the
+// cluster-scope release above cost 0.66 us on GB300 against 0.27 us.
+__device__ __forceinline__ void mbar_arrive_cluster_tmem_free(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 2-D tiled load into this CTA's shared memory whose completion is signalled
 // on an mbarrier in either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
