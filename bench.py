@@ -58,8 +58,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     "gemm_f32": {"bytes": 383779072, "source_sha1": "f2f1b5e280af84d759853c1bb420f8f929f52fed",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
-    "gemm_bf16f32": {"bytes": 1322460672,
-                     "source_sha1": "c783e511080729e042138d66e9ba9af5dfda2306",
+    "gemm_bf16f32": {"bytes": 1335465984,
+                     "source_sha1": "143e4fd6b160b3810890f26054e9fc6bf6e5d7dd",
                      "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {
