@@ -17,7 +17,10 @@
 // Loads and stores move V consecutive values at once (V = 1, 2 or 4: 2-, 4-
 // or 8-byte accesses), the largest V for which every row of A and B starts on
 // a 2V-byte boundary (K and N multiples of V, A and B 2V-byte aligned), so a
-// vector never straddles a row end or a 16-byte swizzle chunk.
+// vector never straddles a row end or a 16-byte swizzle chunk. With 8-byte
+// access the producers issue cp.async copies straight into the swizzled
+// layout and keep three K-slices in flight; the narrower paths stage the
+// values in registers, one K-slice at a time.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -38,6 +41,7 @@ constexpr int kMmaWarp = kProducerWarps;               // warp 8
 constexpr int kFirstEpilogueWarp = kProducerWarps + 1;  // warps 9..12 (quarters 1,2,3,0)
 constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
 constexpr int kGroupM = 16;
+constexpr int kAsyncDepth = 3;  // K-slices in flight per producer thread (cp.async path)
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;
 constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;
 constexpr uint32_t B_STAGE_BYTES = BK * BN * 2;
@@ -117,7 +121,7 @@ __device__ __forceinline__ typename Vec<V>::T vzero()
         return typename Vec<V>::T(0);
 }
 
-template <bool F16, bool C_VEC, int V>
+template <bool F16, bool C_VEC, int V, bool ASYNC>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -164,6 +168,83 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p
     const uint64_t limit = p.limit_ns;
 
     if (warp < kProducerWarps) {
+      if constexpr (ASYNC) {
+        // ------------------------------------------------ producers (cp.async)
+        // V = 2 or 4 (4- or 8-byte copies straight into the swizzled layout,
+        // zero-filled outside M, N, K). A thread's copies for a K-slice form
+        // one cp.async group; up to kAsyncDepth slices are in flight per
+        // thread, and a slice is announced on full[] once the thread's own
+        // copies of it have landed and been fenced for the tensor core, so
+        // no registers hold operands and several slices stream at once.
+        constexpr int A_ROW = BK / V, A_PER = BM * A_ROW / kProducerThreads;
+        constexpr int A_STEP = kProducerThreads / A_ROW;
+        constexpr int B_ROW = BN / V, B_PER = BK * B_ROW / kProducerThreads;
+        constexpr int B_STEP = kProducerThreads / B_ROW;
+        constexpr uint32_t VB = 2 * V;  // bytes per copy
+        static_assert(kAsyncDepth < STAGES, "a reused stage must have been announced");
+        const int tid = threadIdx.x;  // 0 .. 255 among the producer warps
+        const int ar = tid / A_ROW, ac = (tid % A_ROW) * V;
+        const int br = tid / B_ROW, bc = (tid % B_ROW) * V;
+        uint32_t stage = 0, phase = 0, pending = 0, oldest = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok && !*abort; t += gridDim.x) {
+            int m0, n0;
+            tile_coords(t, tiles_m, tiles_n, m0, n0);
+            const uint16_t *pa0 = p.A + (size_t)(m0 + ar) * K + ac;
+            const uint16_t *pb0 = p.B + (size_t)br * N + (n0 + bc);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, limit, abort)) {
+                    give_up(p.err, abort);
+                    ok = false;
+                    break;
+                }
+                const int k0 = kb * BK;
+                const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
+                const uint32_t sB = sA + A_STAGE_BYTES;
+    #pragma unroll
+                for (int j = 0; j < A_PER; ++j) {
+                    const int row = ar + j * A_STEP;
+                    const bool in = m0 + row < M && k0 + ac < K;  // K % V == 0: all or none
+                    const uint16_t *src = in ? pa0 + (size_t)j * A_STEP * K + k0 : p.A;
+                    if constexpr (V == 4)
+                        cp_async_8(sA + swz(row, ac), src, in ? VB : 0u);
+                    else
+                        cp_async_4(sA + swz(row, ac), src, in ? VB : 0u);
+                }
+    #pragma unroll 8
+                for (int j = 0; j < B_PER; ++j) {
+                    const int krow = br + j * B_STEP;
+                    const bool in = k0 + krow < K && n0 + bc < N;  // N % V == 0
+                    const uint16_t *src = in ? pb0 + (size_t)(k0 + j * B_STEP) * N : p.B;
+                    const uint32_t dst = sB + (bc >> 6) * B_ATOM_BYTES + swz(krow, bc & 63);
+                    if constexpr (V == 4)
+                        cp_async_8(dst, src, in ? VB : 0u);
+                    else
+                        cp_async_4(dst, src, in ? VB : 0u);
+                }
+                cp_async_commit();
+                if (++pending == kAsyncDepth) {
+                    cp_async_wait<kAsyncDepth - 1>();  // the oldest slice has landed
+                    fence_proxy_async_shared();
+                    mbar_arrive(&full[oldest]);
+                    oldest = oldest + 1 == STAGES ? 0 : oldest + 1;
+                    --pending;
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // Announce the slices still in flight; on every path (including a
+        // give-up) every copy lands before this thread goes on.
+        cp_async_wait<0>();
+        fence_proxy_async_shared();
+        for (; pending > 0; --pending) {
+            mbar_arrive(&full[oldest]);
+            oldest = oldest + 1 == STAGES ? 0 : oldest + 1;
+        }
+      } else {
         // ------------------------------------------------ producers (plain loads)
         uint32_t stage = 0, phase = 0;
         for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
@@ -269,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p
             if (!ok)
                 break;
         }
+      }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -383,10 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p
     }
 }
 
-template <bool F16, bool C_VEC, int V>
+template <bool F16, bool C_VEC, int V, bool ASYNC = false>
 static cudaError_t launch(const TcLaunch &L, cudaStream_t stream)
 {
-    auto kernel = gemm_tc_any_kernel<F16, C_VEC, V>;
+    auto kernel = gemm_tc_any_kernel<F16, C_VEC, V, ASYNC>;
     static std::atomic<uint64_t> done{0};  // per instantiation
     const cudaError_t e = set_smem_limit_once(kernel, (int)SMEM_BYTES, done);
     if (e != cudaSuccess)
@@ -401,7 +483,11 @@ static cudaError_t launch(const TcLaunch &L, cudaStream_t stream)
 template <bool F16, bool C_VEC>
 static cudaError_t launch_v(const TcLaunch &L, int v, cudaStream_t stream)
 {
-    return v == 4 ? launch<F16, C_VEC, 4>(L, stream)
+    // 8-byte copies through cp.async (several K-slices in flight): 344 -> 529
+    // TFLOP/s at 4096 x 4100 x 4100 on GB300. 4-byte copies stay register-staged:
+    // with twice the copy instructions cp.async was faster only at 8192 x 8190 x
+    // 8190 (331 -> 354) and slower below (2048 x 2050 x 2050: 239 -> 209).
+    return v == 4 ? launch<F16, C_VEC, 4, true>(L, stream)
            : v == 2 ? launch<F16, C_VEC, 2>(L, stream)
                     : launch<F16, C_VEC, 1>(L, stream);
 }

@@ -28,6 +28,14 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
+// 8-byte copy global -> shared; src_bytes in {0, 8} (0: zero-fill).
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 // 16-byte copy global -> shared (L1 bypass); src_bytes in {0, 16}.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
 {

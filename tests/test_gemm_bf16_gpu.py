@@ -360,3 +360,43 @@ def test_pair_k_split_f16_and_workspace_path():
     torch.cuda.synchronize()
     assert rtm.get_device_error() == 0
     assert_close_to_oracle(C, A, B, "bf16")
+
+
+# Rows on 8-byte but not 16-byte boundaries (K and N multiples of 4, not both
+# of 8): the load-and-swizzle kernel's producers copy 8-byte vectors with
+# cp.async, three K-slices in flight.
+@pytest.mark.parametrize("M,N,K", [(1000, 1004, 996), (130, 4100, 4100), (4097, 260, 1028),
+                                   (64, 12, 4), (300, 132, 76)])
+def test_eight_byte_rows_parity(M, N, K):
+    A, B = bf16_inputs(M, N, K, seed=M + 5 * N + K)
+    C = run(A, B)
+    full = M * N * K <= (1 << 31)
+    assert_close_to_oracle(C, A, B, "bf16", full=full, seed=M + N)
+
+
+def test_eight_byte_rows_small_integer_bit_exact_and_guard_band():
+    M, N, K = 520, 132, 4100
+    A, B = workloads.make_inputs(M, N, K, "int", "f32", seed=50)
+    Ad, Bd = A.to(torch.bfloat16).to(DEV), B.to(torch.bfloat16).to(DEV)
+    buf, C = guarded_output(M, N, DEV)
+    rtm.gemm_bf16f32(Ad, Bd, out=C)
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert guard_intact(buf, M, N)
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_eight_byte_offset_pointers_f16():
+    """Operands 8 bytes past a 16-byte boundary (K, N multiples of 8), fp16."""
+    M, N, K = 260, 264, 1000
+    A, B = workloads.make_inputs(M, N, K, "normal", "f16", seed=51)
+    Abuf = torch.zeros(M * K + 4, dtype=torch.float16, device=DEV)
+    Bbuf = torch.zeros(K * N + 4, dtype=torch.float16, device=DEV)
+    Ad = Abuf[4:4 + M * K].view(M, K)
+    Bd = Bbuf[4:4 + K * N].view(K, N)
+    Ad.copy_(A.to(DEV))
+    Bd.copy_(B.to(DEV))
+    C = rtm.gemm_f16f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "bf16")
