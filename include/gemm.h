@@ -120,8 +120,12 @@ typedef enum gemm_f32_kind {
     GEMM_F32_TILES = 1,            /* register-tiled kernel, one CTA per C tile */
     GEMM_F32_TILES_CLUSTER = 2,    /* the same, K split over the CTAs of a cluster */
     GEMM_F32_TILES_WORKSPACE = 3,  /* the same, K split through a workspace + reduction */
-    GEMM_F32_COLUMN_STRIPS = 4     /* M <= 32: column strips (K split over a cluster
+    GEMM_F32_COLUMN_STRIPS = 4,    /* M <= 32: column strips (K split over a cluster
                                       when splits > 1) */
+    GEMM_F32_TILES_TAIL_CLUSTER = 5 /* more tiles than SMs: whole waves of tiles
+                                      unsplit, then the ragged last wave with K split
+                                      over the CTAs of a cluster (splits = cluster
+                                      size) */
 } gemm_f32_kind;
 GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace,
                                int *kind, int *splits);

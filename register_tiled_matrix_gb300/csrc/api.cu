@@ -147,13 +147,12 @@ int64_t padded_copy_bytes(int64_t rows, int64_t cols)
 }
 
 // The register-tiled fp32 product, K split over cluster CTAs when
-// cluster.splits > 1.
+// cluster.splits > 1; otherwise, for products with more tiles than SMs, the
+// ragged last wave may be split over clusters (sgemm_tail_plan).
 cudaError_t run_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
-                          const rtm::SplitK &cluster, cudaStream_t s)
+                          const rtm::SplitK &cluster, int sms, cudaStream_t s)
 {
-    if (cluster.splits > 1)
-        return rtm::launch_sgemm_f32_cluster(M, N, K, A, B, C, cluster, s);
-    return rtm::launch_sgemm_f32(M, N, K, A, B, C, s);
+    return rtm::launch_sgemm_f32_tiles(M, N, K, A, B, C, cluster, sms, s);
 }
 
 bool rows_on_16_bytes(const void *base, int64_t cols)
@@ -171,7 +170,7 @@ cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, f
 {
     if (M <= rtm::kShortMaxM)
         return rtm::launch_sgemm_short(M, N, K, A, B, C, rtm::sgemm_short_splits(M, N, K, sms), s);
-    return run_f32_tiles(M, N, K, A, B, C, rtm::sgemm_cluster_schedule(M, N, K, sms), s);
+    return run_f32_tiles(M, N, K, A, B, C, rtm::sgemm_cluster_schedule(M, N, K, sms), sms, s);
 }
 
 // Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
@@ -374,6 +373,13 @@ int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace, int *k
             if (k == GEMM_F32_NO_KERNEL) {
                 k = cluster.splits > 1 ? GEMM_F32_TILES_CLUSTER : GEMM_F32_TILES;
                 s = cluster.splits;
+                if (cluster.splits <= 1) {
+                    const rtm::TailPlan tail = rtm::sgemm_tail_plan((int)M, (int)N, (int)K, d.sms);
+                    if (tail.tail.splits > 1) {
+                        k = GEMM_F32_TILES_TAIL_CLUSTER;
+                        s = tail.tail.splits;
+                    }
+                }
             }
         }
     }
@@ -428,7 +434,7 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
     const rtm::SplitK &plan = f.workspace;
     const int64_t need = plan.splits > 1 ? (int64_t)plan.splits * M * N * 4 : 0;
     if (need == 0 || workspace_bytes < need)
-        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, s));
+        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, d.sms, s));
     if (overlaps(workspace, need, A, M * K * 4) || overlaps(workspace, need, B, K * N * 4) ||
         overlaps(workspace, need, C, M * N * 4))
         return GEMM_ERR_INVALID_ARG;

@@ -114,6 +114,20 @@ SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&residen
 int sgemm_cluster_resident_spread(int cluster_size);
 // sgemm_cluster_plan with the current device's cluster residency.
 SplitK sgemm_cluster_schedule(int M, int N, int K, int sm_count, double *est = nullptr);
+// Products with more tiles than SMs: tiles 0 .. plain_tiles - 1 run as the
+// plain product, the rest with K split over clusters (tail.splits > 1; none
+// when tail.splits == 1). sgemm_plan.cu.
+struct TailPlan {
+    long long plain_tiles;
+    SplitK tail;
+};
+TailPlan sgemm_tail_plan(int M, int N, int K, int sm_count);
+cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const float *B, float *C,
+                                  const TailPlan &plan, cudaStream_t stream);
+// The register-tiled product on its own schedule: K split over clusters when
+// cluster.splits > 1, else the tail plan, else the plain product.
+cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
+                                   const SplitK &cluster, int sm_count, cudaStream_t stream);
 // How gemm_f32_ws (and gemm_f32_noalloc) schedule a product with M > kShortMaxM:
 // the workspace split when the model prices it below the cluster split (ties
 // go to the workspace), else the cluster split or the plain product.

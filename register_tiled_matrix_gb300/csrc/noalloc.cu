@@ -122,9 +122,7 @@ extern "C" int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
         const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, sc.sms);
         const rtm::SplitK &plan = f.workspace;
         if (plan.splits <= 1) {
-            e = f.cluster.splits > 1
-                    ? rtm::launch_sgemm_f32_cluster((int)M, (int)N, (int)K, A, B, C, f.cluster, s)
-                    : rtm::launch_sgemm_f32((int)M, (int)N, (int)K, A, B, C, s);
+            e = rtm::launch_sgemm_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, sc.sms, s);
         } else {
             if ((int64_t)plan.splits * M * N * (int64_t)sizeof(float) > kScratchBytes)
                 return GEMM_ERR_INVALID_ARG;  // needs more than the fixed 24 MiB of scratch

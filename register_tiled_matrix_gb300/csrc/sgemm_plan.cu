@@ -139,4 +139,37 @@ SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&residen
     return p;
 }
 
+// Products with more 128 x 128 tiles than SMs: the whole waves of CTA slots
+// (2 per SM) run as the plain product, and the ragged last wave can run as a
+// second launch with K split over clusters of 4 CTAs. Measured on GB300 (plain
+// against prefix + split tail): 4097 x 3001 x 1023 601.9 -> 550.8 us, 3072 x 2048
+// x 4096 1015.5 -> 955.1, 2048 x 2048 x 4096 679.2 -> 622.9, 6144^2 x 2048
+// 2611.1 -> 2550.8; but 4096^3 2310.8 -> 2357.0, 8192^2 x 2048 and 5000^2 x 1000
+// slower too: after several full waves a tail of at most one tile per SM
+// already runs one CTA per SM and the second launch loses the overlap of the
+// last wave with the one before. So the tail is split only when it holds more
+// tiles than SMs or the product has fewer than two full waves, and every chunk
+// keeps at least 4 K-slices.
+TailPlan sgemm_tail_plan(int M, int N, int K, int sm_count)
+{
+    TailPlan t{0, SplitK{1, K}};
+    if (M <= kShortTileM || N <= kNarrowN || sm_count <= 0)
+        return t;  // the tail schedule is measured for 128 x 128 tiles only
+    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
+    const long long slots = 2LL * sm_count;
+    if (tiles <= sm_count)
+        return t;  // sgemm_cluster_plan's case
+    const long long plain = tiles / slots * slots;
+    const long long tail = tiles - plain;
+    const long long kslices = (K + kSliceK - 1) / kSliceK;
+    constexpr int S = 4;
+    const long long chunk = (kslices + S - 1) / S;
+    if (tail == 0 || !(tail > sm_count || tiles < 2 * slots) || chunk < 4 ||
+        (long long)S * chunk - kslices >= chunk)
+        return t;
+    t.plain_tiles = plain;
+    t.tail = SplitK{S, (int)(chunk * kSliceK)};
+    return t;
+}
+
 } // namespace rtm

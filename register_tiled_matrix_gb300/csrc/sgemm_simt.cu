@@ -106,10 +106,12 @@ __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n,
 // same masks as the plain epilogue. Kept out of line: inlined, it cost the k
 // loop of the 4-byte-copy variant spilled registers.
 template <int BM, int BN, int PITCH, bool C_VEC>
-__device__ __noinline__ void cluster_add_partials(const float *part, int M, int N, float *C)
+__device__ __noinline__ void cluster_add_partials(const float *part, int M, int N, float *C,
+                                                  int first_tile)
 {
     int tile_m, tile_n;
-    tile_of_block((int)blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tile_m, tile_n);
+    tile_of_block((int)blockIdx.x + first_tile, (M + BM - 1) / BM, (N + BN - 1) / BN, tile_m,
+                  tile_n);
     const int m0 = tile_m * BM, n0 = tile_n * BN;
     const uint32_t S = gridDim.y;  // cluster of (1, S, 1): rank == blockIdx.y
     const uint32_t rank = blockIdx.y;
@@ -151,12 +153,14 @@ template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, b
           int SPLIT>
 __global__ void __launch_bounds__(kThreads, MINB)
     sgemm_rt_kernel(int M, int N, int K_total, int kchunk, const float *__restrict__ A,
-                    const float *__restrict__ B, float *__restrict__ C, size_t c_split_stride)
+                    const float *__restrict__ B, float *__restrict__ C, size_t aux)
 {
     // Split-K: CTA row blockIdx.y of the grid sums k in [y * kchunk, +kchunk);
     // A keeps its full row stride K_total. kSplitWorkspace writes the partial
-    // tile to C + y * c_split_stride; kSplitCluster adds the partial tiles of
-    // the cluster's CTAs (the K chunks of one tile) after the k loop. The plain
+    // tile to C + y * aux (aux: floats between slabs); kSplitCluster adds the
+    // partial tiles of the cluster's CTAs (the K chunks of one tile) after the
+    // k loop, and its grid covers tiles aux .. aux + gridDim.x - 1 (a plain
+    // grid always starts at tile 0 and may stop early). The plain
     // product is compiled without any of this (the extra runtime offsets changed
     // the register allocation of the FFMA loop and cost 6 % on GB300).
     int lda = K_total;
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         A += k_begin;
         B += (size_t)k_begin * N;
         if constexpr (SPLIT == kSplitWorkspace)
-            C += blockIdx.y * c_split_stride;
+            C += blockIdx.y * aux;
     }
 
     using G = Cfg<BM, BN, BK, STAGES>;
@@ -188,7 +192,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int tiles_m = (M + BM - 1) / BM;
     const int tiles_n = (N + BN - 1) / BN;
     int tile_m, tile_n;
-    tile_of_block(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
+    if constexpr (SPLIT == kSplitCluster)
+        tile_of_block((int)blockIdx.x + (int)aux, tiles_m, tiles_n, tile_m, tile_n);
+    else
+        tile_of_block(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
     const int m0 = tile_m * BM;
     const int n0 = tile_n * BN;
 
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         make_float4(v[0], v[1], v[2], v[3]);
                 }
         cluster_sync();
-        cluster_add_partials<BM, BN, PITCH, C_VEC>(smem, M, N, C);
+        cluster_add_partials<BM, BN, PITCH, C_VEC>(smem, M, N, C, (int)aux);
         cluster_sync();
     } else {
         // Epilogue: masked stores, 128-bit where the row allows it.
@@ -435,8 +442,12 @@ constexpr size_t kSpreadSmemBytes = 120 * 1024;
 
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, bool B_VEC, bool C_VEC,
           int SPLIT>
+// tile_first / tile_count: launch only tiles tile_first .. +tile_count - 1 of
+// the grouped raster (tile_count < 0: all from tile_first on); a plain or
+// workspace grid must start at tile 0.
 cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, float *C,
-                       cudaStream_t stream, int splits = 1, int kchunk = 0, bool spread = false)
+                       cudaStream_t stream, int splits = 1, int kchunk = 0, bool spread = false,
+                       long long tile_first = 0, long long tile_count = -1)
 {
     static_assert(Cfg<BM, BN, BK, STAGES>::CLUSTER_SMEM_BYTES <= kSpreadSmemBytes,
                   "the spread reservation holds the pipeline and the partial tile");
@@ -454,9 +465,16 @@ cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, floa
         if (e != cudaSuccess)
             return e;
     }
-    const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    if (tiles > 0x7fffffffLL)
+    const long long all_tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (all_tiles > 0x7fffffffLL)
         return cudaErrorInvalidValue;
+    if (tile_first < 0 || tile_first > all_tiles || (SPLIT != kSplitCluster && tile_first != 0))
+        return cudaErrorInvalidValue;
+    const long long tiles = tile_count < 0 || tile_first + tile_count > all_tiles
+                                ? all_tiles - tile_first
+                                : tile_count;
+    if (tiles == 0)
+        return cudaSuccess;
     if (splits < 1 || splits > 65535 || (SPLIT == kPlain && splits != 1))
         return cudaErrorInvalidValue;
     if (splits == 1)
@@ -477,7 +495,7 @@ cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, floa
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kernel, M, N, K, kchunk, A, B, C, (size_t)M * N);
+        return cudaLaunchKernelEx(&cfg, kernel, M, N, K, kchunk, A, B, C, (size_t)tile_first);
     }
     kernel<<<dim3((unsigned)tiles, (unsigned)splits), kThreads, smem, stream>>>(
         M, N, K, kchunk, A, B, C, (size_t)M * N);
@@ -486,7 +504,8 @@ cudaError_t launch_cfg(int M, int N, int K, const float *A, const float *B, floa
 
 template <int BM, int BN, int BK, int STAGES, int MINB, int ORDER, int SPLIT = kPlain>
 cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, float *C,
-                       cudaStream_t stream, int splits = 1, int kchunk = 0, bool spread = false)
+                       cudaStream_t stream, int splits = 1, int kchunk = 0, bool spread = false,
+                       long long tile_first = 0, long long tile_count = -1)
 {
     const bool b_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(B) & 15) == 0);
     const bool c_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
@@ -494,12 +513,12 @@ cudaError_t launch_any(int M, int N, int K, const float *A, const float *B, floa
     // takes the 4-byte C stores.
     if (b_vec && c_vec)
         return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, true, SPLIT>(
-            M, N, K, A, B, C, stream, splits, kchunk, spread);
+            M, N, K, A, B, C, stream, splits, kchunk, spread, tile_first, tile_count);
     if (b_vec)
         return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, true, false, SPLIT>(
-            M, N, K, A, B, C, stream, splits, kchunk, spread);
+            M, N, K, A, B, C, stream, splits, kchunk, spread, tile_first, tile_count);
     return launch_cfg<BM, BN, BK, STAGES, MINB, ORDER, false, false, SPLIT>(
-        M, N, K, A, B, C, stream, splits, kchunk, spread);
+        M, N, K, A, B, C, stream, splits, kchunk, spread, tile_first, tile_count);
 }
 
 } // namespace simt
@@ -645,6 +664,33 @@ cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const 
                      M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread)
                : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
                      M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread);
+}
+
+cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const float *B, float *C,
+                                  const TailPlan &plan, cudaStream_t stream)
+{
+    using simt::kSplitCluster;
+    if (M <= kShortTileM || N <= kNarrowN || plan.tail.splits < 2)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaSuccess;
+    if (plan.plain_tiles > 0)
+        e = simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream, 1, 0, false,
+                                                               0, plan.plain_tiles);
+    if (e != cudaSuccess)
+        return e;
+    return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
+        M, N, K, A, B, C, stream, plan.tail.splits, plan.tail.kchunk, false, plan.plain_tiles);
+}
+
+cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
+                                   const SplitK &cluster, int sm_count, cudaStream_t stream)
+{
+    if (cluster.splits > 1)
+        return launch_sgemm_f32_cluster(M, N, K, A, B, C, cluster, stream);
+    const TailPlan tail = sgemm_tail_plan(M, N, K, sm_count);
+    if (tail.tail.splits > 1)
+        return launch_sgemm_f32_tail(M, N, K, A, B, C, tail, stream);
+    return launch_sgemm_f32(M, N, K, A, B, C, stream);
 }
 
 } // namespace rtm

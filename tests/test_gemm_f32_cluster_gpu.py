@@ -99,7 +99,6 @@ def test_workspace_entry_takes_the_cheaper_split():
     assert rtm.gemm_f32_workspace_bytes(512, 512, 8192) > 0
     assert rtm.gemm_f32_schedule(512, 512, 8192, workspace=True)[0] == "tiles+workspace-split"
     assert rtm.gemm_f32_schedule(512, 512, 8192)[0] == "tiles+cluster-split"
-    assert rtm.gemm_f32_schedule(4096, 4096, 4096) == ("tiles", 1)
     assert rtm.gemm_f32_schedule(16, 8192, 8192)[0] == "column-strips"
     for M, N, K in [(1024, 1024, 1024), (512, 512, 8192)]:
         A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M + K)
@@ -111,3 +110,51 @@ def test_workspace_entry_takes_the_cheaper_split():
         assert_close_to_oracle(C, A, B, "f32")
         if M == 1024:
             assert torch.equal(C, Cw), "no workspace needed: both entries run the same schedule"
+
+
+# More tiles than SMs: whole waves of tiles unsplit, then the ragged last wave
+# with K split over clusters of 4 (a second launch starting at a tile offset).
+TAIL_SHAPES = [
+    (2048, 1536, 1024),  # 192 tiles, fewer than two waves: all of them split
+    (3072, 2048, 1000),  # 304 tiles unsplit + 80 split, ragged K
+    (2050, 1540, 520),   # 221 edge-heavy tiles, 5-slice chunks
+]
+
+
+@pytest.mark.parametrize("M,N,K", TAIL_SHAPES)
+def test_tail_split_parity(M, N, K):
+    kind, splits = rtm.gemm_f32_schedule(M, N, K)
+    assert kind == "tiles+tail-cluster-split" and splits == 4, (kind, splits)
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M + 3 * N + K)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+def test_tail_split_config_4097x3001x1023_sampled():
+    """The ragged 4097 x 3001 x 1023 workload: 608 tiles unsplit, 184 split."""
+    w = workloads.WORKLOADS["f32_4097x3001x1023"]
+    assert rtm.gemm_f32_schedule(w.M, w.N, w.K)[0] == "tiles+tail-cluster-split"
+    A, B = workloads.workload_inputs(w)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert_close_to_oracle(C, A, B, "f32", full=False, seed=w.seed)
+
+
+def test_tail_split_small_integer_guard_band_repeatability():
+    M, N, K = 2050, 1540, 520
+    A, B = small_int_inputs(M, N, K, seed=52)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf, C = guarded_output(M, N, DEV)
+    rtm.gemm_f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N)
+    assert torch.equal(C, C2)
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_square_headline_stays_unsplit():
+    assert rtm.gemm_f32_schedule(4096, 4096, 4096) == ("tiles", 1)
+    assert rtm.gemm_f32_schedule(8192, 8192, 8192) == ("tiles", 1)
