@@ -117,7 +117,7 @@ def test_workspace_entry_takes_the_cheaper_split():
 TAIL_SHAPES = [
     (2048, 1536, 1024),  # 192 tiles, fewer than two waves: all of them split
     (3072, 2048, 1000),  # 304 tiles unsplit + 80 split, ragged K
-    (2050, 1540, 520),   # 221 edge-heavy tiles, 5-slice chunks
+    (2050, 1540, 1100),  # 221 edge-heavy tiles, 9-slice chunks, ragged K
 ]
 
 
@@ -143,7 +143,7 @@ def test_tail_split_config_4097x3001x1023_sampled():
 
 
 def test_tail_split_small_integer_guard_band_repeatability():
-    M, N, K = 2050, 1540, 520
+    M, N, K = 2050, 1540, 1100
     A, B = small_int_inputs(M, N, K, seed=52)
     Ad, Bd = A.to(DEV), B.to(DEV)
     buf, C = guarded_output(M, N, DEV)
@@ -155,6 +155,7 @@ def test_tail_split_small_integer_guard_band_repeatability():
     assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
 
 
-def test_square_headline_stays_unsplit():
-    assert rtm.gemm_f32_schedule(4096, 4096, 4096) == ("tiles", 1)
+def test_tail_split_rule_leaves_these_unsplit():
+    assert rtm.gemm_f32_schedule(4096, 4096, 4096) == ("tiles", 1)  # 112-tile tail after 3 waves
     assert rtm.gemm_f32_schedule(8192, 8192, 8192) == ("tiles", 1)
+    assert rtm.gemm_f32_schedule(2048, 2304, 512) == ("tiles", 1)   # 4-slice chunks, 95 % full
