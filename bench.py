@@ -56,10 +56,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
 # reported as null once the source changes. See profiles/.
 TRAFFIC = {
-    "gemm_f32": {"bytes": 383779072, "source_sha1": "f2f1b5e280af84d759853c1bb420f8f929f52fed",
+    "gemm_f32": {"bytes": 384730880, "source_sha1": "42150b9fe7160333adf77e7d147a49e0ad114abf",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
-    "gemm_bf16f32": {"bytes": 1335465984,
-                     "source_sha1": "143e4fd6b160b3810890f26054e9fc6bf6e5d7dd",
+    "gemm_bf16f32": {"bytes": 1606195200,
+                     "source_sha1": "f047523335d2949217ffe72c92eb1bd70e6f58f2",
                      "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {
@@ -196,6 +196,29 @@ def make_step_inputs(device, names):
     return items
 
 
+def count_kernel_launches(fn) -> Optional[int]:
+    """How many kernels one call of fn launches, counted from the device kernel
+    activities (memory copies and sets excluded) the PyTorch profiler records
+    for that call. None when the count cannot be taken."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+
+        def kernels():
+            torch.cuda.synchronize()
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                fn()
+                torch.cuda.synchronize()
+            return sum(1 for e in prof.events()
+                       if str(getattr(e, "device_type", "")).endswith("CUDA")
+                       and not e.name.startswith(("Memcpy", "Memset")))
+
+        kernels()  # the first session may start the tracer after the launches
+        n = kernels()
+        return n if n > 0 else None
+    except Exception:  # a count, not a result: report it as unknown
+        return None
+
+
 def kernel_of(w) -> str:
     return "gemm_f32" if w.dtype == "f32" else "gemm_bf16f32"
 
@@ -278,7 +301,10 @@ def run_ours(args) -> Optional[Dict]:
     dev_err = rtm.get_device_error()
     if dev_err != 0:
         raise SystemExit(f"device error in the timed region: {rtm.status_string(dev_err)}")
-    launches = args.steps * len(items)
+    per_call = [count_kernel_launches(
+        lambda it=it: fns[kernel_of(it["w"])](it["A"], it["B"], out=it["C"])) for it in items]
+    launches = args.steps * sum(n if n is not None else 1 for n in per_call)
+    launch_note = {it["name"]: n for it, n in zip(items, per_call)}
 
     kernel_ms = {}
     for i, it in enumerate(items):
@@ -410,6 +436,7 @@ def run_ours(args) -> Optional[Dict]:
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
                 if e2e_steps else None),
         "gpu_launches": launches,
+        "gpu_launches_per_call": launch_note,
         "clocks": clock_summary,
         "peaks": {"source": peaks["source"], "fp32_simt_tflops": round(fp32_peak, 2),
                   "bf16_tflops_burst": bf16_peak, "bf16_tflops_sustained": bf16_sustained},

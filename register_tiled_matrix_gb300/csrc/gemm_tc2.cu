@@ -105,18 +105,30 @@ struct Params {
     int *err;
     unsigned long long limit_ns;
     int mute_producer;
-    int splits;  // 1, or 2: K halves added into a zeroed C (TMA-store epilogue only)
+    int split_from;  // tiles from here on: K halves added into a zeroed C (TMA-store
+                     // epilogue only); the tile count for none
 };
 
-// Work unit u of the persistent loop: tile u / splits, K-blocks
-// [kb_begin, kb_end) of its split u % splits (every split non-empty: the host
-// splits only K of at least two blocks).
-__device__ __forceinline__ void unit_kblocks(int u, int splits, int kblocks, int &kb_begin,
-                                             int &kb_end)
+// Work unit u of the persistent loop: tiles before split_from are one unit
+// each (all K-blocks), every later tile two units, its K halves (each half
+// non-empty: the host splits only K of at least two blocks). A split unit adds
+// its tile into C instead of storing it.
+__device__ __forceinline__ void unit_of(int u, int split_from, int kblocks, int &tile,
+                                        int &kb_begin, int &kb_end, bool &split)
 {
-    const int per = (kblocks + splits - 1) / splits;
-    kb_begin = (u % splits) * per;
-    kb_end = min(kblocks, kb_begin + per);
+    if (u < split_from) {
+        tile = u;
+        kb_begin = 0;
+        kb_end = kblocks;
+        split = false;
+    } else {
+        const int v = u - split_from;
+        const int per = (kblocks + 1) / 2;
+        tile = split_from + (v >> 1);
+        kb_begin = (v & 1) * per;
+        kb_end = min(kblocks, kb_begin + per);
+        split = true;
+    }
 }
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &n0)
@@ -189,8 +201,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const int tiles_m = (p.M + PM - 1) / PM;
     const int tiles_n = (p.N + PN - 1) / PN;
-    const int splits = p.splits;
-    const int nunits = tiles_m * tiles_n * splits;
+    const int split_from = p.split_from;
+    const int nunits = split_from + 2 * (tiles_m * tiles_n - split_from);
     const int kblocks = (p.K + BK - 1) / BK;
     const uint64_t limit = p.limit_ns;
 
@@ -200,9 +212,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             uint32_t issued = 0, issued_parity = 0;
             for (int u = cluster_id; u < nunits && !*abort; u += num_clusters) {
-                int m0, n0, kb_begin, kb_end;
-                tile_coords(u / splits, tiles_m, tiles_n, m0, n0);
-                unit_kblocks(u, splits, kblocks, kb_begin, kb_end);
+                int m0, n0, tile, kb_begin, kb_end;
+                bool split;
+                unit_of(u, split_from, kblocks, tile, kb_begin, kb_end, split);
+                tile_coords(tile, tiles_m, tiles_n, m0, n0);
                 const int row0 = m0 + (int)rank * HM;
                 const int col0 = n0 + (int)rank * HN;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
@@ -249,8 +262,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t acc = 0, acc_phase = 0;
             bool issued_any = false;
             for (int u = cluster_id; u < nunits && !*abort; u += num_clusters) {
-                int kb_begin, kb_end;
-                unit_kblocks(u, splits, kblocks, kb_begin, kb_end);
+                int tile, kb_begin, kb_end;
+                bool split;
+                unit_of(u, split_from, kblocks, tile, kb_begin, kb_end, split);
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, limit, abort)) {
                     give_up(p.err, abort);
                     break;
@@ -302,8 +316,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         uint32_t acc = 0, acc_phase = 0;
         for (int u = cluster_id; u < nunits && !*abort; u += num_clusters) {
-            int m0, n0;
-            tile_coords(u / splits, tiles_m, tiles_n, m0, n0);
+            int m0, n0, tile, kb_begin, kb_end;
+            bool split;
+            unit_of(u, split_from, kblocks, tile, kb_begin, kb_end, split);
+            tile_coords(tile, tiles_m, tiles_n, m0, n0);
             if (!mbar_wait_bounded(&tfull[acc], acc_phase, limit, abort)) {
                 give_up(p.err, abort);
                 break;
@@ -388,7 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int b = 0; b < (second ? 2 : 1); ++b) {
                             const uint32_t src = smem_u32(boxes + b * EPI_BOX_BYTES);
                             const int col = n0 + (c + b) * 32;
-                            if (splits > 1)
+                            if (split)
                                 tma_reduce_add_2d(&tmC, src, col, row0);
                             else
                                 tma_store_2d(&tmC, src, col, row0);
@@ -414,6 +430,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+// Zero the C tiles from tile `first` on (those whose K halves are added into
+// C), clipped to M x N: one CTA per tile, float4 stores (this path has C rows
+// on 16-byte boundaries, N % 4 == 0, so every clipped row is whole float4s).
+__global__ void zero_tiles_kernel(float *C, int M, int N, int first)
+{
+    int m0, n0;
+    tile_coords(first + (int)blockIdx.x, (M + PM - 1) / PM, (N + PN - 1) / PN, m0, n0);
+    const int rows = min(PM, M - m0), quads = min(PN, N - n0) / 4;
+    for (int i = threadIdx.x; i < rows * quads; i += blockDim.x) {
+        const int r = i / quads, q = i - r * quads;
+        *reinterpret_cast<float4 *>(C + (size_t)(m0 + r) * N + n0 + 4 * q) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -510,24 +541,44 @@ cudaError_t launch_gemm_tc_pair_split(const TcLaunch &L, int splits, cudaStream_
             max_clusters[fi][dev].store(clusters_max);
     }
     const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
-    // splits == 0: choose. Products whose tiles fill at most half the pairs
-    // split K in two (each half adds its tile into a zeroed C with TMA
-    // reduce-adds; 0 + a + b is the same in either order, so the result still
-    // repeats exactly), when both halves keep at least 32 K-blocks.
+    // splits == 0: choose. A tile split in two adds each K half into a zeroed
+    // C with TMA reduce-adds; 0 + a + b is the same in either order, so the
+    // result still repeats exactly. Split when both halves keep at least 32
+    // K-blocks and either
+    //  * all tiles fill at most half the pairs (256 x 8192 x 8192: 45.1 ->
+    //    37.2 us), or
+    //  * the last round of the persistent loop is at most half full: its
+    //    tiles become two half-length units each (8192^3: 13 rounds of 76
+    //    tiles, then 36 tiles on 72 pairs for half a round), only those tiles
+    //    zeroed first.
     const int kblocks = (L.K + BK - 1) / BK;
-    if (splits == 0)
-        splits = (c_vec && 2 * ntiles <= clusters_max && kblocks >= 64) ? 2 : 1;
-    if (splits != 1 && (splits != 2 || !c_vec || kblocks < 2))
+    if (splits < 0 || splits > 2)
         return cudaErrorInvalidValue;
-    const long long nunits = ntiles * splits;
-    const int clusters = (int)(nunits < clusters_max ? nunits : clusters_max);
-    if (splits > 1) {
-        e = launch_zero_fill(L.C, (int64_t)L.M * L.N, stream);
-        if (e != cudaSuccess)
-            return e;
+    long long split_from = ntiles;
+    if (splits == 2) {
+        split_from = 0;
+    } else if (splits == 0 && c_vec && kblocks >= 64) {
+        const long long tail = ntiles % clusters_max;
+        if (2 * ntiles <= clusters_max)
+            split_from = 0;
+        else if (ntiles > clusters_max && tail > 0 && 2 * tail <= clusters_max)
+            split_from = ntiles - tail;
     }
+    if (split_from < ntiles && (!c_vec || kblocks < 2))
+        return cudaErrorInvalidValue;
+    const long long nunits = split_from + 2 * (ntiles - split_from);
+    const int clusters = (int)(nunits < clusters_max ? nunits : clusters_max);
+    if (split_from == 0) {
+        e = launch_zero_fill(L.C, (int64_t)L.M * L.N, stream);
+    } else if (split_from < ntiles) {
+        zero_tiles_kernel<<<(unsigned)(ntiles - split_from), 256, 0, stream>>>(L.C, L.M, L.N,
+                                                                             (int)split_from);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess)
+        return e;
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer,
-             splits};
+             (int)split_from};
     kernel<<<2 * clusters, kThreads, smem_bytes, stream>>>(ta, tb, tc, p);
     return cudaGetLastError();
 }
