@@ -9,12 +9,14 @@
 //
 //  * global tiling — a CTA owns 256 columns of C and, when that leaves SMs
 //    idle, one of S K-ranges (S = 2, 4 or 8 CTAs of one cluster split K);
-//  * shared tiling — a 10-stage cp.async ring of 16-deep K-slices (about
-//    165 KB of B in flight per CTA: on GB300 one SM streams only 30-40 GB/s
-//    with 100-160 KB outstanding, so reading B at HBM speed takes most SMs and
-//    a deep ring each): B as stored (16 x 256, 16-byte copies where B's rows
-//    allow) and A transposed to k-major (16 x MR, rows padded to MR + 4
-//    floats);
+//  * shared tiling — a 6-stage cp.async ring of 16-deep K-slices (about
+//    100 KB of B in flight per CTA, two CTAs per SM: on GB300 one SM streams
+//    only 30-40 GB/s with 100-160 KB outstanding, so reading B at HBM speed
+//    takes most SMs, and two rings per SM let K be split eight ways with
+//    every cluster resident; 10 stages at one CTA per SM were 16-26 % slower:
+//    1 x 8192 x 8192 61.5 -> 51.7 us, 16 x 8192 x 8192 108.6 -> 82.0 us):
+//    B as stored (16 x 256, 16-byte copies where B's rows allow) and A
+//    transposed to k-major (16 x MR, rows padded to MR + 4 floats);
 //  * register tiling — thread t keeps C[0..MR)[n0 + 2t .. n0 + 2t + 1] in
 //    registers; per k it reads two B values (one 64-bit read; consecutive
 //    threads, consecutive words) and MR values of A (128-bit broadcast reads)
@@ -38,7 +40,7 @@ namespace sshort {
 
 constexpr int BN = 256;      // columns of C per CTA
 constexpr int BK = 16;       // K-slice depth
-constexpr int STAGES = 10;   // about 165 KB of B in flight per CTA
+constexpr int STAGES = 6;    // about 100 KB of B in flight per CTA, two CTAs per SM
 
 template <int MR>
 struct Cfg {
@@ -254,11 +256,11 @@ int sgemm_short_splits(int M, int N, int K, int sm_count)
     (void)M;
     const long long blocks = (N + sshort::BN - 1) / sshort::BN;
     int splits = 1;
-    while (splits < 8 && blocks * splits * 2 <= sm_count && K / (splits * 2) >= 256)
+    // Up to two CTAs per SM, at least 256 of K per CTA.
+    while (splits < 8 && blocks * splits * 2 <= 2LL * sm_count && K / (splits * 2) >= 256)
         splits *= 2;
-    // Clusters of 8 such CTAs (about 180 KB of shared memory each) fit only
-    // 15 at a time on a 152-SM GPU: a cluster that must wait for another to
-    // finish doubles the time, so 8 only when every cluster is resident.
+    // A cluster that must wait for another to finish doubles the time, so 8
+    // only when every cluster of 8 is resident at once.
     if (splits == 8 && blocks > resident_clusters_of_8())
         splits = 4;
     return splits;

@@ -176,16 +176,19 @@ def test_narrow_tile_boundary(N):
     assert_bit_exact(run(Ai, Bi), (Ai.to(torch.int64) @ Bi.to(torch.int64)).numpy())
 
 
-# M <= 32: one column of C per thread, K split over S CTAs of a cluster
-# (S for a 152-SM GPU noted); no workspace in any fp32 entry point.
-@pytest.mark.parametrize("M,N,K", [(1, 8192, 4096),    # S = 4
-                                   (7, 1000, 999),     # S = 1
-                                   (16, 257, 3000),    # S = 4, 4-byte B copies
+# M <= 32: two columns of C per thread, K split over S CTAs of a cluster
+# (S for a 152-SM GPU noted: up to two CTAs per SM, S = 8 when every cluster
+# of 8 is resident); no workspace in any fp32 entry point.
+@pytest.mark.parametrize("M,N,K", [(1, 8192, 4096),    # S = 8: clusters of 8
+                                   (7, 1000, 999),     # S = 2
+                                   (16, 257, 3000),    # S = 8, 4-byte B copies
                                    (32, 4096, 8192),   # S = 8
                                    (17, 64, 33),       # 32 accumulators, one CTA
                                    (1, 1, 1),
-                                   (9, 8190, 2048),    # S = 4, 4-byte B copies
-                                   (32, 2048, 8192)])  # S = 8: clusters of 8
+                                   (9, 8190, 2048),    # S = 8, 4-byte B copies
+                                   (32, 2048, 8192),   # S = 8
+                                   (8, 16384, 4096),   # S = 4
+                                   (9, 12290, 2048)])  # S = 4, 4-byte B copies
 def test_short_wide_parity(M, N, K):
     A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M * 31 + N + K)
     C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
