@@ -99,7 +99,9 @@ typedef enum gemm_status {
  * Larger products with too few C tiles to fill the GPU split K the same way:
  * the 2, 4 or 8 CTAs that share a C tile form a thread-block cluster, park
  * their partial tiles in shared memory and add them through distributed
- * shared memory in rank order (gemm_f32_schedule reports the choice).
+ * shared memory in rank order. Products with more tiles than SMs may run
+ * their whole waves of tiles unsplit and the ragged last wave split that way,
+ * as a second launch. gemm_f32_schedule reports the choice.
  */
 GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K,
                       const float *A, const float *B, float *C, void *stream);
