@@ -1,0 +1,27 @@
+// Test driver (host code only): prints the fp32 schedule planners' choices for
+// the shapes given on the command line as M,N,K triples, for a 152-SM GPU whose
+// cluster-split CTAs fit 76 clusters of 2, 36 of 4 and 15 of 8 at one CTA per
+// SM (the occupancy the library queries on GB300). Built and run by
+// tests/test_plan_host.py; no GPU is needed.
+#include <cstdio>
+#include <cstdlib>
+
+#include "kernels.h"
+
+int main(int argc, char **argv)
+{
+    const int sms = 152;
+    const int resident[3] = {76, 36, 15};
+    for (int i = 1; i + 2 < argc; i += 3) {
+        const int M = std::atoi(argv[i]), N = std::atoi(argv[i + 1]), K = std::atoi(argv[i + 2]);
+        double cluster_est = 0;
+        const rtm::SplitK c = rtm::sgemm_cluster_plan(M, N, K, sms, resident, &cluster_est);
+        const rtm::SplitK w = rtm::sgemm_splitk_plan(M, N, K, sms);
+        const double w_est = rtm::sgemm_workspace_estimate(M, N, K, sms, w);
+        const bool ws_wins = w.splits > 1 && !(cluster_est < w_est);
+        const rtm::TailPlan t = rtm::sgemm_tail_plan(M, N, K, sms);
+        std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d\n", M, N, K, c.splits,
+                    c.spread ? 1 : 0, w.splits, ws_wins ? 1 : 0, t.plain_tiles, t.tail.splits);
+    }
+    return 0;
+}

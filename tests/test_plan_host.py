@@ -1,0 +1,68 @@
+"""CPU tests of the fp32 schedule planners (host code in sgemm_plan.cu): a
+driver built from tests/plan_driver.cu prints each planner's choice for a
+152-SM GB300, and the choices the GB300 sweeps justified are checked here:
+which products split K over clusters and into how many CTAs, when the
+workspace split is priced below the cluster split, and when the ragged last
+wave of a larger product is split."""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import register_tiled_matrix_gb300 as rtm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "register_tiled_matrix_gb300", "csrc")
+
+# (M, N, K): (cluster splits, spread, workspace splits, workspace priced lower,
+#             unsplit tiles before the tail, tail splits)
+EXPECT = {
+    (256, 256, 256): (8, 1, 8, 0, 0, 1),        # 4 tiles: 8 per cluster, one CTA per SM
+    (1024, 1024, 1024): (4, 0, 2, 0, 0, 1),     # 52.8 us split 4, 55.4 with the workspace
+    (1000, 1000, 999): (4, 0, 2, 0, 0, 1),
+    (300, 260, 129): (2, 0, 5, 1, 0, 1),
+    (512, 512, 8192): (8, 0, 9, 1, 0, 1),       # long K over 16 tiles: the workspace wins
+    (8192, 64, 4096): (4, 0, 7, 1, 0, 1),       # 128 x 64 tiles
+    (64, 8192, 8192): (4, 0, 7, 1, 0, 1),       # 64-row tiles
+    (2048, 1024, 1024): (1, 0, 1, 0, 0, 1),     # 128 tiles: split was no faster
+    (4096, 4096, 4096): (1, 0, 1, 0, 0, 1),     # 3 waves + 112 tiles: tail left alone
+    (4097, 3001, 1023): (1, 0, 1, 0, 608, 4),   # 608 tiles + a 184-tile tail split
+    (2304, 2304, 4096): (1, 0, 1, 0, 304, 4),   # one wave + 20 tiles
+    (2048, 1536, 1024): (1, 0, 1, 0, 0, 4),     # 192 tiles, under two waves
+    (2048, 2304, 512): (1, 0, 1, 0, 0, 1),      # 4-slice chunks, 95 % of the slots
+}
+
+
+@pytest.fixture(scope="module")
+def driver(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    out = str(tmp_path_factory.mktemp("plan") / "plan_driver")
+    cmd = [nvcc, "-std=c++17", "-O2", "-I", CSRC, "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "plan_driver.cu"), os.path.join(CSRC, "sgemm_plan.cu"),
+           "-o", out]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    return out
+
+
+def test_planner_choices(driver):
+    args = [str(x) for shape in EXPECT for x in shape]
+    r = subprocess.run([driver, *args], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    got = {}
+    for line in r.stdout.splitlines():
+        f = line.split()
+        got[(int(f[0]), int(f[1]), int(f[2]))] = (int(f[4]), int(f[5]), int(f[7]), int(f[8]),
+                                                   int(f[10]), int(f[11]))
+    for shape, want in EXPECT.items():
+        assert got[shape] == want, (shape, got[shape], want)
+
+
+def test_schedule_kinds_cover_the_planner_outcomes():
+    """Every outcome above has a name in the binding's schedule kinds."""
+    assert set(rtm.F32_KINDS.values()) >= {"tiles", "tiles+cluster-split", "tiles+workspace-split",
+                                            "column-strips", "tiles+tail-cluster-split"}
