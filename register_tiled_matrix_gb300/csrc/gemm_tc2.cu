@@ -541,29 +541,13 @@ cudaError_t launch_gemm_tc_pair_split(const TcLaunch &L, int splits, cudaStream_
             max_clusters[fi][dev].store(clusters_max);
     }
     const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
-    // splits == 0: choose. A tile split in two adds each K half into a zeroed
-    // C with TMA reduce-adds; 0 + a + b is the same in either order, so the
-    // result still repeats exactly. Split when both halves keep at least 32
-    // K-blocks and either
-    //  * all tiles fill at most half the pairs (256 x 8192 x 8192: 45.1 ->
-    //    37.2 us), or
-    //  * the last round of the persistent loop is at most half full: its
-    //    tiles become two half-length units each (8192^3: 13 rounds of 76
-    //    tiles, then 36 tiles on 72 pairs for half a round), only those tiles
-    //    zeroed first.
+    // splits == 0: choose (pair_split_from, tc_plan.cu); 1: no split; 2: every tile.
     const int kblocks = (L.K + BK - 1) / BK;
     if (splits < 0 || splits > 2)
         return cudaErrorInvalidValue;
-    long long split_from = ntiles;
-    if (splits == 2) {
-        split_from = 0;
-    } else if (splits == 0 && c_vec && kblocks >= 64) {
-        const long long tail = ntiles % clusters_max;
-        if (2 * ntiles <= clusters_max)
-            split_from = 0;
-        else if (ntiles > clusters_max && tail > 0 && 2 * tail <= clusters_max)
-            split_from = ntiles - tail;
-    }
+    const long long split_from = splits == 2   ? 0
+                                 : splits == 1 ? ntiles
+                                               : pair_split_from(ntiles, clusters_max, kblocks, c_vec);
     if (split_from < ntiles && (!c_vec || kblocks < 2))
         return cudaErrorInvalidValue;
     const long long nunits = split_from + 2 * (ntiles - split_from);

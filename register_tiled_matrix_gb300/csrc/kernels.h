@@ -173,6 +173,9 @@ cudaError_t launch_gemm_tc_pair(const TcLaunch &p, cudaStream_t stream);
 // splits 1 or 2 (2: C zero-filled, then each K half reduce-added; C rows must be
 // 16-byte aligned); 0 lets the launcher choose (launch_gemm_tc_pair).
 cudaError_t launch_gemm_tc_pair_split(const TcLaunch &p, int splits, cudaStream_t stream);
+// The first of `ntiles` pair tiles whose K is split in two when `pairs` CTA
+// pairs are resident and K has `kblocks` 64-deep blocks (ntiles: none). tc_plan.cu.
+long long pair_split_from(long long ntiles, int pairs, int kblocks, bool c_vec);
 
 // Copy a rows x cols matrix of 2-byte values (row-major, rows packed, `src`
 // 2-byte aligned) to `dst` with rows `ld` values apart (ld >= cols, ld % 8 ==

@@ -24,7 +24,7 @@ LIB = os.path.join(HERE, "libgemm_gb300.so")
 PTXAS_LOG = os.path.join(BUILD, "ptxas.log")
 
 SOURCES = ["api.cu", "sgemm_simt.cu", "sgemm_ladder.cu", "gemm_tc.cu", "gemm_tc2.cu",
-           "gemm_tc_any.cu", "noalloc.cu", "pack.cu", "sgemm_plan.cu",
+           "gemm_tc_any.cu", "noalloc.cu", "pack.cu", "sgemm_plan.cu", "tc_plan.cu",
            "gemm_tc_t.cu", "sgemm_short.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -1,15 +1,25 @@
 // Test driver (host code only): prints the fp32 schedule planners' choices for
 // the shapes given on the command line as M,N,K triples, for a 152-SM GPU whose
 // cluster-split CTAs fit 76 clusters of 2, 36 of 4 and 15 of 8 at one CTA per
-// SM (the occupancy the library queries on GB300). Built and run by
+// SM (the occupancy the library queries on GB300); with "pair" first, the
+// CTA-pair kernel's K-split choice instead. Built and run by
 // tests/test_plan_host.py; no GPU is needed.
 #include <cstdio>
 #include <cstdlib>
+#include <string>
 
 #include "kernels.h"
 
 int main(int argc, char **argv)
 {
+    if (argc > 1 && std::string(argv[1]) == "pair") {
+        // pair ntiles pairs kblocks c_vec ...: the CTA-pair kernel's first split tile
+        for (int i = 2; i + 3 < argc; i += 4)
+            std::printf("%s %s %s %s split_from %lld\n", argv[i], argv[i + 1], argv[i + 2], argv[i + 3],
+                        rtm::pair_split_from(std::atoll(argv[i]), std::atoi(argv[i + 1]),
+                                             std::atoi(argv[i + 2]), std::atoi(argv[i + 3]) != 0));
+        return 0;
+    }
     const int sms = 152;
     const int resident[3] = {76, 36, 15};
     for (int i = 1; i + 2 < argc; i += 3) {

@@ -1,9 +1,10 @@
-"""CPU tests of the fp32 schedule planners (host code in sgemm_plan.cu): a
-driver built from tests/plan_driver.cu prints each planner's choice for a
-152-SM GB300, and the choices the GB300 sweeps justified are checked here:
-which products split K over clusters and into how many CTAs, when the
-workspace split is priced below the cluster split, and when the ragged last
-wave of a larger product is split."""
+"""CPU tests of the schedule planners (host code in sgemm_plan.cu and
+tc_plan.cu): a driver built from tests/plan_driver.cu prints each planner's
+choice for a 152-SM GB300, and the choices the GB300 sweeps justified are
+checked here: which fp32 products split K over clusters and into how many
+CTAs, when the workspace split is priced below the cluster split, when the
+ragged last wave of a larger product is split, and which tiles of the bf16
+CTA-pair kernel split K in two."""
 
 import os
 import shutil
@@ -43,7 +44,7 @@ def driver(tmp_path_factory):
     out = str(tmp_path_factory.mktemp("plan") / "plan_driver")
     cmd = [nvcc, "-std=c++17", "-O2", "-I", CSRC, "-I", os.path.join(ROOT, "include"),
            os.path.join(ROOT, "tests", "plan_driver.cu"), os.path.join(CSRC, "sgemm_plan.cu"),
-           "-o", out]
+           os.path.join(CSRC, "tc_plan.cu"), "-o", out]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-3000:]
     return out
@@ -60,6 +61,29 @@ def test_planner_choices(driver):
                                                    int(f[10]), int(f[11]))
     for shape, want in EXPECT.items():
         assert got[shape] == want, (shape, got[shape], want)
+
+
+# CTA-pair kernel (bf16/fp16, M > 128): (tiles, resident pairs, 64-deep K blocks,
+# C rows on 16-byte boundaries) -> first tile whose K is split in two.
+PAIR_EXPECT = {
+    (1024, 76, 128, 1): 988,   # 8192^3: 13 rounds + 36 tiles split for half a round
+    (256, 76, 64, 1): 228,     # 4096^3: 3 rounds + 28 tiles
+    (576, 76, 64, 1): 576,     # 6144^2 x 4096: last round 44 tiles, more than half full
+    (128, 76, 128, 1): 128,    # 1024 x 8192^2: last round 52 tiles
+    (32, 76, 128, 1): 0,       # 256 x 8192^2: every tile split
+    (38, 76, 64, 1): 0,        # exactly half the pairs
+    (39, 76, 64, 1): 39,       # more than half, one round: unsplit
+    (32, 76, 32, 1): 32,       # K = 2048: halves too short
+    (1024, 76, 128, 0): 1024,  # C rows not 16-byte aligned: no reduce-add epilogue
+}
+
+
+def test_pair_split_choices(driver):
+    args = ["pair"] + [str(x) for key in PAIR_EXPECT for x in key]
+    r = subprocess.run([driver, *args], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    got = {tuple(int(x) for x in l.split()[:4]): int(l.split()[-1]) for l in r.stdout.splitlines()}
+    assert got == PAIR_EXPECT
 
 
 def test_schedule_kinds_cover_the_planner_outcomes():
