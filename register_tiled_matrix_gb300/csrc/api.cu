@@ -13,6 +13,7 @@
 
 #include "gemm.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -34,8 +35,12 @@ DeviceInfo g_dev[kMaxDevices];
 void *g_encode_tiled = nullptr;
 bool g_encode_tried = false;
 
+// Both zero fills let a dependent kernel launched with programmatic stream
+// serialization start at once (the CTA-pair kernel waits for the zeros only
+// before its reduce-adds).
 __global__ void zero_fill_kernel(float *C, int64_t count)
 {
+    rtm::grid_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride)
         C[i] = 0.0f;
@@ -43,6 +48,7 @@ __global__ void zero_fill_kernel(float *C, int64_t count)
 
 __global__ void zero_fill4_kernel(float4 *C, int64_t count4)
 {
+    rtm::grid_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count4; i += stride)
         C[i] = make_float4(0.f, 0.f, 0.f, 0.f);

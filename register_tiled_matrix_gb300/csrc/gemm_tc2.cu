@@ -401,6 +401,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
+                        if (split)
+                            grid_dependency_wait();  // C zeroed by the preceding fill
                         for (int b = 0; b < (second ? 2 : 1); ++b) {
                             const uint32_t src = smem_u32(boxes + b * EPI_BOX_BYTES);
                             const int col = n0 + (c + b) * 32;
@@ -438,6 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // on 16-byte boundaries, N % 4 == 0, so every clipped row is whole float4s).
 __global__ void zero_tiles_kernel(float *C, int M, int N, int first)
 {
+    grid_launch_dependents();  // the pair kernel waits for these zeros only before adding
     int m0, n0;
     tile_coords(first + (int)blockIdx.x, (M + PM - 1) / PM, (N + PN - 1) / PN, m0, n0);
     const int rows = min(PM, M - m0), quads = min(PN, N - n0) / 4;
@@ -563,8 +566,21 @@ cudaError_t launch_gemm_tc_pair_split(const TcLaunch &L, int splits, cudaStream_
         return e;
     Params p{L.M, L.N, L.K, L.C, L.err, (unsigned long long)L.wait_limit_ns, L.mute_producer,
              (int)split_from};
-    kernel<<<2 * clusters, kThreads, smem_bytes, stream>>>(ta, tb, tc, p);
-    return cudaGetLastError();
+    // After a zero fill the kernel is a programmatic dependent of it: its main
+    // loop reads only A and B, and each split unit waits for the fill (and its
+    // memory) before its first reduce-add, so the fill and its launch overlap
+    // the main loop.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = split_from < ntiles ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
 }
 
 } // namespace rtm

@@ -264,6 +264,21 @@ __device__ __forceinline__ void tmem_wait_ld()
 }
 
 // ---------------------------------------------------------------- clusters
+// Programmatic dependent launch. launch_dependents: kernels launched after this
+// one with programmatic stream serialization may start once every CTA of this
+// grid has executed it (or exited). wait: block until the grids this one
+// depends on have completed and their memory operations are visible (a no-op
+// for a kernel launched without that attribute).
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Special registers read with a volatile move: the compiler cannot reuse an
 // earlier read, so the value need not stay live in a register until then.
 __device__ __forceinline__ uint32_t special_tid_x()

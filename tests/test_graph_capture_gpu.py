@@ -39,6 +39,8 @@ CASES = {
                             lambda A, B, C, W: rtm.gemm_f32_ws(A, B, out=C, workspace=W)),
     "gemm_bf16f32 CTA pairs": ("bf16", 512, 512, 256,
                                lambda A, B, C, W: rtm.gemm_bf16f32(A, B, out=C)),
+    "gemm_bf16f32 CTA pairs, K split": ("bf16", 256, 1024, 4096,
+                                        lambda A, B, C, W: rtm.gemm_bf16f32(A, B, out=C)),
     "gemm_bf16f32 single CTA": ("bf16", 96, 2048, 512,
                                 lambda A, B, C, W: rtm.gemm_bf16f32(A, B, out=C)),
     "gemm_bf16f32_ws re-pitched": ("bf16", 300, 129, 77,
