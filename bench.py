@@ -58,8 +58,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     "gemm_f32": {"bytes": 384730880, "source_sha1": "42150b9fe7160333adf77e7d147a49e0ad114abf",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
-    "gemm_bf16f32": {"bytes": 1345978880,
-                     "source_sha1": "61d197c4a7f7d37734a3f0c27005e5ab6537554e",
+    "gemm_bf16f32": {"bytes": 1365153024,
+                     "source_sha1": "2564a8cd5cb12f0cd75e69661170f865254c938a",
                      "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
 }
 KERNEL_SOURCE = {
