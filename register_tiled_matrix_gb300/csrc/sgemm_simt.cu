@@ -170,8 +170,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
         K = min(kchunk, K_total - k_begin);
         A += k_begin;
         B += (size_t)k_begin * N;
-        if constexpr (SPLIT == kSplitWorkspace)
+        if constexpr (SPLIT == kSplitWorkspace) {
             C += blockIdx.y * aux;
+            grid_launch_dependents();  // the reduction may launch; it waits for this grid
+        }
     }
 
     using G = Cfg<BM, BN, BK, STAGES>;
@@ -530,6 +532,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restr
                                      int64_t count, int splits)
 {
     // C[i] = W[0][i] + W[1][i] + ... in increasing split order (deterministic).
+    grid_dependency_wait();  // launched as a programmatic dependent of the split kernel
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
         float s = W[i];
@@ -542,6 +545,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restr
 __global__ void splitk_reduce4_kernel(const float4 *__restrict__ W, float4 *__restrict__ C,
                                       int64_t count4, int splits)
 {
+    grid_dependency_wait();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count4; i += stride) {
         float4 s = W[i];
@@ -596,14 +600,23 @@ cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const f
     int64_t blocks = (items + 255) / 256;
     if (blocks > 4096)
         blocks = 4096;
+    // A programmatic dependent of the split kernel: launched while the partial
+    // products are still being computed, it waits for them in the kernel.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (vec)
-        splitk_reduce4_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-            reinterpret_cast<const float4 *>(workspace), reinterpret_cast<float4 *>(C),
-            count / 4, plan.splits);
-    else
-        splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(workspace, C, count,
-                                                                  plan.splits);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, splitk_reduce4_kernel,
+                                  reinterpret_cast<const float4 *>(workspace),
+                                  reinterpret_cast<float4 *>(C), count / 4, plan.splits);
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, (const float *)workspace, C, count,
+                              plan.splits);
 }
 
 int sgemm_cluster_resident_spread(int cluster_size)
