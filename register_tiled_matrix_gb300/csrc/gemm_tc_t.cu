@@ -30,11 +30,11 @@
 //    barrier keeps every partial alive until all have been read.
 //
 // The same kernel without the swap (SWAP = false) serves tall, narrow
-// products (many rows of A, N <= 256): A fills the MMA's 128-row side
-// (K-major), B the N side (MN = 64 or 128 columns, MN-major; 256 columns
-// are two tiles, which measured the same as one 256-wide tile with half the
-// stages), TMEM lane i is row m0 + i of C, and K is split over a cluster the
-// same way.
+// products (many rows of A, N <= 128; wider ones up to 256 columns ran faster
+// on the CTA-pair kernel): A fills the MMA's 128-row side (K-major), B the N
+// side (MN = 64 or 128 columns, MN-major; 256 columns as two tiles measured
+// the same as one 256-wide tile with half the stages), TMEM lane i is row
+// m0 + i of C, and K is split over a cluster the same way.
 //
 // Every mbarrier wait is bounded in time; a warp that gives up records
 // GEMM_ERR_TIMEOUT in the device error word and every thread still reaches

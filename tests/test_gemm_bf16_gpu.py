@@ -267,15 +267,20 @@ def test_transposed_bounded_wait_gives_up_and_context_survives():
     assert_close_to_oracle(run(A, B), A, B, "bf16", full=False, seed=52)
 
 
-# M > 128, N <= 256, K >= 2048: A on the MMA's 128-row side, B (64, 128 or 256
+# M > 128, N <= 128, K >= 2048: A on the MMA's 128-row side, B (64 or 128
 # columns) on its N side, K split over S CTAs of a cluster (S for 152 SMs).
+# 128 < N <= 256 runs on the CTA pairs (K split in two where the tiles leave
+# pairs idle); those shapes stay here as the neighbouring case.
 @pytest.mark.parametrize("M,N,K", [(8192, 64, 4096),    # S = 2
                                    (4096, 100, 8192),   # S = 4, ragged N, scalar C rows
-                                   (2000, 256, 2048),   # S = 2, 256 columns
+                                   (2000, 128, 2048),   # S = 2, 128 columns
                                    (300, 8, 4096),      # S = 4
-                                   (19456, 200, 2048),  # S = 1, 152 tiles
-                                   (1000, 136, 8200),   # S = 8, ragged K
-                                   (2048, 64, 8192)])   # 16 tiles: S = 8 only if they all fit
+                                   (19456, 120, 2048),  # S = 1, 152 tiles
+                                   (1000, 104, 8200),   # S = 8, ragged K
+                                   (2048, 64, 8192),    # 16 tiles: S = 8 only if they all fit
+                                   (2000, 256, 2048),   # CTA pairs, 256 columns
+                                   (19456, 200, 2048),  # CTA pairs, ragged N
+                                   (1000, 136, 8200)])  # CTA pairs, K split in two, ragged K
 def test_tall_narrow(M, N, K):
     A, B = bf16_inputs(M, N, K, seed=M + 5 * N + K)
     full = M * N * K <= (1 << 31)
