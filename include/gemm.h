@@ -124,10 +124,16 @@ typedef enum gemm_f32_kind {
     GEMM_F32_TILES_WORKSPACE = 3,  /* the same, K split through a workspace + reduction */
     GEMM_F32_COLUMN_STRIPS = 4,    /* M <= 32: column strips (K split over a cluster
                                       when splits > 1) */
-    GEMM_F32_TILES_TAIL_CLUSTER = 5 /* more tiles than SMs: whole waves of tiles
+    GEMM_F32_TILES_TAIL_CLUSTER = 5, /* more tiles than SMs: whole waves of tiles
                                       unsplit, then the ragged last wave with K split
                                       over the CTAs of a cluster (splits = cluster
                                       size) */
+    GEMM_F32_TALL_TILES = 6,       /* N <= 64, M > 128: 256 x 64 C tiles (16 x 4 per
+                                      thread), one CTA per tile */
+    GEMM_F32_TALL_TILES_CLUSTER = 7 /* the same, K split over the CTAs of a cluster.
+                                      Both tall kinds fall back to 128 x 64 tiles,
+                                      same split, when the rows of B are not on
+                                      16-byte boundaries */
 } gemm_f32_kind;
 GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace,
                                int *kind, int *splits);

@@ -30,11 +30,14 @@ cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> 
 
 // Tiles of the SIMT FP32 product: 128 x 128 C tiles, with 64 columns for
 // N <= 64 and 64 rows for M <= 64 (where 128 would be at least half empty),
-// 32-deep K slices.
+// 32-deep K slices. Tall, narrow products (N <= 64, M > 128) may take 256 x 64
+// tiles instead (16 x 4 outputs per thread: fewer shared reads per FMA than
+// the 8 x 4 of a 128 x 64 tile) where the schedule model prices them lower.
 namespace simt_tiles {
 constexpr int kTileM = 128, kTileN = 128, kSliceK = 32;
 constexpr int kNarrowN = 64;
 constexpr int kShortTileM = 64;
+constexpr int kTallTileM = 256;
 } // namespace simt_tiles
 
 // How many clusters of `cluster_size` CTAs of `kernel` (`threads` threads,
@@ -75,9 +78,10 @@ int resident_clusters(Kernel kernel, int cluster_size, int threads, size_t smem,
 }
 
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
-// 4-byte-aligned pointers. 1 <= K; M, N >= 1.
+// 4-byte-aligned pointers. 1 <= K; M, N >= 1. `tall`: 256 x 64 tiles where
+// N <= 64 (taken only when the rows of B lie on 16-byte boundaries).
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool tall = false);
 
 // SIMT FP32 product for short, wide shapes (sgemm_short.cu): M <= kShortMaxM,
 // any N and K >= 1, 4-byte-aligned pointers. Each thread keeps one column of
@@ -96,6 +100,7 @@ struct SplitK {
     int splits;  // 1: no split (plain product)
     int kchunk;
     bool spread = false;  // cluster split: one CTA per SM (see sgemm_cluster_plan)
+    bool tall = false;    // 256 x 64 tiles (N <= 64; set by sgemm_cluster_plan only)
 };
 SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count);  // sgemm_plan.cu
 // The plan's run time in the slice-time units of sgemm_cluster_plan's
@@ -107,6 +112,8 @@ cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const f
 // Split-K without a workspace: the plan.splits (2, 4 or 8) CTAs that share a C
 // tile form one cluster and add their partial tiles through distributed shared
 // memory in rank order (deterministic). plan.splits == 1 is the plain product.
+// plan.tall: the product (split or not) runs on 256 x 64 tiles. *est: the
+// chosen schedule's estimate (also for an unsplit product).
 // resident_spread[i]: clusters of 2 << i CTAs that fit at once with one CTA
 // per SM (sgemm_cluster_resident_spread; 0 if unknown).
 SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&resident_spread)[3],

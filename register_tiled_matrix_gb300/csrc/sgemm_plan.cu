@@ -65,14 +65,22 @@ struct ShapeCost {
     double slice_time;
 };
 
-ShapeCost shape_cost(int M, int N, int K)
+// `tall`: 256 x 64 tiles. A slice of one takes 1.35 slice-times, fitted to
+// tall, narrow products on GB300 (8192 x 64 x 4096 to 16384 x 64 x 8192, K
+// split 1 to 8 ways): the same area as a 128 x 128 tile, but with 16 x 4
+// outputs per thread its loop reads shared memory 5 times per 64 FMA
+// against 4. A 128 x 64 tile's slice (8 x 4 per thread, 6 reads per 64 FMA)
+// takes 0.8 for half the area.
+ShapeCost shape_cost(int M, int N, int K, bool tall = false)
 {
     const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
-    const int tile_m = M <= kShortTileM ? kShortTileM : kTileM;
+    const int tile_m = tall ? kTallTileM : M <= kShortTileM ? kShortTileM : kTileM;
     ShapeCost c;
     c.tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
     c.kslices = (K + kSliceK - 1) / kSliceK;
-    c.slice_time = (tile_n == kNarrowN || tile_m == kShortTileM) ? 0.8 : 1.0;  // half-area tiles
+    c.slice_time = tall ? 1.35
+                   : (tile_n == kNarrowN || tile_m == kShortTileM) ? 0.8  // half-area tiles
+                                                                   : 1.0;
     return c;
 }
 
@@ -107,16 +115,20 @@ double sgemm_workspace_estimate(int M, int N, int K, int sm_count, const SplitK 
 // CTA can have an SM of its own the plan asks for one CTA per SM (`spread`),
 // provided all the clusters fit at once that way; otherwise it prices the
 // split as packed two to an SM.
-SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&resident_spread)[3],
-                          double *est_out)
+namespace {
+
+// The cluster plan for one tile shape; *est_out: its estimate (the plain
+// product's when not split, priced as waves of CTAs two to an SM where there
+// are more tiles than SMs).
+SplitK cluster_plan_for(const ShapeCost &c, int K, int sm_count, const int (&resident_spread)[3],
+                        double *est_out)
 {
     SplitK p{1, K};
-    if (est_out)
-        *est_out = 1e300;
-    const ShapeCost c = shape_cost(M, N, K);
-    if (sm_count <= 0 || c.tiles > sm_count)
+    const bool few = c.tiles <= sm_count;
+    const double plain = waves_time(c, c.tiles, c.kslices, sm_count, few, 0.0);
+    *est_out = plain;
+    if (!few)
         return p;
-    const double plain = waves_time(c, c.tiles, c.kslices, sm_count, true, 0.0);
     double best = plain;
     for (int i = 0, s = 2; s <= 8; ++i, s *= 2) {
         const long long chunk = (c.kslices + s - 1) / s;
@@ -134,8 +146,37 @@ SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&residen
     }
     if (p.splits > 1 && best > 0.97 * plain)
         p = SplitK{1, K};
+    *est_out = p.splits > 1 ? best : plain;
+    return p;
+}
+
+} // namespace
+
+SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&resident_spread)[3],
+                          double *est_out)
+{
     if (est_out)
-        *est_out = p.splits > 1 ? best : plain;
+        *est_out = 1e300;
+    if (sm_count <= 0)
+        return SplitK{1, K};
+    double est = 0;
+    SplitK p = cluster_plan_for(shape_cost(M, N, K), K, sm_count, resident_spread, &est);
+    if (N <= kNarrowN && M > kTileM && K > 3 * kSliceK) {
+        // Tall, narrow: 256 x 64 tiles, split or not, where they price lower.
+        // Unsplit on GB300: 65536 x 64 x 256 59.5 -> 53.4 us, 65536 x 64 x 2048
+        // 441.8 -> 389.9 us, 131072 x 64 x 1024 the same; with K of one or
+        // two slices the longer CTAs lost (131072 x 16 x 64 30.9 -> 33.0 us).
+        double est_tall = 0;
+        SplitK t = cluster_plan_for(shape_cost(M, N, K, true), K, sm_count, resident_spread,
+                                    &est_tall);
+        if (est_tall < est) {
+            t.tall = true;
+            p = t;
+            est = est_tall;
+        }
+    }
+    if (est_out)
+        *est_out = est;
     return p;
 }
 

@@ -78,7 +78,6 @@ struct Cfg {
                   "A loader: warp w covers rows w*BM/8 .. +BM/8, 4 rows x 8 k per copy");
     static_assert(BK * BN % (4 * kThreads) == 0, "B loader coverage");
     static constexpr int FAST_COPIES = A_PER_THREAD + B4_PER_THREAD;
-    static constexpr int COPIES_PER_K = (FAST_COPIES + BK - 1) / BK;  // spread over the k loop
     // kSplitCluster: the partial tile parked in shared memory after the k loop,
     // rows padded by 4 floats (a quarter-warp's 128-bit stores, 2 rows 4 apart
     // x 64 bytes, then fall in distinct banks).
@@ -240,7 +239,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // B elements (4-byte path, rows of B not on 16-byte boundaries).
     constexpr int FAST_COPIES =
         B_VEC ? G::FAST_COPIES : G::A_PER_THREAD + G::B1_PER_THREAD;
-    constexpr int COPIES_PER_K = (FAST_COPIES + BK - 1) / BK;  // spread over the k loop
+    // The copies are spread over the first 5/8 of the k loop, so that the
+    // last of them still has a few k-steps to land before the wait at the top
+    // of the next iteration: one per k for the 20 copies of the 16-byte path,
+    // two per k for the 32 of the 4-byte path (one per k there left the last
+    // copy issued just before that wait; 2 % slower at 4096 x 4093 x 4096 on
+    // GB300). The cluster-split 4-byte variant keeps one per k: two cost it a
+    // 16-byte register spill.
+    constexpr int COPY_SPAN = (SPLIT == kSplitCluster && !B_VEC) ? BK : BK * 5 / 8;
+    constexpr int COPIES_PER_K = (FAST_COPIES + COPY_SPAN - 1) / COPY_SPAN;
     auto fast_copy = [&](int c, uint32_t stage, int kt) {
         const int k0 = kt * BK;
         if (c < G::A_PER_THREAD) {
@@ -561,9 +568,35 @@ __global__ void splitk_reduce4_kernel(const float4 *__restrict__ W, float4 *__re
 }
 } // namespace
 
-cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream)
+namespace {
+
+// 256 x 64 tiles for tall, narrow products. Only the 16-byte B path is built
+// for them (its 4-byte variant spilled registers under the 128-register
+// budget); rows of B off 16-byte boundaries take 128 x 64 tiles with the same
+// split, packed two CTAs to an SM.
+template <int SPLIT>
+cudaError_t launch_tall(int M, int N, int K, const float *A, const float *B, float *C,
+                        cudaStream_t stream, int splits = 1, int kchunk = 0, bool spread = false)
 {
+    const bool b_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(B) & 15) == 0);
+    const bool c_vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
+    if (!b_vec)
+        return simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, SPLIT>(M, N, K, A, B, C, stream,
+                                                                         splits, kchunk, false);
+    if (c_vec)
+        return simt::launch_cfg<kTallTileM, kNarrowN, kSliceK, 2, 2, 1, true, true, SPLIT>(
+            M, N, K, A, B, C, stream, splits, kchunk, spread);
+    return simt::launch_cfg<kTallTileM, kNarrowN, kSliceK, 2, 2, 1, true, false, SPLIT>(
+        M, N, K, A, B, C, stream, splits, kchunk, spread);
+}
+
+} // namespace
+
+cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
+                             cudaStream_t stream, bool tall)
+{
+    if (tall && N <= kNarrowN)
+        return launch_tall<simt::kPlain>(M, N, K, A, B, C, stream);
     if (M <= kShortTileM) {  // 64-row tiles: 128-row tiles would be at least half empty
         if (N <= kNarrowN)
             return simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
@@ -640,8 +673,10 @@ int sgemm_cluster_resident_spread(int cluster_size)
 
 SplitK sgemm_cluster_schedule(int M, int N, int K, int sm_count, double *est)
 {
+    // The fewest tiles any candidate tile shape gives (256 x 64 for tall,
+    // narrow products).
     const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
-    const int tile_m = M <= kShortTileM ? kShortTileM : kTileM;
+    const int tile_m = M <= kShortTileM ? kShortTileM : N <= kNarrowN ? kTallTileM : kTileM;
     const long long tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
     int resident[3] = {0, 0, 0};
     if (tiles <= sm_count)  // only then is a split considered
@@ -666,6 +701,9 @@ cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const 
                                      const SplitK &plan, cudaStream_t stream)
 {
     using simt::kSplitCluster;
+    if (plan.tall && N <= kNarrowN)
+        return launch_tall<kSplitCluster>(M, N, K, A, B, C, stream, plan.splits, plan.kchunk,
+                                          plan.spread);
     if (M <= kShortTileM)
         return N <= kNarrowN
                    ? simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitCluster>(
@@ -703,7 +741,7 @@ cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const fl
     const TailPlan tail = sgemm_tail_plan(M, N, K, sm_count);
     if (tail.tail.splits > 1)
         return launch_sgemm_f32_tail(M, N, K, A, B, C, tail, stream);
-    return launch_sgemm_f32(M, N, K, A, B, C, stream);
+    return launch_sgemm_f32(M, N, K, A, B, C, stream, cluster.tall);
 }
 
 } // namespace rtm

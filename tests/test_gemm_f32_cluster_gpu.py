@@ -34,8 +34,7 @@ SHAPES = [
     (256, 256, 256),     # 8 per cluster spread one CTA per SM, one slice per chunk
     (300, 200, 1024),    # 8 per cluster spread, ragged tiles
     (129, 65, 999),      # 8 per cluster spread, one spare row and column tile
-    (2000, 60, 2000),    # 128 x 64 tiles, 8 per cluster, two CTAs per SM
-    (8192, 64, 4096),    # 128 x 64 tiles, 4 per cluster
+    (4096, 64, 4096),    # 128 x 64 tiles, 8 per cluster, two CTAs per SM
     (60, 3000, 2000),    # 64 x 128 tiles, 8 per cluster
     (64, 8, 4096),       # 64 x 64 tiles, 8 per cluster spread
     (48, 64, 1000),      # 64 x 64 tiles, 8 per cluster spread, partial last chunk
@@ -53,6 +52,57 @@ def test_cluster_split_parity(M, N, K):
     C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
     torch.cuda.synchronize()
     assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+# Tall, narrow products (N <= 64) on 256 x 64 tiles, 16 x 4 outputs per
+# thread, K split over a cluster or not at all.
+TALL_SHAPES = [
+    (8192, 64, 4096, 8),    # 32 tiles, 8 per cluster, two CTAs per SM
+    (2000, 60, 2000, 8),    # 8 tiles, 8 per cluster spread one CTA per SM, ragged M and N
+    (2049, 64, 1000, 8),    # one spare row: a 256-row tile with a single live row
+    (16384, 64, 2048, 4),   # 64 tiles, 4 per cluster
+    (8192, 61, 4096, 8),    # rows of B off 16-byte boundaries: 128 x 64 tiles, same split
+    (3000, 33, 1500, 8),    # ragged in M, N and K
+    (32768, 64, 512, 1),    # 128 tiles unsplit
+    (20000, 64, 300, 1),    # more tiles than SMs, ragged M and K
+]
+
+
+@pytest.mark.parametrize("M,N,K,splits", TALL_SHAPES)
+def test_tall_tiles_parity(M, N, K, splits):
+    kind, s = rtm.gemm_f32_schedule(M, N, K)
+    want = "tall-tiles+cluster-split" if splits > 1 else "tall-tiles"
+    assert (kind, s) == (want, splits), (kind, s)
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M * 13 + N * 5 + K)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+@pytest.mark.parametrize("M,N,K", [(2000, 60, 2000), (8192, 64, 1024), (20000, 64, 300)])
+def test_tall_tiles_small_integer_guard_band_repeatability(M, N, K):
+    A, B = small_int_inputs(M, N, K, seed=M + 7 * K)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf, C = guarded_output(M, N, DEV)
+    rtm.gemm_f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N), "a store landed outside C"
+    assert torch.equal(C, C2)
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
+def test_tall_tiles_unaligned_output():
+    # C starts 4 bytes past a 16-byte boundary: 4-byte stores on the 256-row tiles.
+    M, N, K = 8192, 64, 1024
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=6)
+    buf = torch.full((M * N + 4,), float("nan"), device=DEV)
+    C = buf[1:1 + M * N].view(M, N)
+    rtm.gemm_f32(A.to(DEV), B.to(DEV), out=C)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[0]) and torch.isnan(buf[1 + M * N:]).all()
     assert_close_to_oracle(C, A, B, "f32")
 
 

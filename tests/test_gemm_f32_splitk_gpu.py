@@ -27,9 +27,10 @@ def run_ws(A, B):
 
 # Workspace only where the schedule prices the workspace split below the split
 # over cluster CTAs (which needs none): long K over few tiles. 1024^3,
-# 1000 x 1000 x 999 and 256^3 split over clusters; 4096^3 and 4097 x 3001 x
-# 1023 fill the GPU unsplit.
-@pytest.mark.parametrize("M,N,K,split", [(8192, 64, 4096, True), (512, 512, 8192, True),
+# 1000 x 1000 x 999, 256^3 and 8192 x 64 x 4096 (on 256 x 64 tiles) split over
+# clusters; 4096^3 and 4097 x 3001 x 1023 fill the GPU unsplit.
+@pytest.mark.parametrize("M,N,K,split", [(2000, 60, 2000, True), (512, 512, 8192, True),
+                                         (8192, 64, 4096, False),
                                          (2048, 128, 4096, True), (1024, 1024, 1024, False),
                                          (1000, 1000, 999, False), (256, 256, 256, False),
                                          (4096, 4096, 4096, False), (4097, 3001, 1023, False)])

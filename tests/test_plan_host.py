@@ -3,8 +3,9 @@ tc_plan.cu): a driver built from tests/plan_driver.cu prints each planner's
 choice for a 152-SM GB300, and the choices the GB300 sweeps justified are
 checked here: which fp32 products split K over clusters and into how many
 CTAs, when the workspace split is priced below the cluster split, when the
-ragged last wave of a larger product is split, and which tiles of the bf16
-CTA-pair kernel split K in two."""
+ragged last wave of a larger product is split, which tall, narrow products
+take 256 x 64 tiles, and which tiles of the bf16 CTA-pair kernel split K in
+two."""
 
 import os
 import shutil
@@ -18,21 +19,32 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "register_tiled_matrix_gb300", "csrc")
 
 # (M, N, K): (cluster splits, spread, workspace splits, workspace priced lower,
-#             unsplit tiles before the tail, tail splits)
+#             unsplit tiles before the tail, tail splits, 256 x 64 tiles)
 EXPECT = {
-    (256, 256, 256): (8, 1, 8, 0, 0, 1),        # 4 tiles: 8 per cluster, one CTA per SM
-    (1024, 1024, 1024): (4, 0, 2, 0, 0, 1),     # 52.8 us split 4, 55.4 with the workspace
-    (1000, 1000, 999): (4, 0, 2, 0, 0, 1),
-    (300, 260, 129): (2, 0, 5, 1, 0, 1),
-    (512, 512, 8192): (8, 0, 9, 1, 0, 1),       # long K over 16 tiles: the workspace wins
-    (8192, 64, 4096): (4, 0, 7, 1, 0, 1),       # 128 x 64 tiles
-    (64, 8192, 8192): (4, 0, 7, 1, 0, 1),       # 64-row tiles
-    (2048, 1024, 1024): (1, 0, 1, 0, 0, 1),     # 128 tiles: split was no faster
-    (4096, 4096, 4096): (1, 0, 1, 0, 0, 1),     # 3 waves + 112 tiles: tail left alone
-    (4097, 3001, 1023): (1, 0, 1, 0, 608, 4),   # 608 tiles + a 184-tile tail split
-    (2304, 2304, 4096): (1, 0, 1, 0, 304, 4),   # one wave + 20 tiles
-    (2048, 1536, 1024): (1, 0, 1, 0, 0, 4),     # 192 tiles, under two waves
-    (2048, 2304, 512): (1, 0, 1, 0, 0, 1),      # 4-slice chunks, 95 % of the slots
+    (256, 256, 256): (8, 1, 8, 0, 0, 1, 0),        # 4 tiles: 8 per cluster, one CTA per SM
+    (1024, 1024, 1024): (4, 0, 2, 0, 0, 1, 0),     # 52.8 us split 4, 55.4 with the workspace
+    (1000, 1000, 999): (4, 0, 2, 0, 0, 1, 0),
+    (300, 260, 129): (2, 0, 5, 1, 0, 1, 0),
+    (512, 512, 8192): (8, 0, 9, 1, 0, 1, 0),       # long K over 16 tiles: the workspace wins
+    (64, 8192, 8192): (4, 0, 7, 1, 0, 1, 0),       # 64-row tiles
+    (2048, 1024, 1024): (1, 0, 1, 0, 0, 1, 0),     # 128 tiles: split was no faster
+    (4096, 4096, 4096): (1, 0, 1, 0, 0, 1, 0),     # 3 waves + 112 tiles: tail left alone
+    (4097, 3001, 1023): (1, 0, 1, 0, 608, 4, 0),   # 608 tiles + a 184-tile tail split
+    (2304, 2304, 4096): (1, 0, 1, 0, 304, 4, 0),   # one wave + 20 tiles
+    (2048, 1536, 1024): (1, 0, 1, 0, 0, 4, 0),     # 192 tiles, under two waves
+    (2048, 2304, 512): (1, 0, 1, 0, 0, 1, 0),      # 4-slice chunks, 95 % of the slots
+    # Tall, narrow (N <= 64): 256 x 64 tiles against 128 x 64, fastest on GB300 in
+    # each row (us): 117.6 for 128 x 64 split 4 against 106.1 here; 230.4 (split 8)
+    # against 196.7; 227.4 against 198.8; 62.7 here against 100.5; 115.0 against
+    # 104.5 with two CTAs to an SM.
+    (8192, 64, 4096): (8, 0, 7, 0, 0, 1, 1),
+    (16384, 64, 4096): (4, 0, 8, 0, 0, 1, 1),
+    (8192, 64, 8192): (8, 0, 7, 0, 0, 1, 1),
+    (4096, 64, 4096): (8, 0, 19, 0, 0, 1, 0),      # 16 tall tiles would pack two to an SM
+    (2048, 64, 8192): (8, 1, 19, 1, 0, 1, 1),
+    (32768, 64, 512): (1, 0, 1, 0, 0, 1, 1),       # 128 tall tiles unsplit
+    (200, 64, 8192): (8, 1, 32, 1, 0, 1, 0),       # M <= 256: one tall tile prices no lower
+    (131072, 16, 64): (1, 0, 1, 0, 0, 1, 0),       # two K slices: 128 x 64 tiles
 }
 
 
@@ -58,7 +70,7 @@ def test_planner_choices(driver):
     for line in r.stdout.splitlines():
         f = line.split()
         got[(int(f[0]), int(f[1]), int(f[2]))] = (int(f[4]), int(f[5]), int(f[7]), int(f[8]),
-                                                   int(f[10]), int(f[11]))
+                                                   int(f[10]), int(f[11]), int(f[13]))
     for shape, want in EXPECT.items():
         assert got[shape] == want, (shape, got[shape], want)
 
@@ -89,4 +101,5 @@ def test_pair_split_choices(driver):
 def test_schedule_kinds_cover_the_planner_outcomes():
     """Every outcome above has a name in the binding's schedule kinds."""
     assert set(rtm.F32_KINDS.values()) >= {"tiles", "tiles+cluster-split", "tiles+workspace-split",
-                                            "column-strips", "tiles+tail-cluster-split"}
+                                            "column-strips", "tiles+tail-cluster-split",
+                                            "tall-tiles", "tall-tiles+cluster-split"}
