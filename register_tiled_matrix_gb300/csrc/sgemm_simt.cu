@@ -233,6 +233,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
     else
         b_dst0 = smem_u32(sB + (tid / (BN / 4)) * BN + (tid % (BN / 4)) * 4);
 
+    // 4-byte B path: this thread's column and first row of every slice.
+    const float *b1_src = B + (size_t)(tid / BN) * N + (n0 + tid % BN);
+    const uint32_t b1_dst0 = smem_u32(sB + (tid / BN) * BN + tid % BN);
+    const float *b1_next = b1_src;
+
     // Unpredicated copies of K-slice kt into `stage` (interior tiles, full
     // slices), one per call so they can be spread over the FMA loop: copies
     // 0 .. A_PER_THREAD-1 are A elements, the rest B vectors (16-byte path) or
@@ -255,12 +260,28 @@ __global__ void __launch_bounds__(kThreads, MINB)
             cp_async_4_full(a_dst0 + stage * A_STAGE_BYTES + (uint32_t)((8 * h * LDA + 4 * j) * 4),
                             a_src + (size_t)(4 * j) * lda + (k0 + 8 * h));
         } else if constexpr (!B_VEC) {
-            // copy i moves B[k0 + i * (256 / BN) + tid / BN][n0 + tid % BN]
+            // copy i moves B[k0 + i * (256 / BN) + tid / BN][n0 + tid % BN]. The
+            // source walks down B from the slice's first row, one pointer bump
+            // per copy: with a separate offset per copy the compiler kept the
+            // 16 offsets live across the loop, and the FFMA loop's register
+            // allocation suffered (4096 x 4093 x 4096 on GB300: 2.655 -> 2.527
+            // ms; the same chain for the A copies slowed 4096^3 by 6 %).
+            // The cluster-split variant keeps the per-copy offsets: with the
+            // chain it spilled 32 bytes.
             const int i = c - G::A_PER_THREAD;
-            const int k = i * (kThreads / BN) + tid / BN;
-            const int n = tid % BN;
-            cp_async_4_full(smem_u32(sB + stage * (BK * BN) + k * BN + n),
-                            B + (size_t)(k0 + k) * N + (n0 + n));
+            if constexpr (SPLIT == kSplitCluster) {
+                const int k = i * (kThreads / BN) + tid / BN;
+                const int n = tid % BN;
+                cp_async_4_full(smem_u32(sB + stage * (BK * BN) + k * BN + n),
+                                B + (size_t)(k0 + k) * N + (n0 + n));
+            } else {
+                if (i == 0)
+                    b1_next = b1_src + (size_t)k0 * N;
+                cp_async_4_full(b1_dst0 + stage * B_STAGE_BYTES +
+                                    (uint32_t)(i * (kThreads / BN) * BN * 4),
+                                b1_next);
+                b1_next += (size_t)(kThreads / BN) * N;
+            }
         } else {
             const int i = c - G::A_PER_THREAD;
             const int krow = i * (kThreads / (BN / 4));

@@ -25,10 +25,12 @@ CHILD = textwrap.dedent(r"""
 
     torch.cuda.init()
     jobs = []
-    for i in range(8):
-        kind = ["f32", "f32_ws", "bf16", "bf16_small", "f16", "bf16_ws", "bf16_any", "f32"][i]
+    for i in range(9):
+        kind = ["f32", "f32_ws", "bf16", "bf16_small", "f16", "bf16_ws", "bf16_any", "f32",
+                "f32"][i]
         M, N, K = [(300, 260, 129), (256, 64, 2048), (384, 264, 200), (96, 1024, 136),
-                   (300, 264, 72), (300, 129, 77), (120, 100, 33), (1000, 1000, 999)][i]
+                   (300, 264, 72), (300, 129, 77), (120, 100, 33), (1000, 1000, 999),
+                   (2000, 60, 2000)][i]
         dt = {"f32": "f32", "f32_ws": "f32", "f16": "f16"}.get(kind, "bf16")
         A, B = workloads.make_inputs(M, N, K, "normal", dt, seed=i + 11)
         jobs.append((kind, A, B))
