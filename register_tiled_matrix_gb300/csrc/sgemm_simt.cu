@@ -9,7 +9,7 @@
 //  * shared tiling — the CTA stages BK-deep K-slices of A and B in shared
 //    memory through a STAGES-deep cp.async ring (zero-filled past M, N, K);
 //    CTAs whose tile lies inside M x N copy full slices without predicates,
-//    one copy per k-step interleaved with the FFMA of the current slice;
+//    interleaved with the FFMA of the current slice over its first 5/8;
 //    A is stored k-major (transposed) so a thread's column of A is one
 //    128-bit load ("理解 Register Tiling", section "用一张图对比三个版本");
 //  * register tiling — each of the 16 x 16 threads keeps a TM x TN fp32
@@ -31,7 +31,8 @@
 //    order (odd rows backwards), so consecutive FFMA always share an operand
 //    and the hardware operand-reuse cache can serve it (measured: +4 % over
 //    row-by-row order on GB300);
-//  * products with N <= 64 use 128 x 64 tiles (8 x 4 per thread);
+//  * products with N <= 64 use 128 x 64 tiles (8 x 4 per thread), or
+//    256 x 64 (16 x 4) where the schedule model prices them lower;
 //  * BK = 32 with two stages (66.6 KB of shared memory per CTA): a sweep of
 //    BK in {8..48} and 2-4 stages on GB300 put this on top (59 TFLOP/s at
 //    4096^3 against 56 for three stages);
