@@ -130,10 +130,13 @@ typedef enum gemm_f32_kind {
                                       size) */
     GEMM_F32_TALL_TILES = 6,       /* N <= 64, M > 128: 256 x 64 C tiles (16 x 4 per
                                       thread), one CTA per tile */
-    GEMM_F32_TALL_TILES_CLUSTER = 7 /* the same, K split over the CTAs of a cluster.
+    GEMM_F32_TALL_TILES_CLUSTER = 7, /* the same, K split over the CTAs of a cluster.
                                       Both tall kinds fall back to 128 x 64 tiles,
                                       same split, when the rows of B are not on
                                       16-byte boundaries */
+    GEMM_F32_WIDE_TILES = 8,       /* 32 < M <= 64, N > 64: 64 x 256 C tiles (4 x 16
+                                      per thread), one CTA per tile */
+    GEMM_F32_WIDE_TILES_CLUSTER = 9 /* the same, K split over the CTAs of a cluster */
 } gemm_f32_kind;
 GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace,
                                int *kind, int *splits);

@@ -32,13 +32,20 @@ cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> 
 // N <= 64 and 64 rows for M <= 64 (where 128 would be at least half empty),
 // 32-deep K slices. Tall, narrow products (N <= 64, M > 128) may take 256 x 64
 // tiles instead (16 x 4 outputs per thread: fewer shared reads per FMA than
-// the 8 x 4 of a 128 x 64 tile) where the schedule model prices them lower.
+// the 8 x 4 of a 128 x 64 tile), and products with 64 rows or fewer 64 x 256
+// tiles (4 x 16 per thread against the 4 x 8 of a 64 x 128 tile), where the
+// schedule model prices them lower.
 namespace simt_tiles {
 constexpr int kTileM = 128, kTileN = 128, kSliceK = 32;
 constexpr int kNarrowN = 64;
 constexpr int kShortTileM = 64;
 constexpr int kTallTileM = 256;
+constexpr int kWideTileN = 256;
 } // namespace simt_tiles
+
+// Tile shape of a SIMT schedule: kStandardTiles (the shapes above by M and N),
+// kTallTiles (256 x 64, N <= 64), kWideTiles (64 x 256, M <= 64).
+enum SimtTiles : int { kStandardTiles = 0, kTallTiles = 1, kWideTiles = 2 };
 
 // How many clusters of `cluster_size` CTAs of `kernel` (`threads` threads,
 // `smem` bytes of dynamic shared memory, attribute already set) can be
@@ -78,10 +85,11 @@ int resident_clusters(Kernel kernel, int cluster_size, int threads, size_t smem,
 }
 
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
-// 4-byte-aligned pointers. 1 <= K; M, N >= 1. `tall`: 256 x 64 tiles where
-// N <= 64 (taken only when the rows of B lie on 16-byte boundaries).
+// 4-byte-aligned pointers. 1 <= K; M, N >= 1. `tiles`: kTallTiles where
+// N <= 64 (taken only when the rows of B lie on 16-byte boundaries),
+// kWideTiles where M <= 64; otherwise the standard shapes.
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream, bool tall = false);
+                             cudaStream_t stream, SimtTiles tiles = kStandardTiles);
 
 // SIMT FP32 product for short, wide shapes (sgemm_short.cu): M <= kShortMaxM,
 // any N and K >= 1, 4-byte-aligned pointers. Each thread keeps one column of
@@ -100,7 +108,7 @@ struct SplitK {
     int splits;  // 1: no split (plain product)
     int kchunk;
     bool spread = false;  // cluster split: one CTA per SM (see sgemm_cluster_plan)
-    bool tall = false;    // 256 x 64 tiles (N <= 64; set by sgemm_cluster_plan only)
+    SimtTiles tiles = kStandardTiles;  // set by sgemm_cluster_plan only
 };
 SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count);  // sgemm_plan.cu
 // The plan's run time in the slice-time units of sgemm_cluster_plan's
@@ -112,7 +120,7 @@ cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const f
 // Split-K without a workspace: the plan.splits (2, 4 or 8) CTAs that share a C
 // tile form one cluster and add their partial tiles through distributed shared
 // memory in rank order (deterministic). plan.splits == 1 is the plain product.
-// plan.tall: the product (split or not) runs on 256 x 64 tiles. *est: the
+// plan.tiles: the tile shape the product (split or not) runs on. *est: the
 // chosen schedule's estimate (also for an unsplit product).
 // resident_spread[i]: clusters of 2 << i CTAs that fit at once with one CTA
 // per SM (sgemm_cluster_resident_spread; 0 if unknown).

@@ -65,20 +65,21 @@ struct ShapeCost {
     double slice_time;
 };
 
-// `tall`: 256 x 64 tiles. A slice of one takes 1.35 slice-times, fitted to
-// tall, narrow products on GB300 (8192 x 64 x 4096 to 16384 x 64 x 8192, K
-// split 1 to 8 ways): the same area as a 128 x 128 tile, but with 16 x 4
-// outputs per thread its loop reads shared memory 5 times per 64 FMA
-// against 4. A 128 x 64 tile's slice (8 x 4 per thread, 6 reads per 64 FMA)
-// takes 0.8 for half the area.
-ShapeCost shape_cost(int M, int N, int K, bool tall = false)
+// kTallTiles (256 x 64) and kWideTiles (64 x 256): a slice of either takes
+// 1.35 slice-times, fitted on GB300 to tall, narrow products (8192 x 64 x 4096
+// to 16384 x 64 x 8192) and to products of 40 to 64 rows (64 x 2048 x 8192 to
+// 64 x 16384 x 8192), K split 1 to 8 ways: the same area as a 128 x 128 tile,
+// but with 16 x 4 or 4 x 16 outputs per thread the loop reads shared memory
+// 5 times per 64 FMA against 4. A 128 x 64 or 64 x 128 tile's slice (8 x 4 or
+// 4 x 8 per thread, 6 reads per 64 FMA) takes 0.8 for half the area.
+ShapeCost shape_cost(int M, int N, int K, SimtTiles shape = kStandardTiles)
 {
-    const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
-    const int tile_m = tall ? kTallTileM : M <= kShortTileM ? kShortTileM : kTileM;
+    const int tile_n = shape == kWideTiles ? kWideTileN : N <= kNarrowN ? kNarrowN : kTileN;
+    const int tile_m = shape == kTallTiles ? kTallTileM : M <= kShortTileM ? kShortTileM : kTileM;
     ShapeCost c;
     c.tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
     c.kslices = (K + kSliceK - 1) / kSliceK;
-    c.slice_time = tall ? 1.35
+    c.slice_time = shape != kStandardTiles ? 1.35
                    : (tile_n == kNarrowN || tile_m == kShortTileM) ? 0.8  // half-area tiles
                                                                    : 1.0;
     return c;
@@ -161,18 +162,24 @@ SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&residen
         return SplitK{1, K};
     double est = 0;
     SplitK p = cluster_plan_for(shape_cost(M, N, K), K, sm_count, resident_spread, &est);
-    if (N <= kNarrowN && M > kTileM && K > 3 * kSliceK) {
-        // Tall, narrow: 256 x 64 tiles, split or not, where they price lower.
-        // Unsplit on GB300: 65536 x 64 x 256 59.5 -> 53.4 us, 65536 x 64 x 2048
-        // 441.8 -> 389.9 us, 131072 x 64 x 1024 the same; with K of one or
-        // two slices the longer CTAs lost (131072 x 16 x 64 30.9 -> 33.0 us).
-        double est_tall = 0;
-        SplitK t = cluster_plan_for(shape_cost(M, N, K, true), K, sm_count, resident_spread,
-                                    &est_tall);
-        if (est_tall < est) {
-            t.tall = true;
+    // Tall, narrow (256 x 64) or short (64 x 256) tiles, split or not, where
+    // they price lower. Tall, unsplit, on GB300: 65536 x 64 x 256 59.5 -> 53.4
+    // us, 65536 x 64 x 2048 441.8 -> 389.9 us, 131072 x 64 x 1024 the same;
+    // with K of one or two slices the longer CTAs lost (131072 x 16 x 64 30.9
+    // -> 33.0 us), so K of three slices or fewer keeps the standard tiles.
+    SimtTiles alt = kStandardTiles;
+    if (N <= kNarrowN && M > kTileM)
+        alt = kTallTiles;
+    else if (M <= kShortTileM && N > kNarrowN)
+        alt = kWideTiles;
+    if (alt != kStandardTiles && K > 3 * kSliceK) {
+        double est_alt = 0;
+        SplitK t = cluster_plan_for(shape_cost(M, N, K, alt), K, sm_count, resident_spread,
+                                    &est_alt);
+        if (est_alt < est) {
+            t.tiles = alt;
             p = t;
-            est = est_tall;
+            est = est_alt;
         }
     }
     if (est_out)

@@ -653,10 +653,12 @@ cudaError_t launch_tall(int M, int N, int K, const float *A, const float *B, flo
 } // namespace
 
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream, bool tall)
+                             cudaStream_t stream, SimtTiles tiles)
 {
-    if (tall && N <= kNarrowN)
+    if (tiles == kTallTiles && N <= kNarrowN)
         return launch_tall<simt::kPlain>(M, N, K, A, B, C, stream);
+    if (tiles == kWideTiles && M <= kShortTileM)  // 64 x 256 tiles, 4 x 16 per thread
+        return simt::launch_any<kShortTileM, kWideTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
     if (M <= kShortTileM) {  // 64-row tiles: 128-row tiles would be at least half empty
         if (N <= kNarrowN)
             return simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
@@ -734,8 +736,8 @@ int sgemm_cluster_resident_spread(int cluster_size)
 SplitK sgemm_cluster_schedule(int M, int N, int K, int sm_count, double *est)
 {
     // The fewest tiles any candidate tile shape gives (256 x 64 for tall,
-    // narrow products).
-    const int tile_n = N <= kNarrowN ? kNarrowN : kTileN;
+    // narrow products, 64 x 256 for short ones).
+    const int tile_n = N <= kNarrowN ? kNarrowN : M <= kShortTileM ? kWideTileN : kTileN;
     const int tile_m = M <= kShortTileM ? kShortTileM : N <= kNarrowN ? kTallTileM : kTileM;
     const long long tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
     int resident[3] = {0, 0, 0};
@@ -761,9 +763,12 @@ cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const 
                                      const SplitK &plan, cudaStream_t stream)
 {
     using simt::kSplitCluster;
-    if (plan.tall && N <= kNarrowN)
+    if (plan.tiles == kTallTiles && N <= kNarrowN)
         return launch_tall<kSplitCluster>(M, N, K, A, B, C, stream, plan.splits, plan.kchunk,
                                           plan.spread);
+    if (plan.tiles == kWideTiles && M <= kShortTileM)
+        return simt::launch_any<kShortTileM, kWideTileN, kSliceK, 2, 2, 1, kSplitCluster>(
+            M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread);
     if (M <= kShortTileM)
         return N <= kNarrowN
                    ? simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitCluster>(
@@ -801,7 +806,7 @@ cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const fl
     const TailPlan tail = sgemm_tail_plan(M, N, K, sm_count);
     if (tail.tail.splits > 1)
         return launch_sgemm_f32_tail(M, N, K, A, B, C, tail, stream);
-    return launch_sgemm_f32(M, N, K, A, B, C, stream, cluster.tall);
+    return launch_sgemm_f32(M, N, K, A, B, C, stream, cluster.tiles);
 }
 
 } // namespace rtm

@@ -30,9 +30,9 @@ int main(int argc, char **argv)
         const double w_est = rtm::sgemm_workspace_estimate(M, N, K, sms, w);
         const bool ws_wins = w.splits > 1 && !(cluster_est < w_est);
         const rtm::TailPlan t = rtm::sgemm_tail_plan(M, N, K, sms);
-        std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d tall %d\n", M, N, K,
+        std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d tiles %d\n", M, N, K,
                     c.splits, c.spread ? 1 : 0, w.splits, ws_wins ? 1 : 0, t.plain_tiles,
-                    t.tail.splits, c.tall ? 1 : 0);
+                    t.tail.splits, (int)c.tiles);
     }
     return 0;
 }

@@ -35,7 +35,7 @@ SHAPES = [
     (300, 200, 1024),    # 8 per cluster spread, ragged tiles
     (129, 65, 999),      # 8 per cluster spread, one spare row and column tile
     (4096, 64, 4096),    # 128 x 64 tiles, 8 per cluster, two CTAs per SM
-    (60, 3000, 2000),    # 64 x 128 tiles, 8 per cluster
+    (48, 4096, 4096),    # 64 x 128 tiles, 8 per cluster, two CTAs per SM
     (64, 8, 4096),       # 64 x 64 tiles, 8 per cluster spread
     (48, 64, 1000),      # 64 x 64 tiles, 8 per cluster spread, partial last chunk
     (300, 201, 1024),    # N % 4 != 0: 4-byte copies of B and stores of C
@@ -79,6 +79,56 @@ def test_tall_tiles_parity(M, N, K, splits):
     torch.cuda.synchronize()
     assert rtm.get_device_error() == 0
     assert_close_to_oracle(C, A, B, "f32")
+
+
+# Products of 33 to 64 rows on 64 x 256 tiles, 4 x 16 outputs per thread.
+WIDE_SHAPES = [
+    (64, 8192, 4096, 8),    # 32 tiles, 8 per cluster, two CTAs per SM
+    (60, 3000, 2000, 8),    # 12 tiles, 8 per cluster spread, ragged M, N and K
+    (48, 2048, 8192, 8),    # 8 tiles spread, a 48-row tile
+    (64, 16384, 2048, 4),   # 64 tiles, 4 per cluster
+    (40, 8192, 4096, 8),    # 40 live rows of 64
+    (64, 8191, 4096, 8),    # N % 4 != 0: 4-byte copies of B and stores of C
+    (64, 65536, 512, 1),    # 256 tiles unsplit
+]
+
+
+@pytest.mark.parametrize("M,N,K,splits", WIDE_SHAPES)
+def test_wide_tiles_parity(M, N, K, splits):
+    kind, s = rtm.gemm_f32_schedule(M, N, K)
+    want = "wide-tiles+cluster-split" if splits > 1 else "wide-tiles"
+    assert (kind, s) == (want, splits), (kind, s)
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M * 11 + N * 3 + K)
+    C = rtm.gemm_f32(A.to(DEV), B.to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "f32")
+
+
+def test_wide_tiles_sampled_64x8192x8192():
+    M, N, K = 64, 8192, 8192
+    assert rtm.gemm_f32_schedule(M, N, K) == ("wide-tiles+cluster-split", 8)
+    assert rtm.gemm_f32_workspace_bytes(M, N, K) == 0  # the workspace split prices higher
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=85)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = rtm.gemm_f32(Ad, Bd)
+    Cw = rtm.gemm_f32_ws(Ad, Bd)
+    torch.cuda.synchronize()
+    assert torch.equal(C, Cw)
+    assert_close_to_oracle(C, A, B, "f32", full=False, seed=85)
+
+
+@pytest.mark.parametrize("M,N,K", [(60, 3000, 2000), (64, 8192, 1024), (64, 65536, 512)])
+def test_wide_tiles_small_integer_guard_band_repeatability(M, N, K):
+    A, B = small_int_inputs(M, N, K, seed=M + 5 * K)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf, C = guarded_output(M, N, DEV)
+    rtm.gemm_f32(Ad, Bd, out=C)
+    C2 = rtm.gemm_f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert guard_intact(buf, M, N), "a store landed outside C"
+    assert torch.equal(C, C2)
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
 
 
 @pytest.mark.parametrize("M,N,K", [(2000, 60, 2000), (8192, 64, 1024), (20000, 64, 300)])

@@ -19,14 +19,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "register_tiled_matrix_gb300", "csrc")
 
 # (M, N, K): (cluster splits, spread, workspace splits, workspace priced lower,
-#             unsplit tiles before the tail, tail splits, 256 x 64 tiles)
+#             unsplit tiles before the tail, tail splits, tile shape: 0 standard,
+#             1 tall 256 x 64, 2 wide 64 x 256)
 EXPECT = {
     (256, 256, 256): (8, 1, 8, 0, 0, 1, 0),        # 4 tiles: 8 per cluster, one CTA per SM
     (1024, 1024, 1024): (4, 0, 2, 0, 0, 1, 0),     # 52.8 us split 4, 55.4 with the workspace
     (1000, 1000, 999): (4, 0, 2, 0, 0, 1, 0),
     (300, 260, 129): (2, 0, 5, 1, 0, 1, 0),
     (512, 512, 8192): (8, 0, 9, 1, 0, 1, 0),       # long K over 16 tiles: the workspace wins
-    (64, 8192, 8192): (4, 0, 7, 1, 0, 1, 0),       # 64-row tiles
+    (64, 4096, 8192): (8, 0, 19, 1, 0, 1, 0),      # 64-row tiles: the workspace wins
     (2048, 1024, 1024): (1, 0, 1, 0, 0, 1, 0),     # 128 tiles: split was no faster
     (4096, 4096, 4096): (1, 0, 1, 0, 0, 1, 0),     # 3 waves + 112 tiles: tail left alone
     (4097, 3001, 1023): (1, 0, 1, 0, 608, 4, 0),   # 608 tiles + a 184-tile tail split
@@ -45,6 +46,19 @@ EXPECT = {
     (32768, 64, 512): (1, 0, 1, 0, 0, 1, 1),       # 128 tall tiles unsplit
     (200, 64, 8192): (8, 1, 32, 1, 0, 1, 0),       # M <= 256: one tall tile prices no lower
     (131072, 16, 64): (1, 0, 1, 0, 0, 1, 0),       # two K slices: 128 x 64 tiles
+    # 33 to 64 rows: 64 x 256 tiles against 64 x 128, fastest on GB300 in each
+    # row (us): 220.0 for 64 x 128 split 4 against 199.0 here; 114.7 (split 2)
+    # against 104.5; 434.9 (split 8) against 385.5; 112.8 against 104.4; 120.4
+    # against 111.3; 64.5 here against 108.8 (16 wide tiles); 20.6 here
+    # against 30.9.
+    (64, 8192, 8192): (8, 0, 7, 0, 0, 1, 2),
+    (64, 16384, 2048): (4, 0, 1, 0, 0, 1, 2),
+    (64, 16384, 8192): (4, 0, 7, 0, 0, 1, 2),
+    (64, 2048, 8192): (8, 1, 19, 1, 0, 1, 2),
+    (40, 8192, 4096): (8, 0, 7, 0, 0, 1, 2),
+    (48, 4096, 4096): (8, 0, 19, 0, 0, 1, 0),
+    (64, 4096, 1024): (4, 0, 4, 0, 0, 1, 0),
+    (64, 65536, 512): (1, 0, 1, 0, 0, 1, 2),       # 256 wide tiles unsplit
 }
 
 
@@ -102,4 +116,5 @@ def test_schedule_kinds_cover_the_planner_outcomes():
     """Every outcome above has a name in the binding's schedule kinds."""
     assert set(rtm.F32_KINDS.values()) >= {"tiles", "tiles+cluster-split", "tiles+workspace-split",
                                             "column-strips", "tiles+tail-cluster-split",
-                                            "tall-tiles", "tall-tiles+cluster-split"}
+                                            "tall-tiles", "tall-tiles+cluster-split",
+                                            "wide-tiles", "wide-tiles+cluster-split"}
