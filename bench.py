@@ -56,7 +56,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
 # reported as null once the source changes. See profiles/.
 TRAFFIC = {
-    "gemm_f32": {"bytes": 391413504, "source_sha1": "69a801c005f7006e51f19b202e511e103d76f8dc",
+    "gemm_f32": {"bytes": 395077120, "source_sha1": "309203ed1ae2e0a8ada0c4e71a8b56d4851365c8",
                  "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
     "gemm_bf16f32": {"bytes": 1365153024,
                      "source_sha1": "2564a8cd5cb12f0cd75e69661170f865254c938a",

@@ -379,11 +379,11 @@ int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace, int *k
             } else {
                 cluster = rtm::sgemm_cluster_schedule((int)M, (int)N, (int)K, d.sms);
             }
-            if (k == GEMM_F32_NO_KERNEL && cluster.tiles == rtm::kTallTiles) {
+            if (k == GEMM_F32_NO_KERNEL && cluster.tile.m == rtm::simt_tiles::kTallTileM) {
                 k = cluster.splits > 1 ? GEMM_F32_TALL_TILES_CLUSTER : GEMM_F32_TALL_TILES;
                 s = cluster.splits;
             }
-            if (k == GEMM_F32_NO_KERNEL && cluster.tiles == rtm::kWideTiles) {
+            if (k == GEMM_F32_NO_KERNEL && cluster.tile.n == rtm::simt_tiles::kWideTileN) {
                 k = cluster.splits > 1 ? GEMM_F32_WIDE_TILES_CLUSTER : GEMM_F32_WIDE_TILES;
                 s = cluster.splits;
             }

@@ -43,9 +43,21 @@ constexpr int kTallTileM = 256;
 constexpr int kWideTileN = 256;
 } // namespace simt_tiles
 
-// Tile shape of a SIMT schedule: kStandardTiles (the shapes above by M and N),
-// kTallTiles (256 x 64, N <= 64), kWideTiles (64 x 256, M <= 64).
-enum SimtTiles : int { kStandardTiles = 0, kTallTiles = 1, kWideTiles = 2 };
+// Tile shape of a SIMT schedule, rows x columns of C per CTA: 128 x 128,
+// 128 x 64, 64 x 128, 64 x 64, 256 x 64 or 64 x 256. {0, 0} stands for the
+// standard shape of the product (simt_standard_tile).
+struct SimtTile {
+    int m = 0, n = 0;
+};
+inline SimtTile simt_standard_tile(int M, int N)
+{
+    return SimtTile{M <= simt_tiles::kShortTileM ? simt_tiles::kShortTileM : simt_tiles::kTileM,
+                    N <= simt_tiles::kNarrowN ? simt_tiles::kNarrowN : simt_tiles::kTileN};
+}
+inline SimtTile simt_resolve_tile(SimtTile t, int M, int N)
+{
+    return t.m > 0 && t.n > 0 ? t : simt_standard_tile(M, N);
+}
 
 // How many clusters of `cluster_size` CTAs of `kernel` (`threads` threads,
 // `smem` bytes of dynamic shared memory, attribute already set) can be
@@ -85,11 +97,11 @@ int resident_clusters(Kernel kernel, int cluster_size, int threads, size_t smem,
 }
 
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
-// 4-byte-aligned pointers. 1 <= K; M, N >= 1. `tiles`: kTallTiles where
-// N <= 64 (taken only when the rows of B lie on 16-byte boundaries),
-// kWideTiles where M <= 64; otherwise the standard shapes.
+// 4-byte-aligned pointers. 1 <= K; M, N >= 1. `tile`: the CTA tile shape
+// (any of SimtTile's; 256 x 64 tiles are taken only when the rows of B lie on
+// 16-byte boundaries, 128 x 64 otherwise).
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream, SimtTiles tiles = kStandardTiles);
+                             cudaStream_t stream, SimtTile tile = SimtTile{});
 
 // SIMT FP32 product for short, wide shapes (sgemm_short.cu): M <= kShortMaxM,
 // any N and K >= 1, 4-byte-aligned pointers. Each thread keeps one column of
@@ -108,7 +120,7 @@ struct SplitK {
     int splits;  // 1: no split (plain product)
     int kchunk;
     bool spread = false;  // cluster split: one CTA per SM (see sgemm_cluster_plan)
-    SimtTiles tiles = kStandardTiles;  // set by sgemm_cluster_plan only
+    SimtTile tile{};  // set by sgemm_cluster_plan only ({0, 0}: the standard shape)
 };
 SplitK sgemm_splitk_plan(int M, int N, int K, int sm_count);  // sgemm_plan.cu
 // The plan's run time in the slice-time units of sgemm_cluster_plan's
@@ -120,7 +132,7 @@ cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const f
 // Split-K without a workspace: the plan.splits (2, 4 or 8) CTAs that share a C
 // tile form one cluster and add their partial tiles through distributed shared
 // memory in rank order (deterministic). plan.splits == 1 is the plain product.
-// plan.tiles: the tile shape the product (split or not) runs on. *est: the
+// plan.tile: the tile shape the product (split or not) runs on. *est: the
 // chosen schedule's estimate (also for an unsplit product).
 // resident_spread[i]: clusters of 2 << i CTAs that fit at once with one CTA
 // per SM (sgemm_cluster_resident_spread; 0 if unknown).

@@ -65,23 +65,27 @@ struct ShapeCost {
     double slice_time;
 };
 
-// kTallTiles (256 x 64) and kWideTiles (64 x 256): a slice of either takes
-// 1.35 slice-times, fitted on GB300 to tall, narrow products (8192 x 64 x 4096
-// to 16384 x 64 x 8192) and to products of 40 to 64 rows (64 x 2048 x 8192 to
-// 64 x 16384 x 8192), K split 1 to 8 ways: the same area as a 128 x 128 tile,
-// but with 16 x 4 or 4 x 16 outputs per thread the loop reads shared memory
-// 5 times per 64 FMA against 4. A 128 x 64 or 64 x 128 tile's slice (8 x 4 or
-// 4 x 8 per thread, 6 reads per 64 FMA) takes 0.8 for half the area.
-ShapeCost shape_cost(int M, int N, int K, SimtTiles shape = kStandardTiles)
+// Slice-times of one slice of each tile shape. 256 x 64 and 64 x 256 take
+// 1.35, fitted on GB300 to tall, narrow products (8192 x 64 x 4096 to 16384 x
+// 64 x 8192) and to products of 40 to 64 rows (64 x 2048 x 8192 to 64 x 16384
+// x 8192), K split 1 to 8 ways: the same area as a 128 x 128 tile, but with
+// 16 x 4 or 4 x 16 outputs per thread the loop reads shared memory 5 times
+// per 64 FMA against 4. A 128 x 64 or 64 x 128 tile's slice (8 x 4 or 4 x 8
+// per thread, 6 reads per 64 FMA) takes 0.8 for half the area, a 64 x 64
+// tile's (4 x 4 per thread, 8 reads per 64 FMA) 0.45 for a quarter: with it
+// the plan picked the fastest tile and split measured on GB300 for 256^3,
+// 384^3, 512^3 and 256 x 256 x 1024.
+ShapeCost shape_cost(int M, int N, int K, SimtTile shape = SimtTile{})
 {
-    const int tile_n = shape == kWideTiles ? kWideTileN : N <= kNarrowN ? kNarrowN : kTileN;
-    const int tile_m = shape == kTallTiles ? kTallTileM : M <= kShortTileM ? kShortTileM : kTileM;
+    const SimtTile t = simt_resolve_tile(shape, M, N);
     ShapeCost c;
-    c.tiles = (long long)((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
+    c.tiles = (long long)((M + t.m - 1) / t.m) * ((N + t.n - 1) / t.n);
     c.kslices = (K + kSliceK - 1) / kSliceK;
-    c.slice_time = shape != kStandardTiles ? 1.35
-                   : (tile_n == kNarrowN || tile_m == kShortTileM) ? 0.8  // half-area tiles
-                                                                   : 1.0;
+    const int area = t.m * t.n;
+    c.slice_time = t.m == kTallTileM || t.n == kWideTileN ? 1.35
+                   : area == kTileM * kTileN              ? 1.0
+                   : area == kTileM * kNarrowN            ? 0.8
+                                                          : 0.45;
     return c;
 }
 
@@ -162,22 +166,40 @@ SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&residen
         return SplitK{1, K};
     double est = 0;
     SplitK p = cluster_plan_for(shape_cost(M, N, K), K, sm_count, resident_spread, &est);
-    // Tall, narrow (256 x 64) or short (64 x 256) tiles, split or not, where
-    // they price lower. Tall, unsplit, on GB300: 65536 x 64 x 256 59.5 -> 53.4
-    // us, 65536 x 64 x 2048 441.8 -> 389.9 us, 131072 x 64 x 1024 the same;
-    // with K of one or two slices the longer CTAs lost (131072 x 16 x 64 30.9
-    // -> 33.0 us), so K of three slices or fewer keeps the standard tiles.
-    SimtTiles alt = kStandardTiles;
-    if (N <= kNarrowN && M > kTileM)
-        alt = kTallTiles;
-    else if (M <= kShortTileM && N > kNarrowN)
-        alt = kWideTiles;
-    if (alt != kStandardTiles && K > 3 * kSliceK) {
+    // Other tile shapes, split or not, where they price lower: tall, narrow
+    // (256 x 64) or short (64 x 256) tiles; and for products with few tiles,
+    // 64-row and 64-column tiles, whose smaller CTAs spread the work over
+    // more SMs. Tall, unsplit, on GB300: 65536 x 64 x 256 59.5 -> 53.4 us,
+    // 65536 x 64 x 2048 441.8 -> 389.9 us, 131072 x 64 x 1024 the same; with K
+    // of one or two slices the longer CTAs lost (131072 x 16 x 64 30.9 -> 33.0
+    // us), so K of three slices or fewer keeps the standard tiles. Smaller
+    // tiles, against 128 x 128 split over clusters: 256^3 10.3 -> 8.2 us
+    // (64 x 64, split 4), 384^3 16.4 -> 8.8 (64 x 64, split 4), 512^3 18.5 ->
+    // 12.4 (64 x 128, split 4), 256 x 256 x 1024 18.5 -> 12.5 (64 x 128, split 8).
+    const SimtTile std_tile = simt_standard_tile(M, N);
+    SimtTile alts[4];
+    int n_alt = 0;
+    if (K > 3 * kSliceK) {
+        if (N <= kNarrowN && M > kTileM)
+            alts[n_alt++] = SimtTile{kTallTileM, kNarrowN};
+        else if (M <= kShortTileM && N > kNarrowN)
+            alts[n_alt++] = SimtTile{kShortTileM, kWideTileN};
+    }
+    if (M > kShortTileM)
+        alts[n_alt++] = SimtTile{kShortTileM, std_tile.n};
+    if (N > kNarrowN)
+        alts[n_alt++] = SimtTile{std_tile.m, kNarrowN};
+    if (M > kShortTileM && N > kNarrowN)
+        alts[n_alt++] = SimtTile{kShortTileM, kNarrowN};
+    for (int i = 0; i < n_alt; ++i) {
+        const ShapeCost c = shape_cost(M, N, K, alts[i]);
+        const bool tall_or_wide = alts[i].m == kTallTileM || alts[i].n == kWideTileN;
+        if (!tall_or_wide && c.tiles > sm_count)
+            continue;  // smaller tiles only where they all fit at once
         double est_alt = 0;
-        SplitK t = cluster_plan_for(shape_cost(M, N, K, alt), K, sm_count, resident_spread,
-                                    &est_alt);
+        SplitK t = cluster_plan_for(c, K, sm_count, resident_spread, &est_alt);
         if (est_alt < est) {
-            t.tiles = alt;
+            t.tile = alts[i];
             p = t;
             est = est_alt;
         }

@@ -650,23 +650,39 @@ cudaError_t launch_tall(int M, int N, int K, const float *A, const float *B, flo
         M, N, K, A, B, C, stream, splits, kchunk, spread);
 }
 
+// The SIMT kernel on tile shape `tile` (resolved: both sides set), plain or
+// with K split over the CTAs of a cluster.
+template <int SPLIT>
+cudaError_t launch_tile(SimtTile tile, int M, int N, int K, const float *A, const float *B,
+                        float *C, cudaStream_t stream, int splits = 1, int kchunk = 0,
+                        bool spread = false)
+{
+    if (tile.m == kTallTileM && tile.n == kNarrowN)
+        return launch_tall<SPLIT>(M, N, K, A, B, C, stream, splits, kchunk, spread);
+    if (tile.m == kShortTileM && tile.n == kWideTileN)  // 4 x 16 per thread
+        return simt::launch_any<kShortTileM, kWideTileN, kSliceK, 2, 2, 1, SPLIT>(
+            M, N, K, A, B, C, stream, splits, kchunk, spread);
+    if (tile.m == kShortTileM && tile.n == kNarrowN)
+        return simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, SPLIT>(
+            M, N, K, A, B, C, stream, splits, kchunk, spread);
+    if (tile.m == kShortTileM)
+        return simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1, SPLIT>(
+            M, N, K, A, B, C, stream, splits, kchunk, spread);
+    if (tile.n == kNarrowN)
+        return simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, SPLIT>(
+            M, N, K, A, B, C, stream, splits, kchunk, spread);
+    return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, SPLIT>(M, N, K, A, B, C, stream,
+                                                                   splits, kchunk, spread);
+}
+
 } // namespace
 
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream, SimtTiles tiles)
+                             cudaStream_t stream, SimtTile tile)
 {
-    if (tiles == kTallTiles && N <= kNarrowN)
-        return launch_tall<simt::kPlain>(M, N, K, A, B, C, stream);
-    if (tiles == kWideTiles && M <= kShortTileM)  // 64 x 256 tiles, 4 x 16 per thread
-        return simt::launch_any<kShortTileM, kWideTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
-    if (M <= kShortTileM) {  // 64-row tiles: 128-row tiles would be at least half empty
-        if (N <= kNarrowN)
-            return simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
-        return simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
-    }
-    if (N <= kNarrowN)
-        return simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
-    return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream);
+    // Without a choice, 64-row tiles for M <= 64 (128-row tiles would be at
+    // least half empty) and 64-column tiles for N <= 64.
+    return launch_tile<simt::kPlain>(simt_resolve_tile(tile, M, N), M, N, K, A, B, C, stream);
 }
 
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
@@ -762,24 +778,8 @@ F32Schedule sgemm_ws_schedule(int M, int N, int K, int sm_count)
 cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const float *B, float *C,
                                      const SplitK &plan, cudaStream_t stream)
 {
-    using simt::kSplitCluster;
-    if (plan.tiles == kTallTiles && N <= kNarrowN)
-        return launch_tall<kSplitCluster>(M, N, K, A, B, C, stream, plan.splits, plan.kchunk,
-                                          plan.spread);
-    if (plan.tiles == kWideTiles && M <= kShortTileM)
-        return simt::launch_any<kShortTileM, kWideTileN, kSliceK, 2, 2, 1, kSplitCluster>(
-            M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread);
-    if (M <= kShortTileM)
-        return N <= kNarrowN
-                   ? simt::launch_any<kShortTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitCluster>(
-                         M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread)
-                   : simt::launch_any<kShortTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
-                         M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread);
-    return N <= kNarrowN
-               ? simt::launch_any<kTileM, kNarrowN, kSliceK, 2, 2, 1, kSplitCluster>(
-                     M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread)
-               : simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
-                     M, N, K, A, B, C, stream, plan.splits, plan.kchunk, plan.spread);
+    return launch_tile<simt::kSplitCluster>(simt_resolve_tile(plan.tile, M, N), M, N, K, A, B, C,
+                                            stream, plan.splits, plan.kchunk, plan.spread);
 }
 
 cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const float *B, float *C,
@@ -806,7 +806,7 @@ cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const fl
     const TailPlan tail = sgemm_tail_plan(M, N, K, sm_count);
     if (tail.tail.splits > 1)
         return launch_sgemm_f32_tail(M, N, K, A, B, C, tail, stream);
-    return launch_sgemm_f32(M, N, K, A, B, C, stream, cluster.tiles);
+    return launch_sgemm_f32(M, N, K, A, B, C, stream, cluster.tile);
 }
 
 } // namespace rtm

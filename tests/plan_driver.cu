@@ -30,9 +30,10 @@ int main(int argc, char **argv)
         const double w_est = rtm::sgemm_workspace_estimate(M, N, K, sms, w);
         const bool ws_wins = w.splits > 1 && !(cluster_est < w_est);
         const rtm::TailPlan t = rtm::sgemm_tail_plan(M, N, K, sms);
-        std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d tiles %d\n", M, N, K,
+        const rtm::SimtTile tile = rtm::simt_resolve_tile(c.tile, M, N);
+        std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d tile %d %d\n", M, N, K,
                     c.splits, c.spread ? 1 : 0, w.splits, ws_wins ? 1 : 0, t.plain_tiles,
-                    t.tail.splits, (int)c.tiles);
+                    t.tail.splits, tile.m, tile.n);
     }
     return 0;
 }

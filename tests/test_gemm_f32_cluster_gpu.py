@@ -26,7 +26,8 @@ def _lib():
 
 
 SHAPES = [
-    (300, 260, 129),     # 2 per cluster
+    (300, 3000, 700),    # 2 per cluster
+    (300, 700, 400),     # 64 x 64 tiles (the plan's choice for few tiles), 2 per cluster
     (1024, 1024, 1024),  # 4 per cluster, two CTAs per SM
     (1000, 1000, 999),   # the same, ragged in M, N and K
     (512, 512, 512),     # 4 per cluster, one CTA per SM
@@ -59,11 +60,10 @@ def test_cluster_split_parity(M, N, K):
 # thread, K split over a cluster or not at all.
 TALL_SHAPES = [
     (8192, 64, 4096, 8),    # 32 tiles, 8 per cluster, two CTAs per SM
-    (2000, 60, 2000, 8),    # 8 tiles, 8 per cluster spread one CTA per SM, ragged M and N
-    (2049, 64, 1000, 8),    # one spare row: a 256-row tile with a single live row
+    (8193, 64, 2048, 8),    # one spare row: a 256-row tile with a single live row
     (16384, 64, 2048, 4),   # 64 tiles, 4 per cluster
     (8192, 61, 4096, 8),    # rows of B off 16-byte boundaries: 128 x 64 tiles, same split
-    (3000, 33, 1500, 8),    # ragged in M, N and K
+    (3000, 33, 1500, 8),    # 12 tiles spread one CTA per SM, ragged in M, N and K
     (32768, 64, 512, 1),    # 128 tiles unsplit
     (20000, 64, 300, 1),    # more tiles than SMs, ragged M and K
 ]
@@ -85,7 +85,7 @@ def test_tall_tiles_parity(M, N, K, splits):
 WIDE_SHAPES = [
     (64, 8192, 4096, 8),    # 32 tiles, 8 per cluster, two CTAs per SM
     (60, 3000, 2000, 8),    # 12 tiles, 8 per cluster spread, ragged M, N and K
-    (48, 2048, 8192, 8),    # 8 tiles spread, a 48-row tile
+    (60, 8192, 2048, 8),    # a 60-row tile
     (64, 16384, 2048, 4),   # 64 tiles, 4 per cluster
     (40, 8192, 4096, 8),    # 40 live rows of 64
     (64, 8191, 4096, 8),    # N % 4 != 0: 4-byte copies of B and stores of C
@@ -131,7 +131,7 @@ def test_wide_tiles_small_integer_guard_band_repeatability(M, N, K):
     assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
 
 
-@pytest.mark.parametrize("M,N,K", [(2000, 60, 2000), (8192, 64, 1024), (20000, 64, 300)])
+@pytest.mark.parametrize("M,N,K", [(8193, 64, 2048), (8192, 64, 1024), (20000, 64, 300)])
 def test_tall_tiles_small_integer_guard_band_repeatability(M, N, K):
     A, B = small_int_inputs(M, N, K, seed=M + 7 * K)
     Ad, Bd = A.to(DEV), B.to(DEV)

@@ -35,7 +35,7 @@ CASES = {
     "gemm_f32": ("f32", 640, 520, 384, lambda A, B, C, W: rtm.gemm_f32(A, B, out=C)),
     "gemm_f32 cluster split-K": ("f32", 1000, 1000, 999,
                                  lambda A, B, C, W: rtm.gemm_f32(A, B, out=C)),
-    "gemm_f32 256x64 tiles, cluster split-K": ("f32", 2000, 60, 2000,
+    "gemm_f32 256x64 tiles, cluster split-K": ("f32", 8192, 64, 1024,
                                                lambda A, B, C, W: rtm.gemm_f32(A, B, out=C)),
     "gemm_f32_ws split-K": ("f32", 512, 64, 2048,
                             lambda A, B, C, W: rtm.gemm_f32_ws(A, B, out=C, workspace=W)),

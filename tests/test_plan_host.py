@@ -3,9 +3,10 @@ tc_plan.cu): a driver built from tests/plan_driver.cu prints each planner's
 choice for a 152-SM GB300, and the choices the GB300 sweeps justified are
 checked here: which fp32 products split K over clusters and into how many
 CTAs, when the workspace split is priced below the cluster split, when the
-ragged last wave of a larger product is split, which tall, narrow products
-take 256 x 64 tiles, and which tiles of the bf16 CTA-pair kernel split K in
-two."""
+ragged last wave of a larger product is split, which tile shape a product
+takes (256 x 64 and 64 x 256 for tall and short ones, 64-row and 64-column
+tiles for products with few tiles), and which tiles of the bf16 CTA-pair
+kernel split K in two."""
 
 import os
 import shutil
@@ -19,46 +20,48 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "register_tiled_matrix_gb300", "csrc")
 
 # (M, N, K): (cluster splits, spread, workspace splits, workspace priced lower,
-#             unsplit tiles before the tail, tail splits, tile shape: 0 standard,
-#             1 tall 256 x 64, 2 wide 64 x 256)
+#             unsplit tiles before the tail, tail splits, CTA tile rows x columns)
 EXPECT = {
-    (256, 256, 256): (8, 1, 8, 0, 0, 1, 0),        # 4 tiles: 8 per cluster, one CTA per SM
-    (1024, 1024, 1024): (4, 0, 2, 0, 0, 1, 0),     # 52.8 us split 4, 55.4 with the workspace
-    (1000, 1000, 999): (4, 0, 2, 0, 0, 1, 0),
-    (300, 260, 129): (2, 0, 5, 1, 0, 1, 0),
-    (512, 512, 8192): (8, 0, 9, 1, 0, 1, 0),       # long K over 16 tiles: the workspace wins
-    (64, 4096, 8192): (8, 0, 19, 1, 0, 1, 0),      # 64-row tiles: the workspace wins
-    (2048, 1024, 1024): (1, 0, 1, 0, 0, 1, 0),     # 128 tiles: split was no faster
-    (4096, 4096, 4096): (1, 0, 1, 0, 0, 1, 0),     # 3 waves + 112 tiles: tail left alone
-    (4097, 3001, 1023): (1, 0, 1, 0, 608, 4, 0),   # 608 tiles + a 184-tile tail split
-    (2304, 2304, 4096): (1, 0, 1, 0, 304, 4, 0),   # one wave + 20 tiles
-    (2048, 1536, 1024): (1, 0, 1, 0, 0, 4, 0),     # 192 tiles, under two waves
-    (2048, 2304, 512): (1, 0, 1, 0, 0, 1, 0),      # 4-slice chunks, 95 % of the slots
+    (256, 256, 256): (4, 0, 8, 0, 0, 1, (64, 64)),       # 10.3 -> 8.2 us against 128 x 128 split 8
+    (384, 384, 384): (4, 0, 12, 0, 0, 1, (64, 64)),      # 16.4 -> 8.8 us
+    (512, 512, 512): (4, 0, 8, 0, 0, 1, (64, 128)),      # 18.5 -> 12.4 us
+    (256, 256, 1024): (8, 1, 32, 1, 0, 1, (64, 128)),    # 18.5 -> 12.5 us
+    (1024, 1024, 1024): (4, 0, 2, 0, 0, 1, (128, 128)),  # 52.8 us split 4, 55.4 with the workspace
+    (1000, 1000, 999): (4, 0, 2, 0, 0, 1, (128, 128)),
+    (512, 512, 8192): (8, 0, 9, 1, 0, 1, (64, 128)),     # 182.2 -> 115.0 us; the workspace wins
+    (64, 4096, 8192): (8, 0, 19, 1, 0, 1, (64, 128)),    # 64-row tiles: the workspace wins
+    (2048, 1024, 1024): (1, 0, 1, 0, 0, 1, (128, 128)),  # 128 tiles: split was no faster
+    (4096, 4096, 4096): (1, 0, 1, 0, 0, 1, (128, 128)),  # 3 waves + 112 tiles: tail left alone
+    (4097, 3001, 1023): (1, 0, 1, 0, 608, 4, (128, 128)),  # 608 tiles + a 184-tile tail split
+    (2304, 2304, 4096): (1, 0, 1, 0, 304, 4, (128, 128)),  # one wave + 20 tiles
+    (2048, 1536, 1024): (1, 0, 1, 0, 0, 4, (128, 128)),  # 192 tiles, under two waves
+    (2048, 2304, 512): (1, 0, 1, 0, 0, 1, (128, 128)),   # 4-slice chunks, 95 % of the slots
+    (300, 3000, 700): (2, 0, 2, 0, 0, 1, (128, 128)),
     # Tall, narrow (N <= 64): 256 x 64 tiles against 128 x 64, fastest on GB300 in
     # each row (us): 117.6 for 128 x 64 split 4 against 106.1 here; 230.4 (split 8)
-    # against 196.7; 227.4 against 198.8; 62.7 here against 100.5; 115.0 against
-    # 104.5 with two CTAs to an SM.
-    (8192, 64, 4096): (8, 0, 7, 0, 0, 1, 1),
-    (16384, 64, 4096): (4, 0, 8, 0, 0, 1, 1),
-    (8192, 64, 8192): (8, 0, 7, 0, 0, 1, 1),
-    (4096, 64, 4096): (8, 0, 19, 0, 0, 1, 0),      # 16 tall tiles would pack two to an SM
-    (2048, 64, 8192): (8, 1, 19, 1, 0, 1, 1),
-    (32768, 64, 512): (1, 0, 1, 0, 0, 1, 1),       # 128 tall tiles unsplit
-    (200, 64, 8192): (8, 1, 32, 1, 0, 1, 0),       # M <= 256: one tall tile prices no lower
-    (131072, 16, 64): (1, 0, 1, 0, 0, 1, 0),       # two K slices: 128 x 64 tiles
+    # against 196.7; 227.4 against 198.8; 62.7 here against 100.5; 2048 x 64 x 8192
+    # on 64 x 64 tiles 77.1 through gemm_f32 against 105.2 on 256 x 64.
+    (8192, 64, 4096): (8, 0, 7, 0, 0, 1, (256, 64)),
+    (16384, 64, 4096): (4, 0, 8, 0, 0, 1, (256, 64)),
+    (8192, 64, 8192): (8, 0, 7, 0, 0, 1, (256, 64)),
+    (4096, 64, 4096): (8, 0, 19, 0, 0, 1, (128, 64)),    # 16 tall tiles would pack two to an SM
+    (2048, 64, 8192): (8, 0, 19, 1, 0, 1, (64, 64)),
+    (32768, 64, 512): (1, 0, 1, 0, 0, 1, (256, 64)),     # 128 tall tiles unsplit
+    (200, 64, 8192): (8, 1, 32, 1, 0, 1, (64, 64)),
+    (131072, 16, 64): (1, 0, 1, 0, 0, 1, (128, 64)),     # two K slices: 128 x 64 tiles
     # 33 to 64 rows: 64 x 256 tiles against 64 x 128, fastest on GB300 in each
     # row (us): 220.0 for 64 x 128 split 4 against 199.0 here; 114.7 (split 2)
-    # against 104.5; 434.9 (split 8) against 385.5; 112.8 against 104.4; 120.4
-    # against 111.3; 64.5 here against 108.8 (16 wide tiles); 20.6 here
-    # against 30.9.
-    (64, 8192, 8192): (8, 0, 7, 0, 0, 1, 2),
-    (64, 16384, 2048): (4, 0, 1, 0, 0, 1, 2),
-    (64, 16384, 8192): (4, 0, 7, 0, 0, 1, 2),
-    (64, 2048, 8192): (8, 1, 19, 1, 0, 1, 2),
-    (40, 8192, 4096): (8, 0, 7, 0, 0, 1, 2),
-    (48, 4096, 4096): (8, 0, 19, 0, 0, 1, 0),
-    (64, 4096, 1024): (4, 0, 4, 0, 0, 1, 0),
-    (64, 65536, 512): (1, 0, 1, 0, 0, 1, 2),       # 256 wide tiles unsplit
+    # against 104.5; 434.9 (split 8) against 385.5; 120.4 against 111.3; 64.5
+    # here against 108.8 (16 wide tiles); 20.6 here against 30.9; 64 x 2048 x
+    # 8192 on 64 x 64 tiles 76.6 through gemm_f32 against 105.2 on 64 x 256.
+    (64, 8192, 8192): (8, 0, 7, 0, 0, 1, (64, 256)),
+    (64, 16384, 2048): (4, 0, 1, 0, 0, 1, (64, 256)),
+    (64, 16384, 8192): (4, 0, 7, 0, 0, 1, (64, 256)),
+    (40, 8192, 4096): (8, 0, 7, 0, 0, 1, (64, 256)),
+    (48, 4096, 4096): (8, 0, 19, 0, 0, 1, (64, 128)),
+    (64, 4096, 1024): (4, 0, 4, 0, 0, 1, (64, 128)),
+    (64, 2048, 8192): (8, 0, 19, 1, 0, 1, (64, 64)),
+    (64, 65536, 512): (1, 0, 1, 0, 0, 1, (64, 256)),     # 256 wide tiles unsplit
 }
 
 
@@ -84,7 +87,7 @@ def test_planner_choices(driver):
     for line in r.stdout.splitlines():
         f = line.split()
         got[(int(f[0]), int(f[1]), int(f[2]))] = (int(f[4]), int(f[5]), int(f[7]), int(f[8]),
-                                                   int(f[10]), int(f[11]), int(f[13]))
+                                                   int(f[10]), int(f[11]), (int(f[13]), int(f[14])))
     for shape, want in EXPECT.items():
         assert got[shape] == want, (shape, got[shape], want)
 

@@ -45,7 +45,7 @@ def call_noalloc(f, A, B):
     return C
 
 
-@pytest.mark.parametrize("M,N,K", [(512, 512, 8192), (2000, 60, 2000)])
+@pytest.mark.parametrize("M,N,K", [(512, 512, 8192), (48, 2048, 8192)])
 def test_noalloc_matches_workspace_entry_point_two_calls(noalloc, M, N, K):
     need = rtm.gemm_f32_workspace_bytes(M, N, K)
     assert 0 < need <= SCRATCH_BYTES, "the shape uses the built-in scratch"
