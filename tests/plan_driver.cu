@@ -1,5 +1,6 @@
-// Test driver (host code only): prints the fp32 schedule planners' choices for
-// the shapes given on the command line as M,N,K triples, for a 152-SM GPU whose
+// Test driver (host code only): prints the fp32 schedule planners' choices
+// (splits, spread, tile shape and K chunks) for the shapes given on the command
+// line as M,N,K triples, for a 152-SM GPU whose
 // cluster-split CTAs fit 76 clusters of 2, 36 of 4 and 15 of 8 at one CTA per
 // SM (the occupancy the library queries on GB300); with "pair" first, the
 // CTA-pair kernel's K-split choice instead. Built and run by
@@ -31,9 +32,10 @@ int main(int argc, char **argv)
         const bool ws_wins = w.splits > 1 && !(cluster_est < w_est);
         const rtm::TailPlan t = rtm::sgemm_tail_plan(M, N, K, sms);
         const rtm::SimtTile tile = rtm::simt_resolve_tile(c.tile, M, N);
-        std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d tile %d %d\n", M, N, K,
-                    c.splits, c.spread ? 1 : 0, w.splits, ws_wins ? 1 : 0, t.plain_tiles,
-                    t.tail.splits, tile.m, tile.n);
+        std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d tile %d %d "
+                    "chunks %d %d %d\n",
+                    M, N, K, c.splits, c.spread ? 1 : 0, w.splits, ws_wins ? 1 : 0, t.plain_tiles,
+                    t.tail.splits, tile.m, tile.n, c.kchunk, w.kchunk, t.tail.kchunk);
     }
     return 0;
 }

@@ -92,6 +92,52 @@ def test_planner_choices(driver):
         assert got[shape] == want, (shape, got[shape], want)
 
 
+def _shape_grid():
+    dims = [1, 7, 33, 64, 65, 100, 128, 129, 200, 256, 257, 500, 1000, 1024, 2047, 4096, 8192,
+            20000]
+    ks = [1, 31, 32, 33, 96, 97, 200, 1000, 4096, 8193]
+    return [(m, n, k) for m in dims for n in dims for k in ks]
+
+
+def test_planner_invariants_over_a_grid(driver):
+    """Every plan the fp32 planners make over a grid of 3240 shapes is one the
+    launchers accept: a cluster size of 1, 2, 4 or 8 that divides the tile
+    height, a tile shape the kernel is built for (256 x 64 only for N <= 64,
+    64 x 256 only for M <= 64), K chunks of whole 32-deep slices that cover K
+    with none empty, one CTA per SM only for clusters of 8, at most 32
+    workspace chunks, and a tail split only after whole waves of 304 slots."""
+    shapes = _shape_grid()
+    args = [str(x) for shape in shapes for x in shape]
+    r = subprocess.run([driver, *args], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = r.stdout.splitlines()
+    assert len(lines) == len(shapes)
+    shapes_ok = {(128, 128), (128, 64), (64, 128), (64, 64), (256, 64), (64, 256)}
+
+    def chunks_ok(splits, chunk, K):
+        if splits == 1:
+            return True
+        return chunk % 32 == 0 and splits * chunk >= K and (splits - 1) * chunk < K
+
+    for line in lines:
+        f = line.split()
+        M, N, K = int(f[0]), int(f[1]), int(f[2])
+        cs, spread, ws, plain_tiles, ts = int(f[4]), int(f[5]), int(f[7]), int(f[10]), int(f[11])
+        tm, tn = int(f[13]), int(f[14])
+        cchunk, wchunk, tchunk = int(f[16]), int(f[17]), int(f[18])
+        where = f"{M}x{N}x{K}: {line}"
+        assert cs in (1, 2, 4, 8) and tm % cs == 0, where
+        assert (tm, tn) in shapes_ok, where
+        assert tm != 256 or N <= 64, where
+        assert tn != 256 or M <= 64, where
+        assert chunks_ok(cs, cchunk, K), where
+        assert spread == 0 or cs == 8, where
+        assert 1 <= ws <= 32 and chunks_ok(ws, wchunk, K), where
+        assert ts in (1, 4), where
+        if ts == 4:
+            assert plain_tiles % 304 == 0 and chunks_ok(ts, tchunk, K) and M > 64 and N > 64, where
+
+
 # CTA-pair kernel (bf16/fp16, M > 128): (tiles, resident pairs, 64-deep K blocks,
 # C rows on 16-byte boundaries) -> first tile whose K is split in two.
 PAIR_EXPECT = {
