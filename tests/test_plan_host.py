@@ -161,6 +161,31 @@ def test_pair_split_choices(driver):
     assert got == PAIR_EXPECT
 
 
+def test_pair_split_invariants_over_a_grid(driver):
+    """For every (tiles, pairs, K-blocks, aligned C) on a grid: the split tiles
+    are a suffix of the tile order; none split without aligned C or with K
+    halves under 32 blocks; either every tile splits (the tiles fill at most
+    half the pairs) or only the last round's tiles do, and then that round is
+    at most half full, so its 2 x tail half-length units fit in one round."""
+    keys = [(t, p, kb, cv) for t in list(range(1, 200)) + [255, 256, 576, 988, 1024, 4096]
+            for p in (1, 38, 76) for kb in (1, 32, 63, 64, 65, 128) for cv in (0, 1)]
+    args = ["pair"] + [str(x) for key in keys for x in key]
+    r = subprocess.run([driver, *args], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    got = {tuple(int(x) for x in l.split()[:4]): int(l.split()[-1]) for l in r.stdout.splitlines()}
+    assert len(got) == len(keys)
+    for (t, p, kb, cv), sf in got.items():
+        where = (t, p, kb, cv, sf)
+        assert 0 <= sf <= t, where
+        if not cv or kb < 64:
+            assert sf == t, where
+        split = t - sf
+        if split and sf:
+            assert sf % p == 0 and 2 * split <= p, where   # the last round only
+        if split and not sf:
+            assert 2 * t <= p, where                       # every tile, all at once
+
+
 def test_schedule_kinds_cover_the_planner_outcomes():
     """Every outcome above has a name in the binding's schedule kinds."""
     assert set(rtm.F32_KINDS.values()) >= {"tiles", "tiles+cluster-split", "tiles+workspace-split",
