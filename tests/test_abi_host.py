@@ -3,6 +3,7 @@ symbol that include/gemm.h declares, and rejects bad arguments on the host
 before any CUDA call. No kernel is launched here (there is no GPU)."""
 
 import ctypes
+import os
 import shutil
 import subprocess
 
@@ -134,6 +135,15 @@ def test_f32_schedule_host_checks(lib):
     assert f(0, 8, 8, 0, ctypes.byref(kind), ctypes.byref(splits)) == 0
     assert (kind.value, splits.value) == (0, 1)  # GEMM_F32_NO_KERNEL
     assert f(8, 8, 0, 1, ctypes.byref(kind), None) == 0 and kind.value == 0
+
+
+def test_f32_schedule_kinds_match_the_header():
+    """The binding names exactly the values of gemm_f32_kind in include/gemm.h."""
+    import re
+    text = open(os.path.join(rtm.native_build.INCLUDE, "gemm.h")).read()
+    enum = text[text.index("typedef enum gemm_f32_kind"):text.index("} gemm_f32_kind;")]
+    values = {int(v) for v in re.findall(r"GEMM_F32_\w+\s*=\s*(\d+)", enum)}
+    assert values == set(rtm.F32_KINDS), (sorted(values), sorted(rtm.F32_KINDS))
 
 
 def _ceil256(x):
