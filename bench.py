@@ -606,6 +606,37 @@ def run_configs(args) -> Optional[Dict]:
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / args.steps
 
+    def timed_graph(fn):
+        """Per-call time with the calls replayed from a CUDA graph: the device
+        time without the binding's host cost per call, which bounds small
+        products called back to back from Python. None if capture fails."""
+        calls = max(1, min(args.steps, 20))
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                fn()  # per-device caches filled outside the capture
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(calls):
+                    fn()
+            graph.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            reps = 3
+            e0.record()
+            for _ in range(reps):
+                graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / (reps * calls)
+        except RuntimeError:
+            torch.cuda.synchronize()
+            return None
+
     if args.shapes:
         todo = []
         for i, spec in enumerate(args.shapes.split(",")):
@@ -643,6 +674,7 @@ def run_configs(args) -> Optional[Dict]:
                                 float(peaks["bf16_tflops"])))
         for entry, fn, peak in entries:
             ms = timed(fn)
+            ms_graph = timed_graph(fn)
             tf = w.flops / ms / 1e9
             # Binding roofline of this product: the larger of its compute time
             # at the peak and its algorithmic bytes at the measured copy bandwidth.
@@ -654,7 +686,10 @@ def run_configs(args) -> Optional[Dict]:
                          "ms": round(ms, 4), "tflops": round(tf, 2),
                          "frac_of_peak": round(tf / peak, 4),
                          "bound": "compute" if t_compute >= t_memory else "hbm",
-                         "roof_ms": round(roof_ms, 4), "frac_of_roofline": round(roof_ms / ms, 4)})
+                         "roof_ms": round(roof_ms, 4), "frac_of_roofline": round(roof_ms / ms, 4),
+                         "ms_graph": None if ms_graph is None else round(ms_graph, 4),
+                         "frac_of_roofline_graph": (None if ms_graph is None
+                                                    else round(roof_ms / ms_graph, 4))})
         del A, B, C
         torch.cuda.empty_cache()
     if rtm.get_device_error() != 0:
