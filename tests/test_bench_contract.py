@@ -65,3 +65,18 @@ def test_our_arm_line():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     c = d["clocks"]
     assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)
+
+
+@pytest.mark.gpu
+def test_configs_line_reports_binding_and_graph_times():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--configs", "--steps", "5",
+                        "--warmup", "3", "--shapes", "256x256x256:f32,512x512x512:bf16"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    rows = json.loads(lines[0])["configs"]
+    assert [row["entry"].split(" ")[0] for row in rows] == ["gemm_f32", "gemm_bf16f32"]
+    for row in rows:
+        assert row["ms"] > 0 and row["ms_graph"] is not None and row["ms_graph"] > 0
+        assert row["frac_of_roofline_graph"] > 0
