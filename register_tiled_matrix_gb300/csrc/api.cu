@@ -312,6 +312,19 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
 } // namespace
 
 namespace rtm {
+int check_f32_args(int64_t M, int64_t N, int64_t K, const float *A, const float *B, const float *C,
+                   bool *nothing_to_do)
+{
+    const int st = check_common(M, N, K, A, B, C, 4, nothing_to_do);
+    if (st != GEMM_OK || *nothing_to_do)
+        return st;
+    if ((reinterpret_cast<uintptr_t>(C) & 3) != 0 ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3) != 0 ||
+                   (reinterpret_cast<uintptr_t>(B) & 3) != 0)))
+        return GEMM_ERR_ALIGNMENT;
+    return GEMM_OK;
+}
+
 cudaError_t launch_zero_fill(float *C, int64_t count, cudaStream_t stream)
 {
     if (count <= 0)

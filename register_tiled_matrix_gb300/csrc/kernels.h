@@ -223,6 +223,12 @@ cudaError_t launch_gemm_tc_t(const TcLaunch &p, int splits, bool swap, cudaStrea
 // operands loaded by producer warps instead of TMA. mute_producer unused.
 cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);
 
+// The host-side argument checks of the fp32 entry points (api.cu), made
+// before any CUDA call: GEMM_OK with *nothing_to_do set when M or N is zero,
+// else GEMM_OK or the status the entry points return for these arguments.
+int check_f32_args(int64_t M, int64_t N, int64_t K, const float *A, const float *B, const float *C,
+                   bool *nothing_to_do);
+
 // C[0 .. count) = 0 (the K == 0 product).
 cudaError_t launch_zero_fill(float *C, int64_t count, cudaStream_t stream);
 

@@ -24,28 +24,21 @@ constexpr int64_t kScratchBytes = 24ll << 20;  // 24 MiB per device
 
 // The scratch: every partial product slab of a call lives here. Its contents
 // persist from one call to the next; a call writes every element it later
-// reads, so nothing needs clearing, but two calls in flight on the GPU at the
-// same time (for example on two streams) race on it.
+// reads before reading it, so nothing needs clearing, but two calls in flight
+// on the GPU at the same time (for example on two streams) race on it.
 static __device__ __align__(256) float g_noalloc_scratch[kScratchBytes / sizeof(float)];
 
 namespace {
 
 constexpr int kMaxDevices = 64;
 
-struct ScratchInfo {
-    bool ready = false;
-    float *ptr = nullptr;  // device address of g_noalloc_scratch on this device
-    int sms = 0;
-    int cc = 0;
-};
-
 std::mutex g_scratch_mutex;
-ScratchInfo g_scratch[kMaxDevices];
+float *g_scratch_ptr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
 
 // Set-up, once per device, with that device current: look up the device
 // address of the scratch array (in host code the array's name is only a
-// stand-in for it) and the SM count the split plan depends on.
-int scratch_for_current_device(ScratchInfo *out)
+// stand-in for it, not an address the GPU can use).
+int scratch_for_current_device(float **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -53,35 +46,16 @@ int scratch_for_current_device(ScratchInfo *out)
         return GEMM_ERR_LAUNCH;
     }
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    ScratchInfo &s = g_scratch[dev];
-    if (!s.ready) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
+    if (!g_scratch_ptr[dev]) {
         float *ptr = nullptr;
         if (cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
-        s.ptr = ptr;
-        s.sms = sms;
-        s.cc = major * 10 + minor;
-        s.ready = true;
+        g_scratch_ptr[dev] = ptr;
     }
-    *out = s;
-    return s.cc == 103 ? GEMM_OK : GEMM_ERR_DEVICE;
-}
-
-bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes)
-{
-    if (!a || !b || a_bytes <= 0 || b_bytes <= 0)
-        return false;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + (uintptr_t)b_bytes && b0 < a0 + (uintptr_t)a_bytes;
+    *out = g_scratch_ptr[dev];
+    return GEMM_OK;
 }
 
 } // namespace
@@ -89,49 +63,17 @@ bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_byt
 extern "C" int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
                                 float *C, void *stream)
 {
-    constexpr int64_t kMaxDim = 0x7fffffff;
-    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-        return GEMM_ERR_INVALID_ARG;
-    if (M == 0 || N == 0)
-        return GEMM_OK;
-    if (!C || (K > 0 && (!A || !B)))
-        return GEMM_ERR_INVALID_ARG;
-    if (M * N > (int64_t)1 << 52 || M * K > (int64_t)1 << 52 || K * N > (int64_t)1 << 52)
-        return GEMM_ERR_INVALID_ARG;
-    if (K > 0 && (ranges_overlap(C, M * N * 4, A, M * K * 4) ||
-                  ranges_overlap(C, M * N * 4, B, K * N * 4)))
-        return GEMM_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(C) & 3) != 0 ||
-        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3) != 0 ||
-                   (reinterpret_cast<uintptr_t>(B) & 3) != 0)))
-        return GEMM_ERR_ALIGNMENT;
-
-    ScratchInfo sc;
-    int st = scratch_for_current_device(&sc);
+    // The same host-side checks as gemm_f32, before any CUDA call.
+    bool nothing = false;
+    int st = rtm::check_f32_args(M, N, K, A, B, C, &nothing);
+    if (st != GEMM_OK || nothing)
+        return st;
+    float *scratch = nullptr;
+    st = scratch_for_current_device(&scratch);
     if (st != GEMM_OK)
         return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (K == 0) {
-        e = rtm::launch_zero_fill(C, M * N, s);
-    } else if (M <= rtm::kShortMaxM) {
-        // Short, wide products split K over CTA clusters and need no scratch.
-        e = rtm::launch_sgemm_short((int)M, (int)N, (int)K, A, B, C,
-                                    rtm::sgemm_short_splits((int)M, (int)N, (int)K, sc.sms), s);
-    } else {
-        const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, sc.sms);
-        const rtm::SplitK &plan = f.workspace;
-        if (plan.splits <= 1) {
-            e = rtm::launch_sgemm_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, sc.sms, s);
-        } else {
-            if ((int64_t)plan.splits * M * N * (int64_t)sizeof(float) > kScratchBytes)
-                return GEMM_ERR_INVALID_ARG;  // needs more than the fixed 24 MiB of scratch
-            e = rtm::launch_sgemm_f32_splitk((int)M, (int)N, (int)K, A, B, C, plan, sc.ptr, s);
-        }
-    }
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
-    }
-    return GEMM_OK;
+    // gemm_f32_ws over the built-in array: it splits K through the array when
+    // the split fits in it, and otherwise runs gemm_f32's schedule (K split over
+    // cluster CTAs, or none), which needs no scratch at all.
+    return gemm_f32_ws(M, N, K, A, B, C, scratch, kScratchBytes, stream);
 }
