@@ -54,13 +54,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of each kernel, keyed to the kernel source it was taken on;
-# reported as null once the source changes. See profiles/.
+# reported as null once the source changes.
 TRAFFIC = {
-    "gemm_f32": {"bytes": 395077120, "source_sha1": "309203ed1ae2e0a8ada0c4e71a8b56d4851365c8",
-                 "profile": "profiles/gemm_f32_4096_sgemm_rt_kernel.md"},
+    "gemm_f32": {"bytes": 395077120, "source_sha1": "309203ed1ae2e0a8ada0c4e71a8b56d4851365c8"},
     "gemm_bf16f32": {"bytes": 1365153024,
-                     "source_sha1": "2564a8cd5cb12f0cd75e69661170f865254c938a",
-                     "profile": "profiles/gemm_bf16f32_8192_tc_kernel.md"},
+                     "source_sha1": "2564a8cd5cb12f0cd75e69661170f865254c938a"},
 }
 KERNEL_SOURCE = {
     "gemm_f32": "register_tiled_matrix_gb300/csrc/sgemm_simt.cu",
@@ -116,27 +114,86 @@ def barrier():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """Samples the SM clock, power and clock-event reasons of one GPU during a
+    timed region, read-only: through NVML (libnvidia-ml, every `period_ms`)
+    where it loads, else through `nvidia-smi -lms`."""
+
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    # NVML clock-event reason bits (nvml.h: nvmlClocksEventReason*)
+    NVML_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                 "hw_thermal_slowdown": 0x40}
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
+    def __init__(self, gpu_index: int, period_ms: int = 10, uuid: Optional[str] = None):
         self.gpu_index = gpu_index
         self.period_ms = period_ms
+        self.uuid = uuid
+        self.samples: List[tuple] = []  # (sm_mhz, max_mhz, power_w, reason bits)
         self.lines: List[str] = []
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
+        self.source = None
+
+    def _nvml(self):
+        import ctypes
+
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if nv.nvmlInit_v2() != 0:
+            return None
+        handle = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            for u in (self.uuid, "GPU-" + self.uuid):
+                if nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(handle)) == 0:
+                    ok = True
+                    break
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(self.gpu_index, ctypes.byref(handle)) != 0:
+            return None
+        reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or getattr(
+            nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        return nv, handle, reasons
+
+    def _nvml_loop(self, nv, handle, reasons):
+        import ctypes
+
+        sm, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM = 1
+        while not self.stop_flag.is_set():
+            if nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(sm)) == 0:
+                power = mw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(handle, ctypes.byref(mw)) == 0 \
+                    else None
+                bits = rs.value if reasons is not None and reasons(handle, ctypes.byref(rs)) == 0 \
+                    else 0
+                self.samples.append((float(sm.value), float(mx.value), power, bits))
+            self.stop_flag.wait(self.period_ms / 1e3)
 
     def start(self):
+        nvml = None
+        try:
+            nvml = self._nvml()
+        except (OSError, AttributeError):
+            nvml = None
+        if nvml is not None:
+            self.source = f"nvml every {self.period_ms} ms"
+            self.thread = threading.Thread(target=self._nvml_loop, args=nvml, daemon=True)
+            self.thread.start()
+            time.sleep(0.05)
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", str(self.period_ms), "-i", str(self.gpu_index)],
+                 "-lms", str(max(self.period_ms, 20)), "-i", str(self.gpu_index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
             return
+        self.source = f"nvidia-smi every {max(self.period_ms, 20)} ms"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
         time.sleep(0.3)  # let the first sample land before the timed region
@@ -146,18 +203,28 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self) -> Dict:
-        if self.proc is None:
+        if self.source is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
+                    "note": "neither NVML nor nvidia-smi available"}
+        self.stop_flag.set()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
         sm, mx, pw = [], [], []
         active = set()
+        for (s_mhz, m_mhz, p_w, bits) in self.samples:
+            sm.append(s_mhz)
+            mx.append(m_mhz)
+            if p_w is not None:
+                pw.append(p_w)
+            for name, bit in self.NVML_BITS.items():
+                if bits & bit:
+                    active.add(name)
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
@@ -174,9 +241,12 @@ class ClockSampler:
         return {
             "sm_mhz": statistics.median(sm) if sm else None,
             "sm_max_mhz": max(mx) if mx else None,
+            "sm_mhz_min": min(sm) if sm else None,
             "reasons": sorted(active),
             "samples": len(sm),
+            "power_w_median": statistics.median(pw) if pw else None,
             "power_w_max": max(pw) if pw else None,
+            "source": self.source,
         }
 
 
@@ -282,11 +352,21 @@ def run_ours(args) -> Optional[Dict]:
         raise SystemExit("device error during warm-up")
 
     # ---- timed region: K steps, inputs resident in HBM
+    # The FP32 pipes' own throughput on this GPU (the denominator of gemm_f32's
+    # roofline), measured before the timed region: independent FMA chains, no
+    # memory traffic, scalar and packed forms.
+    fp32_measured = None
+    if "gemm_f32" in {kernel_of(it["w"]) for it in items} and not args.no_peak:
+        fp32_measured = {"scalar": rtm.fp32_pipe_peak(iters=5000, packed=False),
+                         "packed": rtm.fp32_pipe_peak(iters=5000, packed=True)}
+        torch.cuda.synchronize(device)
+
     per_kernel = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in items] for _ in range(args.steps)]
     e_all0 = torch.cuda.Event(enable_timing=True)
     e_all1 = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(device)
+    clocks = ClockSampler(torch.cuda.current_device(), uuid=str(getattr(props, "uuid", "") or ""))
     clocks.start()
     barrier()
     torch.cuda.synchronize(device)
@@ -313,7 +393,7 @@ def run_ours(args) -> Optional[Dict]:
                                  "min": min(ts)}
 
     # ---- end to end: host buffers, copies inside the timed region
-    e2e_steps = 0 if args.no_e2e else max(3, args.steps // 5)
+    e2e_steps = 0 if args.no_e2e else args.steps
     h2d = sum(it["A_host"].numel() * it["A_host"].element_size()
               + it["B_host"].numel() * it["B_host"].element_size() for it in items)
     d2h = sum(it["C_host"].numel() * 4 for it in items)
@@ -381,7 +461,20 @@ def run_ours(args) -> Optional[Dict]:
     peaks = load_peaks()
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     max_mhz = float(peaks.get("sm_max_mhz") or FALLBACK_PEAKS["sm_max_mhz"])
-    fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    fp32_derived = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    # gemm_f32's roofline peak: the faster of the two measured FMA forms (the
+    # pipes' own ceiling on this GPU); the derived figure when not measured.
+    if fp32_measured is not None:
+        fp32_peak = max(fp32_measured["scalar"]["tflops"], fp32_measured["packed"]["tflops"])
+        fp32_note = ("measured on this GPU before the timed region: best of scalar and packed "
+                     "FP32 FMA chains (gemm_fp32_pipe_peak), "
+                     f"{fp32_measured['scalar']['tflops']:.2f} / "
+                     f"{fp32_measured['packed']['tflops']:.2f} TFLOP/s at "
+                     f"{fp32_measured['scalar']['sm_mhz']:.0f} MHz")
+    else:
+        fp32_peak = fp32_derived
+        fp32_note = (f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x "
+                     f"{max_mhz:.0f} MHz")
     # The step alternates an FP32-pipe product with the tensor-core product and
     # does not reach the power cap (the clock record shows it), so the tensor
     # product is compared with the burst bf16 figure; the power-capped
@@ -396,8 +489,7 @@ def run_ours(args) -> Optional[Dict]:
         ms = kernel_ms[it["name"]]["mean"]
         achieved = w.flops / (ms / 1e3) / 1e12
         if kern == "gemm_f32":
-            bound, peak, peak_note = "alu", fp32_peak, (
-                f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {max_mhz:.0f} MHz")
+            bound, peak, peak_note = "alu", fp32_peak, fp32_note
         else:
             bound, peak, peak_note = "tensor", bf16_peak, (
                 f"{peaks['source']} dense bf16 burst (cuBLAS 8192^3); clocks stay at max in "
@@ -414,6 +506,11 @@ def run_ours(args) -> Optional[Dict]:
         }
         if kern == "gemm_bf16f32":
             rooflines[kern]["frac_of_sustained"] = round(achieved / bf16_sustained, 4)
+        else:
+            rooflines[kern]["frac_of_derived"] = round(achieved / fp32_derived, 4)
+            if fp32_measured is not None:
+                rooflines[kern]["frac_of_scalar_ffma"] = round(
+                    achieved / fp32_measured["scalar"]["tflops"], 4)
     dominant = max(items, key=lambda it: kernel_ms[it["name"]]["mean"])
     out = {
         "metric": METRIC,
@@ -439,6 +536,14 @@ def run_ours(args) -> Optional[Dict]:
         "gpu_launches_per_call": launch_note,
         "clocks": clock_summary,
         "peaks": {"source": peaks["source"], "fp32_simt_tflops": round(fp32_peak, 2),
+                  "fp32_simt_tflops_measured": (round(fp32_peak, 2) if fp32_measured else None),
+                  "fp32_scalar_ffma_tflops_measured": (
+                      round(fp32_measured["scalar"]["tflops"], 2) if fp32_measured else None),
+                  "fp32_packed_ffma_tflops_measured": (
+                      round(fp32_measured["packed"]["tflops"], 2) if fp32_measured else None),
+                  "fp32_peak_sm_mhz": (round(fp32_measured["scalar"]["sm_mhz"], 1)
+                                       if fp32_measured else None),
+                  "fp32_simt_tflops_derived": round(fp32_derived, 2),
                   "bf16_tflops_burst": bf16_peak, "bf16_tflops_sustained": bf16_sustained},
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -496,7 +601,7 @@ def cpu_baseline(names, items=None, budget_s: float = 15.0) -> Dict:
         total_f += fl
         desc.append(f"{count} seeded entries of C for {w.name}")
     return {"value": total_f / total_t / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
-            "kind": "oracle",
+            "cpu_model": cpu_model(), "kind": "oracle",
             "sample": "; ".join(desc) + f" (fp64 dot products of length K, {total_t:.1f} s)"}
 
 
@@ -534,7 +639,7 @@ def run_reference(args) -> Optional[Dict]:
         "data": "synthetic (seeded N(0,1); bf16 inputs rounded to nearest even)",
         "config": step_config(names, 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -588,10 +693,35 @@ def run_configs(args) -> Optional[Dict]:
         raise SystemExit("bench.py --configs needs a CUDA GPU (sm_103a)")
     rtm.build()
     peaks = load_peaks()
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    fp32_peak = sms * FP32_LANES_PER_SM * 2 * float(peaks.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    props = torch.cuda.get_device_properties(0)
+    sms = props.multi_processor_count
+    fp32_derived = sms * FP32_LANES_PER_SM * 2 * float(peaks.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    fp32_measured = {"scalar": rtm.fp32_pipe_peak(iters=5000, packed=False),
+                     "packed": rtm.fp32_pipe_peak(iters=5000, packed=True)}
+    fp32_peak = max(fp32_measured["scalar"]["tflops"], fp32_measured["packed"]["tflops"])
     hbm = float(peaks.get("hbm_gbs") or 6800.0)
     rows = []
+    oracle_rows = []
+    # L2-cold timing: before each timed call, write a buffer twice the L2's size
+    # (outside the timed interval), so the call finds none of its operands in L2.
+    l2_bytes = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device="cuda")
+
+    def timed_cold(fn, reps=None):
+        reps = reps or max(3, min(args.steps, 20))
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
 
     def timed(fn):
         for _ in range(args.warmup):
@@ -674,6 +804,7 @@ def run_configs(args) -> Optional[Dict]:
                                 float(peaks["bf16_tflops"])))
         for entry, fn, peak in entries:
             ms = timed(fn)
+            ms_cold = timed_cold(fn)
             ms_graph = timed_graph(fn)
             tf = w.flops / ms / 1e9
             # Binding roofline of this product: the larger of its compute time
@@ -685,20 +816,101 @@ def run_configs(args) -> Optional[Dict]:
             rows.append({"config": name, "M": w.M, "N": w.N, "K": w.K, "entry": entry,
                          "ms": round(ms, 4), "tflops": round(tf, 2),
                          "frac_of_peak": round(tf / peak, 4),
+                         "l2_cold_ms": round(ms_cold, 4),
+                         "l2_cold_tflops": round(w.flops / ms_cold / 1e9, 2),
                          "bound": "compute" if t_compute >= t_memory else "hbm",
                          "roof_ms": round(roof_ms, 4), "frac_of_roofline": round(roof_ms / ms, 4),
                          "ms_graph": None if ms_graph is None else round(ms_graph, 4),
                          "frac_of_roofline_graph": (None if ms_graph is None
                                                     else round(roof_ms / ms_graph, 4))})
+        if not args.no_oracle and not args.shapes:
+            oracle_rows.append(oracle_timing(w))
         del A, B, C
         torch.cuda.empty_cache()
     if rtm.get_device_error() != 0:
         raise SystemExit("device error in the configs run")
-    return {"metric": "GEMM TFLOP/s per configuration (report only)", "unit": UNIT,
-            "steps": args.steps, "warmup": args.warmup,
-            "peaks": {"fp32_simt_tflops": round(fp32_peak, 2),
-                      "bf16_tflops_burst": float(peaks["bf16_tflops"]), "hbm_gbs": hbm},
-            "l2": "back-to-back launches (L2-warm for the smaller configs)", "configs": rows}
+    out = {"metric": "GEMM TFLOP/s per configuration (report only)", "unit": UNIT,
+           "steps": args.steps, "warmup": args.warmup,
+           "peaks": {"fp32_simt_tflops": round(fp32_peak, 2),
+                     "fp32_simt_tflops_source": "measured (gemm_fp32_pipe_peak, best of scalar "
+                                                "and packed FMA chains)",
+                     "fp32_scalar_ffma_tflops_measured": round(fp32_measured["scalar"]["tflops"], 2),
+                     "fp32_packed_ffma_tflops_measured": round(fp32_measured["packed"]["tflops"], 2),
+                     "fp32_simt_tflops_derived": round(fp32_derived, 2),
+                     "bf16_tflops_burst": float(peaks["bf16_tflops"]), "hbm_gbs": hbm},
+           "l2": ("ms: back-to-back launches (L2-warm for the smaller configs); l2_cold_ms: "
+                  f"median of single launches, each after writing {2 * l2_bytes >> 20} MiB "
+                  "(twice the L2) outside the timed interval"),
+           "configs": rows}
+    if oracle_rows:
+        out["oracle"] = {"cpu_model": cpu_model(), "cores": _oracle_cores(), "rows": oracle_rows}
+    return out
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def _oracle_cores() -> int:
+    import oracle
+
+    oracle.build()
+    return oracle.max_threads()
+
+
+# Products the oracle multiplies in full when timed (M*N*K <= 2^31); larger
+# ones are timed on sampled entries and extrapolated to the full product by
+# their rate per multiply-add.
+ORACLE_FULL_MACS = 1 << 31
+
+
+def oracle_timing(w, sample_count: int = 4096) -> Dict:
+    """The oracle, as it stands, on one configuration: one thread and all host
+    cores; the whole product where M*N*K <= 2^31, else sampled entries of C
+    with the full-product time extrapolated from their rate."""
+    import oracle
+
+    oracle.build()
+    A, B = workloads.workload_inputs(w)
+    macs = w.M * w.N * w.K
+    row = {"config": w.name, "M": w.M, "N": w.N, "K": w.K, "cores": oracle.max_threads()}
+    if macs <= ORACLE_FULL_MACS:
+        for label, threads in (("one_thread_s", 1), ("all_cores_s", 0)):
+            t0 = time.perf_counter()
+            oracle.gemm(A, B, threads=threads)
+            row[label] = round(time.perf_counter() - t0, 4)
+        row["kind"] = "full product"
+    else:
+        rows_i, cols_i = workloads.sample_indices(w.M, w.N, count=sample_count, seed=w.seed + 5,
+                                                  edge_count=0)
+        rows_i, cols_i = rows_i[:sample_count], cols_i[:sample_count]
+        sampled_macs = len(rows_i) * w.K
+        for label, threads in (("one_thread_s", 1), ("all_cores_s", 0)):
+            t0 = time.perf_counter()
+            oracle.gemm_sampled(A, B, rows_i, cols_i, threads=threads)
+            dt = time.perf_counter() - t0
+            row[label + "_sampled"] = round(dt, 4)
+            row[label] = round(dt * macs / sampled_macs, 2)
+        row["kind"] = (f"extrapolated from {len(rows_i)} sampled entries of C "
+                       "(time per multiply-add x M*N*K)")
+    return row
 
 
 def main(argv=None):
@@ -709,6 +921,9 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--no-peak", action="store_true",
+                   help="skip the FP32 pipe measurement (gemm_f32's roofline then uses the "
+                        "derived peak)")
     p.add_argument("--only", choices=["gemm_f32", "gemm_bf16f32"], default=None,
                    help="time one entry point's product instead of the whole step")
     p.add_argument("--cpu-budget", type=float, default=15.0,
@@ -722,6 +937,8 @@ def main(argv=None):
                    help="time every configuration's product (report only)")
     p.add_argument("--config-names", default=None,
                    help="comma-separated workload names for --configs (default: all)")
+    p.add_argument("--no-oracle", action="store_true",
+                   help="--configs without the oracle's CPU timings")
     p.add_argument("--shapes", default=None,
                    help="--configs on these products instead, e.g. 16x8192x8192:bf16,4096x4096x4096:f32")
     args = p.parse_args(argv)

@@ -109,10 +109,11 @@ GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K,
 /*
  * gemm_f32_schedule — how an M x N x K fp32 product would be computed on the
  * current device: by gemm_f32 when use_workspace == 0, by gemm_f32_ws with a
- * workspace of gemm_f32_workspace_bytes (and by gemm_f32_noalloc) when
- * use_workspace != 0. Launches nothing. Writes *kind (one of the values
- * below) and *splits (the number of K chunks; 1 when K is not split); either
- * pointer may be null. Returns GEMM_OK, GEMM_ERR_INVALID_ARG for sizes the
+ * workspace of gemm_f32_workspace_bytes when use_workspace != 0 (also what
+ * gemm_f32_noalloc runs when that many bytes are at most its 24 MiB; above
+ * that it runs the use_workspace == 0 schedule). Launches nothing. Writes
+ * *kind (one of the values below) and *splits (the number of K chunks; 1 when
+ * K is not split); either pointer may be null. Returns GEMM_OK, GEMM_ERR_INVALID_ARG for sizes the
  * entry points reject, or GEMM_ERR_LAUNCH / GEMM_ERR_DEVICE when no usable
  * device is current. Products with M == 0, N == 0 or K == 0 report
  * GEMM_F32_NO_KERNEL.
@@ -181,17 +182,20 @@ GEMM_API int gemm_f32_ws(int64_t M, int64_t N, int64_t K,
  * library (every GPU that loads the library holds it until the process
  * exits). The register-tiling pages have no counterpart of this entry point.
  *
- * Same arguments, layout, ownership, degenerate-shape and alignment rules as
- * gemm_f32. Products that need no split run gemm_f32's schedule; products
- * whose split needs more than 24 MiB (splits * M * N * 4 bytes, see
- * gemm_f32_workspace_bytes) are rejected with GEMM_ERR_INVALID_ARG.
+ * Same arguments, layout, ownership, degenerate-shape, alignment and error
+ * rules as gemm_f32 (argument errors are reported before any CUDA call). It
+ * runs what gemm_f32_ws runs with the built-in array as its workspace: the
+ * split-K schedule when that split fits in 24 MiB (splits * M * N * 4 bytes,
+ * see gemm_f32_workspace_bytes), and otherwise gemm_f32's own schedule, which
+ * needs no scratch memory. Every valid product therefore succeeds.
  *
  * The first call on each device looks up the device address of the built-in
  * array (cudaGetSymbolAddress, with that device current); make that first
  * call before any stream capture. All calls on a device share the array:
  * its contents persist between calls, nothing in it needs to start at zero
- * (a call writes every element it reads), and two calls whose work overlaps
- * on the GPU (for example on two streams) race on it.
+ * (a call writes every element of it that it reads, before reading it), and
+ * two calls whose work overlaps on the GPU (for example on two streams) race
+ * on it.
  */
 GEMM_API int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
                               const float *A, const float *B, float *C, void *stream);
@@ -324,6 +328,28 @@ GEMM_API int gemm_get_device_error(void *stream);
 GEMM_API int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K,
                                            const uint16_t *A, const uint16_t *B, float *C,
                                            int64_t wait_limit_ns, void *stream);
+
+/*
+ * gemm_fp32_pipe_peak — measurement of the FP32 FMA pipes that gemm_f32's
+ * register tiles feed ("GPU架构基础", the SM and CUDA-core section: the FP32
+ * cores of an SM), used as the measured denominator of gemm_f32's roofline.
+ * Launches, on `stream`, 4 CTAs of 256 threads per SM, each thread running
+ * 16 independent chains of `iters` x 32 dependent FMAs x <- x * a + b on
+ * registers only (no memory traffic); with `packed` != 0 the same chains go
+ * through the packed two-wide FP32 FMA. Writes the launch's floating-point
+ * operation count (2 per FMA) to *flops on the host before returning. The
+ * kernel raises clock_out[0] to the largest number of SM clock cycles and
+ * clock_out[1] to the largest number of global-timer nanoseconds any CTA
+ * spent (atomic maxima; clock_out is a device array of two 8-byte-aligned
+ * unsigned 64-bit values that the caller zeroes first), so that
+ * clock_out[0] / clock_out[1] is the SM clock in GHz during the run. The
+ * caller times the launch (CUDA events on `stream`). Returns
+ * GEMM_ERR_INVALID_ARG for iters outside [1, 2^40] or null pointers,
+ * GEMM_ERR_ALIGNMENT for a misaligned clock_out, GEMM_ERR_DEVICE when the
+ * current device is not sm_103, GEMM_ERR_LAUNCH when the launch fails.
+ */
+GEMM_API int gemm_fp32_pipe_peak(int64_t iters, int packed, unsigned long long *clock_out,
+                                 double *flops, void *stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 GEMM_API const char *gemm_status_string(int status);

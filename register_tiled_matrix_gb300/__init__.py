@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     gemm_f32_schedule,
     gemm_f32_workspace_bytes,
     F32_KINDS,
+    fp32_pipe_peak,
     gemm_f32_ws,
     get_device_error,
     header_symbols,

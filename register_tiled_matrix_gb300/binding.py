@@ -72,6 +72,9 @@ def load_library() -> ctypes.CDLL:
         lib.gemm_f32_ladder.restype = ctypes.c_int
         lib.gemm_bf16f32_selftest_timeout.argtypes = [i64, i64, i64, p, p, p, i64, p]
         lib.gemm_bf16f32_selftest_timeout.restype = ctypes.c_int
+        lib.gemm_fp32_pipe_peak.argtypes = [i64, ctypes.c_int, p, ctypes.POINTER(ctypes.c_double),
+                                            p]
+        lib.gemm_fp32_pipe_peak.restype = ctypes.c_int
         lib.gemm_get_device_error.argtypes = [p]
         lib.gemm_get_device_error.restype = ctypes.c_int
         lib.gemm_status_string.argtypes = [ctypes.c_int]
@@ -288,3 +291,38 @@ def gemm_bf16f32_selftest_timeout(A: torch.Tensor, B: torch.Tensor, out: torch.T
 def get_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise the stream; return and clear the device error word."""
     return int(load_library().gemm_get_device_error(_stream_handle(stream)))
+
+
+def fp32_pipe_peak(iters: int = 20000, packed: bool = False, repeats: int = 5,
+                   device: Optional[torch.device] = None) -> dict:
+    """Measured throughput of the FP32 FMA pipes (gemm_fp32_pipe_peak).
+
+    Times `repeats` launches with CUDA events on the current stream after one
+    warm-up launch and returns the best: {"tflops", "ms", "sm_mhz"} where
+    sm_mhz is the SM clock the launch ran at (clock cycles over global-timer
+    nanoseconds, read by the kernel)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    lib = load_library()
+    best = None
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        clk = torch.zeros(2, dtype=torch.int64, device=dev)
+        flops = ctypes.c_double(0.0)
+        for r in range(repeats + 1):
+            clk.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            _check(lib.gemm_fp32_pipe_peak(int(iters), 1 if packed else 0, clk.data_ptr(),
+                                           ctypes.byref(flops), int(stream.cuda_stream)))
+            e1.record(stream)
+            stream.synchronize()
+            if r == 0:
+                continue  # warm-up launch
+            ms = e0.elapsed_time(e1)
+            cycles, ns = (int(v) for v in clk.cpu().tolist())
+            res = {"tflops": flops.value / (ms * 1e-3) / 1e12, "ms": ms,
+                   "sm_mhz": (cycles / ns * 1e3) if ns > 0 else None}
+            if best is None or res["tflops"] > best["tflops"]:
+                best = res
+    return best
