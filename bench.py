@@ -61,7 +61,7 @@ TRAFFIC = {
                      "source_sha1": "2564a8cd5cb12f0cd75e69661170f865254c938a"},
 }
 KERNEL_SOURCE = {
-    "gemm_f32": "register_tiled_matrix_gb300/csrc/sgemm_simt.cu",
+    "gemm_f32": "register_tiled_matrix_gb300/csrc/sgemm_tma.cu",  # 4096^3: the TMA-fed tiles
     "gemm_bf16f32": "register_tiled_matrix_gb300/csrc/gemm_tc2.cu",  # M > 128: CTA pairs
 }
 

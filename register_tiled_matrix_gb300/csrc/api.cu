@@ -154,11 +154,17 @@ int64_t padded_copy_bytes(int64_t rows, int64_t cols)
 
 // The register-tiled fp32 product, K split over cluster CTAs when
 // cluster.splits > 1; otherwise, for products with more tiles than SMs, the
-// ragged last wave may be split over clusters (sgemm_tail_plan).
+// ragged last wave may be split over clusters (sgemm_tail_plan). Unsplit
+// 128 x 128 tiles run on the TMA-fed kernel where the operands allow it.
 cudaError_t run_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
-                          const rtm::SplitK &cluster, int sms, cudaStream_t s)
+                          const rtm::SplitK &cluster, const DeviceInfo &d, cudaStream_t s)
 {
-    return rtm::launch_sgemm_f32_tiles(M, N, K, A, B, C, cluster, sms, s);
+    rtm::SimtTma tma;
+    tma.encode_tiled = encode_tiled_fn();
+    tma.err = d.err;
+    tma.wait_limit_ns = kDefaultWaitLimitNs;
+    return rtm::launch_sgemm_f32_tiles(M, N, K, A, B, C, cluster, d.sms, s,
+                                       tma.encode_tiled ? &tma : nullptr);
 }
 
 bool rows_on_16_bytes(const void *base, int64_t cols)
@@ -171,12 +177,13 @@ bool rows_on_16_bytes(const void *base, int64_t cols)
 // register-tiled kernel with 128 x 128 tiles otherwise (64 columns for
 // N <= 64, 64 rows for M <= 64), with K split over the CTAs of a cluster
 // when the product has too few tiles to fill the GPU. K >= 1.
-cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, float *C, int sms,
-                          cudaStream_t s)
+cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, float *C,
+                          const DeviceInfo &d, cudaStream_t s)
 {
     if (M <= rtm::kShortMaxM)
-        return rtm::launch_sgemm_short(M, N, K, A, B, C, rtm::sgemm_short_splits(M, N, K, sms), s);
-    return run_f32_tiles(M, N, K, A, B, C, rtm::sgemm_cluster_schedule(M, N, K, sms), sms, s);
+        return rtm::launch_sgemm_short(M, N, K, A, B, C, rtm::sgemm_short_splits(M, N, K, d.sms),
+                                       s);
+    return run_f32_tiles(M, N, K, A, B, C, rtm::sgemm_cluster_schedule(M, N, K, d.sms), d, s);
 }
 
 // Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
@@ -363,7 +370,7 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, const float *B, fl
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return finish(rtm::launch_zero_fill(C, M * N, s));
-    return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d.sms, s));
+    return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d, s));
 }
 
 int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace, int *kind, int *splits)
@@ -459,12 +466,12 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
     if (K == 0)
         return finish(rtm::launch_zero_fill(C, M * N, s));
     if (M <= rtm::kShortMaxM)
-        return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d.sms, s));
+        return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d, s));
     const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
     const rtm::SplitK &plan = f.workspace;
     const int64_t need = plan.splits > 1 ? (int64_t)plan.splits * M * N * 4 : 0;
     if (need == 0 || workspace_bytes < need)
-        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, d.sms, s));
+        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, d, s));
     if (overlaps(workspace, need, A, M * K * 4) || overlaps(workspace, need, B, K * N * 4) ||
         overlaps(workspace, need, C, M * N * 4))
         return GEMM_ERR_INVALID_ARG;

@@ -96,12 +96,40 @@ int resident_clusters(Kernel kernel, int cluster_size, int threads, size_t smem,
     return n;
 }
 
+// What the TMA-fed SIMT kernel needs from the caller: the driver's
+// cuTensorMapEncodeTiled, the device error word its bounded waits report to,
+// and the wait limit.
+struct SimtTma {
+    void *encode_tiled = nullptr;
+    int *err = nullptr;
+    uint64_t wait_limit_ns = 0;
+};
+// The plain 128 x 128 product with its K slices loaded by TMA (sgemm_tma.cu):
+// tiles 0 .. tile_count - 1 of the grouped raster (tile_count < 0: all).
+// Needs sgemm_tma_eligible: K % 4 == 0, N % 4 == 0, A and B 16-byte aligned.
+// Same sums in the same order as the cp.async kernel (same bits).
+bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B);
+cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const float *B, float *C,
+                                 const SimtTma &tma, long long tile_count, cudaStream_t stream);
+
+// Stream-K over the TMA-fed 128 x 128 tiles (sgemm_tma.cu): `ctas` CTAs take
+// equal ranges of the tiles x K-slices iterations; tiles split between CTAs
+// are added by a fixup kernel in a fixed order (repeatable bit for bit).
+// workspace: sgemm_streamk_workspace_floats(M, N, ctas) floats, 16-byte
+// aligned. Operands as launch_sgemm_f32_tma.
+int64_t sgemm_streamk_workspace_floats(int M, int N, int ctas);
+cudaError_t launch_sgemm_f32_streamk(int M, int N, int K, const float *A, const float *B, float *C,
+                                     const SimtTma &tma, int ctas, float *workspace,
+                                     cudaStream_t stream);
+
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
 // 4-byte-aligned pointers. 1 <= K; M, N >= 1. `tile`: the CTA tile shape
 // (any of SimtTile's; 256 x 64 tiles are taken only when the rows of B lie on
-// 16-byte boundaries, 128 x 64 otherwise).
+// 16-byte boundaries, 128 x 64 otherwise). With `tma` set, 128 x 128 tiles of
+// operands sgemm_tma_eligible accepts run on the TMA-fed kernel.
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream, SimtTile tile = SimtTile{});
+                             cudaStream_t stream, SimtTile tile = SimtTile{},
+                             const SimtTma *tma = nullptr);
 
 // SIMT FP32 product for short, wide shapes (sgemm_short.cu): M <= kShortMaxM,
 // any N and K >= 1, 4-byte-aligned pointers. Each thread keeps one column of
@@ -150,11 +178,15 @@ struct TailPlan {
 };
 TailPlan sgemm_tail_plan(int M, int N, int K, int sm_count);
 cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const float *B, float *C,
-                                  const TailPlan &plan, cudaStream_t stream);
+                                  const TailPlan &plan, cudaStream_t stream,
+                                  const SimtTma *tma = nullptr);
 // The register-tiled product on its own schedule: K split over clusters when
-// cluster.splits > 1, else the tail plan, else the plain product.
+// cluster.splits > 1, else the tail plan, else the plain product (its
+// unsplit 128 x 128 tiles on the TMA-fed kernel when `tma` is set and the
+// operands allow it).
 cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
-                                   const SplitK &cluster, int sm_count, cudaStream_t stream);
+                                   const SplitK &cluster, int sm_count, cudaStream_t stream,
+                                   const SimtTma *tma = nullptr);
 // How gemm_f32_ws (and gemm_f32_noalloc) schedule a product with M > kShortMaxM:
 // the workspace split when the model prices it below the cluster split (ties
 // go to the workspace), else the cluster split or the plain product.

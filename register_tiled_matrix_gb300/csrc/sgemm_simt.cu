@@ -678,11 +678,14 @@ cudaError_t launch_tile(SimtTile tile, int M, int N, int K, const float *A, cons
 } // namespace
 
 cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B, float *C,
-                             cudaStream_t stream, SimtTile tile)
+                             cudaStream_t stream, SimtTile tile, const SimtTma *tma)
 {
     // Without a choice, 64-row tiles for M <= 64 (128-row tiles would be at
     // least half empty) and 64-column tiles for N <= 64.
-    return launch_tile<simt::kPlain>(simt_resolve_tile(tile, M, N), M, N, K, A, B, C, stream);
+    const SimtTile t = simt_resolve_tile(tile, M, N);
+    if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B))
+        return launch_sgemm_f32_tma(M, N, K, A, B, C, *tma, -1, stream);
+    return launch_tile<simt::kPlain>(t, M, N, K, A, B, C, stream);
 }
 
 cudaError_t launch_sgemm_f32_splitk(int M, int N, int K, const float *A, const float *B, float *C,
@@ -783,13 +786,15 @@ cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const 
 }
 
 cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const float *B, float *C,
-                                  const TailPlan &plan, cudaStream_t stream)
+                                  const TailPlan &plan, cudaStream_t stream, const SimtTma *tma)
 {
     using simt::kSplitCluster;
     if (M <= kShortTileM || N <= kNarrowN || plan.tail.splits < 2)
         return cudaErrorInvalidValue;
     cudaError_t e = cudaSuccess;
-    if (plan.plain_tiles > 0)
+    if (plan.plain_tiles > 0 && tma && sgemm_tma_eligible(M, N, K, A, B))
+        e = launch_sgemm_f32_tma(M, N, K, A, B, C, *tma, plan.plain_tiles, stream);
+    else if (plan.plain_tiles > 0)
         e = simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream, 1, 0, false,
                                                                0, plan.plain_tiles);
     if (e != cudaSuccess)
@@ -799,14 +804,15 @@ cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const flo
 }
 
 cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
-                                   const SplitK &cluster, int sm_count, cudaStream_t stream)
+                                   const SplitK &cluster, int sm_count, cudaStream_t stream,
+                                   const SimtTma *tma)
 {
     if (cluster.splits > 1)
         return launch_sgemm_f32_cluster(M, N, K, A, B, C, cluster, stream);
     const TailPlan tail = sgemm_tail_plan(M, N, K, sm_count);
     if (tail.tail.splits > 1)
-        return launch_sgemm_f32_tail(M, N, K, A, B, C, tail, stream);
-    return launch_sgemm_f32(M, N, K, A, B, C, stream, cluster.tile);
+        return launch_sgemm_f32_tail(M, N, K, A, B, C, tail, stream, tma);
+    return launch_sgemm_f32(M, N, K, A, B, C, stream, cluster.tile, tma);
 }
 
 } // namespace rtm
