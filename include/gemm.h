@@ -137,7 +137,11 @@ typedef enum gemm_f32_kind {
                                       16-byte boundaries */
     GEMM_F32_WIDE_TILES = 8,       /* 32 < M <= 64, N > 64: 64 x 256 C tiles (4 x 16
                                       per thread), one CTA per tile */
-    GEMM_F32_WIDE_TILES_CLUSTER = 9 /* the same, K split over the CTAs of a cluster */
+    GEMM_F32_WIDE_TILES_CLUSTER = 9, /* the same, K split over the CTAs of a cluster */
+    GEMM_F32_TILES_STREAM_K = 10   /* gemm_f32_ws only: 128 x 128 tiles, the tiles x
+                                      K-slices iterations cut into equal ranges over
+                                      `splits` CTAs (stream-K); split tiles added by a
+                                      second kernel through the workspace */
 } gemm_f32_kind;
 GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace,
                                int *kind, int *splits);
@@ -147,26 +151,35 @@ GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspac
  * M x N x K product on the current device: 0 when the product has enough C
  * tiles to fill the GPU, or when splitting K over cluster CTAs (which needs
  * no workspace, see gemm_f32) is estimated to be at least as fast (gemm_f32_ws
- * then runs what gemm_f32 runs), otherwise splits * M * N * 4 for the
- * split-K schedule described below. The workspace split can cut K into up to
- * 32 chunks against a cluster's 8, so it wins for long K over few tiles. Returns a
- * negative status on invalid sizes (GEMM_ERR_INVALID_ARG) or when no usable
- * device is current (GEMM_ERR_LAUNCH, GEMM_ERR_DEVICE).
+ * then runs what gemm_f32 runs); otherwise the size of one of the two
+ * workspace schedules below, whichever is estimated faster: splits * M * N * 4
+ * for the K split, (tiles + ctas - 1) * 65536 for stream-K (tiles: the
+ * product's 128 x 128 C tiles; ctas: the `splits` gemm_f32_schedule reports).
+ * Returns a negative status on invalid sizes (GEMM_ERR_INVALID_ARG) or when
+ * no usable device is current (GEMM_ERR_LAUNCH, GEMM_ERR_DEVICE).
  *
  * gemm_f32_ws — the same product as gemm_f32 (same layout, ownership and
  * degenerate-shape rules) for shapes with few C tiles, such as skinny or
- * small products: when workspace_bytes >= gemm_f32_workspace_bytes(M, N, K)
- * > 0, K is split into `splits` chunks (a multiple of 32 deep); each chunk's
- * partial M x N product is written to its own slab of `workspace` (device
- * memory owned by the caller, 4-byte aligned, 16-byte aligned for the
- * vector path, not overlapping A, B or C), and a second kernel adds the slabs
- * into C in increasing chunk order, so results are bit-for-bit reproducible
- * from call to call. Otherwise (no split needed, or the workspace too small)
- * it runs exactly what gemm_f32 runs. The workspace contents on return are
- * unspecified; two calls in flight at once must not share a workspace. The
- * split is the pages' global tiling applied to K as well as to C tiles
- * ("寄存器Tiling跨架构解析", section 1.1: global tiling decides how much work
- * each block gets) and changes only the summation order.
+ * small products, given a workspace of at least gemm_f32_workspace_bytes(M,
+ * N, K) > 0 bytes (device memory owned by the caller, 4-byte aligned, 16-byte
+ * aligned for the vector paths, not overlapping A, B or C):
+ *   - K split: K is cut into `splits` chunks (a multiple of 32 deep); each
+ *     chunk's partial M x N product goes to its own slab of the workspace and
+ *     a second kernel adds the slabs into C in increasing chunk order. Up to
+ *     32 chunks against a cluster's 8: long K over few tiles.
+ *   - stream-K (128 x 128 tiles; K % 4 == 0, N % 4 == 0, A, B and the
+ *     workspace 16-byte aligned, else gemm_f32's schedule runs): the product's
+ *     tiles x 32-deep K-slices are cut into `splits` equal ranges, one per CTA,
+ *     so every SM works the same time; a tile a CTA computes whole goes to C,
+ *     parts of tiles shared by several CTAs go to the workspace and a second
+ *     kernel adds them in increasing K order.
+ * Both give bit-for-bit the same result from call to call. Otherwise (no
+ * workspace schedule planned, or the workspace too small) it runs exactly
+ * what gemm_f32 runs. The workspace contents on return are unspecified; two
+ * calls in flight at once must not share a workspace. The splits are the
+ * pages' global tiling applied to K as well as to C tiles
+ * ("寄存器Tiling跨架构解析", sections 1.1 and 2.4: global tiling decides how much
+ * work each block gets) and change only the summation order.
  */
 GEMM_API int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K);
 GEMM_API int gemm_f32_ws(int64_t M, int64_t N, int64_t K,

@@ -142,7 +142,8 @@ def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = Non
 
 F32_KINDS = {0: "none", 1: "tiles", 2: "tiles+cluster-split", 3: "tiles+workspace-split",
              4: "column-strips", 5: "tiles+tail-cluster-split", 6: "tall-tiles",
-             7: "tall-tiles+cluster-split", 8: "wide-tiles", 9: "wide-tiles+cluster-split"}
+             7: "tall-tiles+cluster-split", 8: "wide-tiles", 9: "wide-tiles+cluster-split",
+             10: "tiles+stream-k"}
 
 
 def gemm_f32_schedule(M: int, N: int, K: int, workspace: bool = False) -> Tuple[str, int]:

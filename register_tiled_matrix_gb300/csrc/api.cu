@@ -392,7 +392,10 @@ int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspace, int *k
             if (use_workspace) {
                 const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
                 cluster = f.cluster;
-                if (f.workspace.splits > 1) {
+                if (f.streamk > 0) {
+                    k = GEMM_F32_TILES_STREAM_K;
+                    s = f.streamk;
+                } else if (f.workspace.splits > 1) {
                     k = GEMM_F32_TILES_WORKSPACE;
                     s = f.workspace.splits;
                 }
@@ -440,7 +443,11 @@ int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
         return st;
     if (M <= rtm::kShortMaxM)
         return 0;  // short, wide products split K without a workspace
-    const rtm::SplitK plan = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms).workspace;
+    const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
+    if (f.streamk > 0)
+        return rtm::sgemm_streamk_workspace_floats((int)M, (int)N, f.streamk) *
+               (int64_t)sizeof(float);
+    const rtm::SplitK &plan = f.workspace;
     return plan.splits > 1 ? (int64_t)plan.splits * M * N * (int64_t)sizeof(float) : 0;
 }
 
@@ -468,6 +475,26 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
     if (M <= rtm::kShortMaxM)
         return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d, s));
     const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
+    if (f.streamk > 0) {
+        // Stream-K needs the TMA-fed kernel (K % 4 == 0, N % 4 == 0, 16-byte
+        // aligned A, B and workspace); otherwise gemm_f32's schedule runs.
+        const int64_t need = rtm::sgemm_streamk_workspace_floats((int)M, (int)N, f.streamk) * 4;
+        rtm::SimtTma tma;
+        tma.encode_tiled = encode_tiled_fn();
+        tma.err = d.err;
+        tma.wait_limit_ns = kDefaultWaitLimitNs;
+        if (workspace_bytes >= need && tma.encode_tiled &&
+            (reinterpret_cast<uintptr_t>(workspace) & 15) == 0 &&
+            rtm::sgemm_tma_eligible((int)M, (int)N, (int)K, A, B)) {
+            if (overlaps(workspace, need, A, M * K * 4) || overlaps(workspace, need, B, K * N * 4) ||
+                overlaps(workspace, need, C, M * N * 4))
+                return GEMM_ERR_INVALID_ARG;
+            return finish(rtm::launch_sgemm_f32_streamk((int)M, (int)N, (int)K, A, B, C, tma,
+                                                        f.streamk, f.streamk <= d.sms,
+                                                        static_cast<float *>(workspace), s));
+        }
+        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, d, s));
+    }
     const rtm::SplitK &plan = f.workspace;
     const int64_t need = plan.splits > 1 ? (int64_t)plan.splits * M * N * 4 : 0;
     if (need == 0 || workspace_bytes < need)

@@ -116,10 +116,10 @@ cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const floa
 // equal ranges of the tiles x K-slices iterations; tiles split between CTAs
 // are added by a fixup kernel in a fixed order (repeatable bit for bit).
 // workspace: sgemm_streamk_workspace_floats(M, N, ctas) floats, 16-byte
-// aligned. Operands as launch_sgemm_f32_tma.
+// aligned. Operands as launch_sgemm_f32_tma. spread: one CTA per SM.
 int64_t sgemm_streamk_workspace_floats(int M, int N, int ctas);
 cudaError_t launch_sgemm_f32_streamk(int M, int N, int K, const float *A, const float *B, float *C,
-                                     const SimtTma &tma, int ctas, float *workspace,
+                                     const SimtTma &tma, int ctas, bool spread, float *workspace,
                                      cudaStream_t stream);
 
 // SIMT FP32 register-tiled product (sgemm_simt.cu): any shape and
@@ -192,8 +192,13 @@ cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const fl
 // go to the workspace), else the cluster split or the plain product.
 struct F32Schedule {
     SplitK workspace;  // splits > 1: split-K through a workspace of splits * M * N floats
-    SplitK cluster;    // used when workspace.splits == 1
+    SplitK cluster;    // used when workspace.splits == 1 and streamk == 0
+    int streamk = 0;   // > 0: stream-K over this many CTAs (launch_sgemm_f32_streamk)
 };
+// Stream-K's CTA count for a product (0: not a stream-K product: 64-row or
+// 64-column tiles, or more 128 x 128 tiles than SMs) and, in *est, its run
+// time in the slice-time units of sgemm_cluster_plan's estimate. sgemm_plan.cu.
+int sgemm_streamk_plan(int M, int N, int K, int sm_count, double *est);
 F32Schedule sgemm_ws_schedule(int M, int N, int K, int sm_count);
 cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const float *B, float *C,
                                      const SplitK &plan, cudaStream_t stream);

@@ -209,6 +209,41 @@ SplitK sgemm_cluster_plan(int M, int N, int K, int sm_count, const int (&residen
     return p;
 }
 
+// Stream-K over 128 x 128 tiles (sgemm_tma.cu), for products with at most one
+// tile per SM: the CTAs take equal ranges of the tiles x K-slices iterations,
+// so every SM works the same time instead of the cluster split's whole CTAs
+// that leave some SMs with two and others with one; split tiles are added by
+// a fixup kernel. Two CTAs per SM where that leaves each at least 4 slices,
+// else one. Priced in slice-times like the other schedules (0.9 x twice a lone
+// CTA's time for two per SM), x 0.95 for the packed-FMA loop, plus a fixed
+// cost for the prologue, the partial tiles and the fixup (kStreamKFixed),
+// fitted on GB300 to 1024^3, 512^2 x 8192, 640^2 x 4096 and 1280^2 x 1024
+// (4.1-5.1; 48.5, 83.9, 68.1, 71.1 us at 304 CTAs against 49.8, 92.5 (the
+// workspace split), 94.3 and 74.2 before). Only for K % 4 == 0 and N % 4 == 0:
+// the TMA loads need rows on 16-byte boundaries.
+constexpr double kStreamKFixed = 4.4;
+constexpr double kPackedLoop = 0.95;
+
+int sgemm_streamk_plan(int M, int N, int K, int sm_count, double *est)
+{
+    if (est)
+        *est = 1e300;
+    if (M <= kShortTileM || N <= kNarrowN || sm_count <= 0 || K % 4 != 0 || N % 4 != 0)
+        return 0;
+    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
+    if (tiles > sm_count)
+        return 0;
+    const long long iters = tiles * ((K + kSliceK - 1) / kSliceK);
+    if (iters >= (1LL << 31))
+        return 0;
+    const bool two = iters >= 8LL * sm_count;
+    const int ctas = two ? 2 * sm_count : (int)(iters < sm_count ? iters : sm_count);
+    const long long chunk = (iters + ctas - 1) / ctas;
+    if (est)
+        *est = (two ? kPackedRate * 2.0 : 1.0) * (double)chunk * kPackedLoop + kStreamKFixed;
+    return ctas;
+}
+
 // Products with more 128 x 128 tiles than SMs: the whole waves of CTA slots
 // (2 per SM) run as the plain product, and the ragged last wave can run as a
 // second launch with K split over clusters of 4 CTAs. Measured on GB300 (plain

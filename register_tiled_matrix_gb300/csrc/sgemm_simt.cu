@@ -768,13 +768,18 @@ SplitK sgemm_cluster_schedule(int M, int N, int K, int sm_count, double *est)
 
 F32Schedule sgemm_ws_schedule(int M, int N, int K, int sm_count)
 {
-    double cluster_est = 0;
+    double cluster_est = 0, streamk_est = 1e300;
     F32Schedule f;
     f.workspace = sgemm_splitk_plan(M, N, K, sm_count);
     f.cluster = sgemm_cluster_schedule(M, N, K, sm_count, &cluster_est);
-    if (f.workspace.splits > 1 &&
-        cluster_est < sgemm_workspace_estimate(M, N, K, sm_count, f.workspace))
+    const double ws_est = sgemm_workspace_estimate(M, N, K, sm_count, f.workspace);
+    if (f.workspace.splits > 1 && cluster_est < ws_est)
         f.workspace = SplitK{1, K};
+    const int sk = sgemm_streamk_plan(M, N, K, sm_count, &streamk_est);
+    if (sk > 0 && streamk_est < cluster_est && (f.workspace.splits <= 1 || streamk_est < ws_est)) {
+        f.streamk = sk;
+        f.workspace = SplitK{1, K};
+    }
     return f;
 }
 

@@ -5,7 +5,7 @@
 // cp.async kernel (sgemm_simt.cu): 16 x 16 threads, 8 x 8 accumulators per
 // thread as 2 x 2 sub-blocks of 4 x 4 spaced 64 apart, 32-deep K slices, A
 // k-major with rows padded to 132 floats, B as stored; per k, 4 LDS.128 feed
-// 64 FFMA walked in serpentine order ("理解 Register Tiling", section
+// 64 FMAs, here as 32 packed two-wide FMAs ("理解 Register Tiling", section
 // "关键循环：为什么省了 Shared Memory 读取？"; "寄存器Tiling跨架构解析",
 // sections 1.1 and 6.3 on staging K slices through shared memory).
 //
@@ -33,8 +33,8 @@
 //
 // Requirements (checked by the launcher): K % 4 == 0 and N % 4 == 0 (TMA row
 // strides are multiples of 16 bytes), A and B 16-byte aligned. The sum over k
-// runs in the same order with the same FMA as the cp.async kernel, so the
-// two give the same bits.
+// runs in the same order with the same rounding as the cp.async kernel, so
+// the two give the same bits.
 #include <atomic>
 #include <cstdint>
 
@@ -62,6 +62,7 @@ constexpr int OFF_A = OFF_B + 2 * B_STAGE * 4;
 constexpr int OFF_BAR = OFF_A + 2 * A_STAGE * 4;
 constexpr int SMEM_BYTES = OFF_BAR + 16 + 1024;  // + room to align the base
 constexpr uint32_t kSliceBytes = (BM * BK + BK * BN) * 4;
+constexpr int kSpreadSmem = 120 * 1024;  // more than half of an SM's 228 KB
 
 __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n, int &tile_m,
                                               int &tile_n)
@@ -89,6 +90,31 @@ __device__ __forceinline__ void sts128(uint32_t addr, float x, float y, float z,
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y), "f"(z),
                  "f"(w)
                  : "memory");
+}
+
+// One k-step of the 8 x 8 register tile: acc[i][j] += a[i] * b[j], as 32
+// packed two-wide FMAs (fma.rn.f32x2) on pairs of rows (2 i', 2 i' + 1) of
+// one column j, with b[j] in both halves; each half rounds exactly like a
+// scalar fmaf, so every accumulator sees the same operations in the same
+// order as the scalar loop. Columns in order, row pairs in serpentine
+// order. On GB300 4096^3: 2.255 ms with scalar FFMA, 2.141 ms packed (pairs
+// along n with a[i] in both halves: 2.152 ms); half the FMA instructions
+// leave issue slots to the loads and the transpose.
+__device__ __forceinline__ void outer_product_step(float (&acc)[8][8], const float (&a)[8],
+                                                   const float (&b)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float2 bb = make_float2(b[j], b[j]);
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+            const int i2 = (j & 1) ? 3 - ii : ii;
+            float2 d = make_float2(acc[2 * i2][j], acc[2 * i2 + 1][j]);
+            d = __ffma2_rn(make_float2(a[2 * i2], a[2 * i2 + 1]), bb, d);
+            acc[2 * i2][j] = d.x;
+            acc[2 * i2 + 1][j] = d.y;
+        }
+    }
 }
 
 template <bool C_VEC>
@@ -202,13 +228,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 b[p * 4 + 2] = v.z;
                 b[p * 4 + 3] = v.w;
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int j = (i & 1) ? 7 - jj : jj;  // serpentine: an operand carries over
-                    acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                }
+            outer_product_step(acc, a, b);
             if (k == BK - 1 && next)
                 transpose(kt + 1);
         }
@@ -274,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int abort_flag;
     __shared__ int issued, confirmed;  // thread 0's count of slices issued / seen landed
+    __shared__ int it_ks, it_m0, it_n0, it_tile;  // thread 0: the next slice to issue
+    // This CTA's range, written once by thread 0 and read where it is used
+    // (volatile), so that none of it holds a register across the FMA loop.
+    __shared__ int sk_n, sk_t0, sk_ks0, sk_ktiles, sk_tiles_m, sk_tiles_n;
     const uint32_t raw = smem_u32(smem_raw);
     unsigned char *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     float *stA = reinterpret_cast<float *>(base + OFF_ST);
@@ -284,38 +308,59 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    const int ktiles = (K + BK - 1) / BK;
-    const long long iters = (long long)tiles_m * tiles_n * ktiles;
-    const int c = (int)blockIdx.x;
-    const long long g0 = (long long)c * iters / gridDim.x;
-    const int n = (int)((long long)(c + 1) * iters / gridDim.x - g0);
     const int tm = (warp >> 1) * 4 + (((lane >> 2) & 1) | ((lane >> 3) & 2));
     const int tn = (warp & 1) * 8 + ((lane & 3) | ((lane >> 1) & 4));
 
     if (tid == 0) {
+        const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+        const int ktiles = (K + BK - 1) / BK;
+        const long long iters = (long long)tiles_m * tiles_n * ktiles;
+        const long long g0 = (long long)blockIdx.x * iters / gridDim.x;
+        const int t0 = (int)(g0 / ktiles);
+        sk_n = (int)((long long)(blockIdx.x + 1) * iters / gridDim.x - g0);
+        sk_t0 = t0;
+        sk_ks0 = (int)(g0 % ktiles);
+        sk_ktiles = ktiles;
+        sk_tiles_m = tiles_m;
+        sk_tiles_n = tiles_n;
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
         fence_mbarrier_init();
         abort_flag = 0;
         issued = 0;
         confirmed = 0;
+        int tmi, tni;
+        tile_of_block(t0, tiles_m, tiles_n, tmi, tni);
+        it_tile = t0;
+        it_ks = sk_ks0;
+        it_m0 = tmi * BM;
+        it_n0 = tni * BN;
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
     __syncthreads();
+    auto shared_int = [](const int &v) { return *reinterpret_cast<const volatile int *>(&v); };
+    const int n = shared_int(sk_n);
 
-    // Thread 0: slice s of this CTA's range (iteration g0 + s) into stage s % 2.
+    // Thread 0: slice s of this CTA's range into stage s % 2. Its position
+    // (tile, K-slice) advances by one per call and lives in shared memory, so
+    // no division runs per slice and no register is taken from the loop.
     auto issue = [&](int s) {
-        const long long g = g0 + s;
-        int tmi, tni;
-        tile_of_block((int)(g / ktiles), tiles_m, tiles_n, tmi, tni);
-        const int ks = (int)(g % ktiles);
+        const int ks = it_ks;
         uint64_t *bar = &full[s & 1];
         mbar_arrive_expect_tx(bar, kSliceBytes);
-        tma_load_2d(smem_u32(stA), &tmA, bar, ks * BK, tmi * BM);
-        tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, tni * BN, ks * BK);
+        tma_load_2d(smem_u32(stA), &tmA, bar, ks * BK, it_m0);
+        tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, it_n0, ks * BK);
         ++issued;
+        if (ks + 1 == sk_ktiles) {
+            int tmi, tni;
+            tile_of_block(++it_tile, sk_tiles_m, sk_tiles_n, tmi, tni);
+            it_m0 = tmi * BM;
+            it_n0 = tni * BN;
+            it_ks = 0;
+        } else {
+            it_ks = ks + 1;
+        }
     };
     const int r4 = warp * 4 + (lane & 3);
     const int q = ((lane >> 3) << 1) | ((lane >> 2) & 1);
@@ -352,9 +397,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // Tile segments of the range: [s, s + len) is K-slices ks0 .. ks0 + len - 1
     // of one tile. The inner loop is the plain kernel's slice loop.
-    for (int s = 0; s < n;) {
-        const long long g = g0 + s;
-        const int ks0 = (int)(g % ktiles);
+    for (int s = 0, t = shared_int(sk_t0), ks0 = shared_int(sk_ks0); s < n; ++t, ks0 = 0) {
+        const int ktiles = shared_int(sk_ktiles);
         const int len = min(n - s, ktiles - ks0);
         float acc[8][8];
 #pragma unroll
@@ -385,13 +429,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     b[p * 4 + 2] = v.z;
                     b[p * 4 + 3] = v.w;
                 }
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int j = (i & 1) ? 7 - jj : jj;
-                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                    }
+                outer_product_step(acc, a, b);
                 if (k == BK - 1 && next)
                     transpose(s + 1);
             }
@@ -400,11 +438,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 issue(s + 2);
         }
         // The segment's accumulators: a whole tile to C, a part to its slot.
-        const int t = (int)(g / ktiles);
         int tmi, tni;
-        tile_of_block(t, tiles_m, tiles_n, tmi, tni);
-        const bool whole = ks0 == 0 && len == ktiles;
-        float *slot = W + (size_t)(c + t) * (BM * BN);
+        tile_of_block(t, shared_int(sk_tiles_m), shared_int(sk_tiles_n), tmi, tni);
+        const bool whole = ks0 == 0 && len == shared_int(sk_ktiles);
+        float *slot = W + (size_t)(blockIdx.x + t) * (BM * BN);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -449,8 +486,13 @@ __device__ __forceinline__ long long streamk_cta_of(long long g, long long iters
     return ((g + 1) * ctas - 1) / iters;
 }
 
-// One CTA per tile: tiles split between CTAs c0 < ... < c1 get C = W[c0 + t]
-// + ... + W[c1 + t], added in that order; tiles computed whole are left alone.
+// Tiles split between CTAs c0 < ... < c1 get C = W[c0 + t] + ... + W[c1 + t],
+// added in that order; tiles computed whole are left alone. Grid (tiles,
+// kFixupParts): CTA (t, y) owns rows y * BM / kFixupParts .. of tile t, one
+// float4 per thread, and loads up to 8 parts before adding them, so the
+// fixup runs at the speed of its loads rather than one L2 round trip per part.
+constexpr int kFixupParts = BM * BN / 4 / kThreads;  // 16: one float4 per thread
+
 template <bool C_VEC>
 __global__ void __launch_bounds__(kThreads)
     sgemm_streamk_fixup_kernel(const float *__restrict__ W, float *__restrict__ C, int M, int N,
@@ -467,31 +509,41 @@ __global__ void __launch_bounds__(kThreads)
         return;
     int tmi, tni;
     tile_of_block(t, tiles_m, tiles_n, tmi, tni);
-    for (int f = (int)threadIdx.x; f < BM * BN / 4; f += kThreads) {
-        const int r = f / (BN / 4), cc = (f % (BN / 4)) * 4;
-        const size_t off = (size_t)r * BN + cc;
-        float4 sum = *reinterpret_cast<const float4 *>(W + (size_t)(c0 + t) * (BM * BN) + off);
-        for (long long c = c0 + 1; c <= c1; ++c) {
-            const float4 v = *reinterpret_cast<const float4 *>(W + (size_t)(c + t) * (BM * BN) + off);
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
-        }
-        const int gm = tmi * BM + r, gn = tni * BN + cc;
-        if (gm >= M)
-            continue;
-        float *crow = C + (size_t)gm * N;
-        if constexpr (C_VEC) {
-            if (gn < N)
-                *reinterpret_cast<float4 *>(crow + gn) = sum;
-        } else {
-            const float w[4] = {sum.x, sum.y, sum.z, sum.w};
+    const int f = (int)blockIdx.y * kThreads + (int)threadIdx.x;  // float4 index in the tile
+    const int r = f / (BN / 4), cc = (f % (BN / 4)) * 4;
+    const size_t off = (size_t)r * BN + cc;
+    auto part = [&](long long c) {
+        return *reinterpret_cast<const float4 *>(W + (size_t)(c + t) * (BM * BN) + off);
+    };
+    float4 sum = part(c0);
+    for (long long c = c0 + 1; c <= c1; c += 8) {
+        float4 v[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (gn + j < N)
-                    crow[gn + j] = w[j];
-        }
+        for (int u = 0; u < 8; ++u)
+            if (c + u <= c1)
+                v[u] = part(c + u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (c + u <= c1) {
+                sum.x += v[u].x;
+                sum.y += v[u].y;
+                sum.z += v[u].z;
+                sum.w += v[u].w;
+            }
+    }
+    const int gm = tmi * BM + r, gn = tni * BN + cc;
+    if (gm >= M)
+        return;
+    float *crow = C + (size_t)gm * N;
+    if constexpr (C_VEC) {
+        if (gn < N)
+            *reinterpret_cast<float4 *>(crow + gn) = sum;
+    } else {
+        const float w[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (gn + j < N)
+                crow[gn + j] = w[j];
     }
 }
 
@@ -559,7 +611,7 @@ int64_t sgemm_streamk_workspace_floats(int M, int N, int ctas)
 }
 
 cudaError_t launch_sgemm_f32_streamk(int M, int N, int K, const float *A, const float *B, float *C,
-                                     const SimtTma &tma, int ctas, float *workspace,
+                                     const SimtTma &tma, int ctas, bool spread, float *workspace,
                                      cudaStream_t stream)
 {
     using namespace simt_tma;
@@ -582,17 +634,20 @@ cudaError_t launch_sgemm_f32_streamk(int M, int N, int K, const float *A, const 
     const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
     auto kernel = c_vec ? sgemm_tma_streamk_kernel<true> : sgemm_tma_streamk_kernel<false>;
     static std::atomic<uint64_t> done_vec{0}, done_any{0};
-    cudaError_t e = set_smem_limit_once(kernel, SMEM_BYTES, c_vec ? done_vec : done_any);
+    cudaError_t e = set_smem_limit_once(kernel, kSpreadSmem, c_vec ? done_vec : done_any);
     if (e != cudaSuccess)
         return e;
-    kernel<<<(unsigned)ctas, kThreads, SMEM_BYTES, stream>>>(ta, tb, M, N, K, C, workspace,
-                                                              tma.err, tma.wait_limit_ns);
+    // spread: reserve more than half of an SM's shared memory so that every
+    // CTA has an SM to itself (the scheduler may otherwise pair CTAs on some
+    // SMs and leave others idle).
+    kernel<<<(unsigned)ctas, kThreads, spread ? kSpreadSmem : SMEM_BYTES, stream>>>(
+        ta, tb, M, N, K, C, workspace, tma.err, tma.wait_limit_ns);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     // The fixup: a programmatic dependent of the stream-K grid, launched while
     // it runs and waiting for it inside the kernel.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)tiles, 1, 1);
+    cfg.gridDim = dim3((unsigned)tiles, kFixupParts, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -1,5 +1,7 @@
 // Test driver (host code only): prints the fp32 schedule planners' choices
-// (splits, spread, tile shape and K chunks) for the shapes given on the command
+// (splits, spread, tile shape, K chunks; the workspace split "priced lower"
+// against the cluster split alone; stream-K's CTAs and whether stream-K is the
+// workspace entry's choice over both) for the shapes given on the command
 // line as M,N,K triples, for a 152-SM GPU whose
 // cluster-split CTAs fit 76 clusters of 2, 36 of 4 and 15 of 8 at one CTA per
 // SM (the occupancy the library queries on GB300); with "pair" first, the
@@ -32,10 +34,14 @@ int main(int argc, char **argv)
         const bool ws_wins = w.splits > 1 && !(cluster_est < w_est);
         const rtm::TailPlan t = rtm::sgemm_tail_plan(M, N, K, sms);
         const rtm::SimtTile tile = rtm::simt_resolve_tile(c.tile, M, N);
+        double sk_est = 0;
+        const int sk = rtm::sgemm_streamk_plan(M, N, K, sms, &sk_est);
+        const bool sk_wins = sk > 0 && sk_est < cluster_est && (!ws_wins || sk_est < w_est);
         std::printf("%d %d %d cluster %d %d workspace %d %d tail %lld %d tile %d %d "
-                    "chunks %d %d %d\n",
-                    M, N, K, c.splits, c.spread ? 1 : 0, w.splits, ws_wins ? 1 : 0, t.plain_tiles,
-                    t.tail.splits, tile.m, tile.n, c.kchunk, w.kchunk, t.tail.kchunk);
+                    "chunks %d %d %d streamk %d %d\n",
+                    M, N, K, c.splits, c.spread ? 1 : 0, w.splits, ws_wins ? 1 : 0,
+                    t.plain_tiles, t.tail.splits, tile.m, tile.n, c.kchunk, w.kchunk,
+                    t.tail.kchunk, sk, sk_wins ? 1 : 0);
     }
     return 0;
 }

@@ -191,16 +191,20 @@ def test_cluster_split_unaligned_output():
 
 
 def test_workspace_entry_takes_the_cheaper_split():
-    # 1024^3 splits over clusters (no workspace); 512 x 512 x 8192 needs more
-    # chunks than a cluster holds and keeps the workspace split. Both agree
-    # with the oracle through both entry points.
-    assert rtm.gemm_f32_workspace_bytes(1024, 1024, 1024) == 0
-    assert rtm.gemm_f32_schedule(1024, 1024, 1024, workspace=True)[0] == "tiles+cluster-split"
+    # gemm_f32 splits 1024^3 and 512 x 512 x 8192 over clusters (no
+    # workspace); gemm_f32_ws runs them as stream-K through its workspace.
+    # 1000 x 1000 x 999 (K % 4 != 0: no TMA loads, no stream-K) takes the
+    # cluster split through both, and 256 x 256 x 2048 the workspace split.
+    assert rtm.gemm_f32_schedule(1024, 1024, 1024)[0] == "tiles+cluster-split"
+    assert rtm.gemm_f32_schedule(1024, 1024, 1024, workspace=True)[0] == "tiles+stream-k"
     assert rtm.gemm_f32_workspace_bytes(512, 512, 8192) > 0
-    assert rtm.gemm_f32_schedule(512, 512, 8192, workspace=True)[0] == "tiles+workspace-split"
+    assert rtm.gemm_f32_schedule(512, 512, 8192, workspace=True)[0] == "tiles+stream-k"
     assert rtm.gemm_f32_schedule(512, 512, 8192)[0] == "tiles+cluster-split"
+    assert rtm.gemm_f32_workspace_bytes(1000, 1000, 999) == 0
+    assert rtm.gemm_f32_schedule(1000, 1000, 999, workspace=True)[0] == "tiles+cluster-split"
+    assert rtm.gemm_f32_schedule(256, 256, 2048, workspace=True)[0] == "tiles+workspace-split"
     assert rtm.gemm_f32_schedule(16, 8192, 8192)[0] == "column-strips"
-    for M, N, K in [(1024, 1024, 1024), (512, 512, 8192)]:
+    for M, N, K in [(1024, 1024, 1024), (512, 512, 8192), (1000, 1000, 999), (256, 256, 2048)]:
         A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M + K)
         Ad, Bd = A.to(DEV), B.to(DEV)
         Cw = rtm.gemm_f32_ws(Ad, Bd)
@@ -208,7 +212,7 @@ def test_workspace_entry_takes_the_cheaper_split():
         torch.cuda.synchronize()
         assert_close_to_oracle(Cw, A, B, "f32")
         assert_close_to_oracle(C, A, B, "f32")
-        if M == 1024:
+        if K == 999:
             assert torch.equal(C, Cw), "no workspace needed: both entries run the same schedule"
 
 

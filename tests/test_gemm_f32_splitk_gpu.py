@@ -25,20 +25,29 @@ def run_ws(A, B):
     return C
 
 
-# Workspace only where the schedule prices the workspace split below the split
-# over cluster CTAs (which needs none): long K over few tiles. 1024^3,
-# 1000 x 1000 x 999, 256^3 and 8192 x 64 x 4096 (on 256 x 64 tiles) split over
-# clusters; 4096^3 and 4097 x 3001 x 1023 fill the GPU unsplit.
-@pytest.mark.parametrize("M,N,K,split", [(48, 2048, 8192, True), (512, 512, 8192, True),
-                                         (8192, 64, 4096, False),
-                                         (2048, 128, 4096, True), (1024, 1024, 1024, False),
-                                         (1000, 1000, 999, False), (256, 256, 256, False),
-                                         (4096, 4096, 4096, False), (4097, 3001, 1023, False)])
-def test_workspace_size_policy(M, N, K, split):
+# Workspace only where the schedule prices a workspace schedule below the split
+# over cluster CTAs (which needs none): the workspace split (long K over few
+# tiles of 64 rows or columns) or stream-K (few 128 x 128 tiles, K % 4 == 0,
+# N % 4 == 0). 8192 x 64 x 4096 (on 256 x 64 tiles), 1000 x 1000 x 999 (K % 4
+# != 0) and 256^3 split over clusters; 4096^3 and 4097 x 3001 x 1023 fill the
+# GPU unsplit.
+@pytest.mark.parametrize("M,N,K,kind", [(48, 2048, 8192, "ws"), (512, 512, 8192, "sk"),
+                                        (8192, 64, 4096, None), (2048, 128, 4096, "sk"),
+                                        (1024, 1024, 1024, "sk"), (1000, 1000, 999, None),
+                                        (256, 256, 256, None), (4096, 4096, 4096, None),
+                                        (4097, 3001, 1023, None)])
+def test_workspace_size_policy(M, N, K, kind):
     n = rtm.gemm_f32_workspace_bytes(M, N, K)
-    assert (n > 0) == split
-    if split:
-        assert n % (M * N * 4) == 0 and 2 <= n // (M * N * 4) <= 32
+    assert (n > 0) == (kind is not None)
+    sched, splits = rtm.gemm_f32_schedule(M, N, K, workspace=True)
+    if kind == "ws":
+        assert sched == "tiles+workspace-split"
+        assert n % (M * N * 4) == 0 and n // (M * N * 4) == splits and 2 <= splits <= 32
+    elif kind == "sk":
+        # One 128 x 128 part per (CTA, tile) pair a range boundary cuts.
+        assert sched == "tiles+stream-k"
+        tiles = ((M + 127) // 128) * ((N + 127) // 128)
+        assert n == (tiles + splits - 1) * 128 * 128 * 4
 
 
 @pytest.mark.parametrize("name", ["f32_8192x64x4096", "f32_1024_uniform", "f32_1000x1000x999",

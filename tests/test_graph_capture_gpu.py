@@ -39,6 +39,8 @@ CASES = {
                                                lambda A, B, C, W: rtm.gemm_f32(A, B, out=C)),
     "gemm_f32_ws split-K": ("f32", 512, 64, 2048,
                             lambda A, B, C, W: rtm.gemm_f32_ws(A, B, out=C, workspace=W)),
+    "gemm_f32_ws stream-K": ("f32", 1024, 1024, 1024,
+                             lambda A, B, C, W: rtm.gemm_f32_ws(A, B, out=C, workspace=W)),
     "gemm_bf16f32 CTA pairs": ("bf16", 512, 512, 256,
                                lambda A, B, C, W: rtm.gemm_bf16f32(A, B, out=C)),
     "gemm_bf16f32 CTA pairs, K split": ("bf16", 256, 1024, 4096,

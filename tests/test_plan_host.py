@@ -92,6 +92,37 @@ def test_planner_choices(driver):
         assert got[shape] == want, (shape, got[shape], want)
 
 
+# Stream-K (gemm_f32_ws, TMA-fed 128 x 128 tiles): (CTAs, chosen over the
+# cluster and workspace splits). Measured on GB300 (us, graph replay, scalar
+# loop): 1024^3 48.5 against 49.8 for the cluster split; 512^2 x 8192 83.9
+# against 92.5 for the workspace split; 640^2 x 4096 68.1 against 94.3;
+# 2048 x 1024 x 1024 88.3 against 93.6 unsplit; 256^2 x 2048 keeps the
+# workspace split (13.2 against 15.1); K % 4 != 0 cannot be loaded by TMA.
+STREAMK_EXPECT = {
+    (1024, 1024, 1024): (304, 1),
+    (512, 512, 8192): (304, 1),
+    (640, 640, 4096): (304, 1),
+    (2048, 1024, 1024): (304, 1),
+    (256, 256, 2048): (152, 0),
+    (1000, 1000, 999): (0, 0),
+    (200, 300, 4096): (152, 0),
+    (64, 4096, 8192): (0, 0),      # 64-row tiles: not a stream-K shape
+    (4096, 4096, 4096): (0, 0),    # more tiles than SMs
+}
+
+
+def test_streamk_choices(driver):
+    args = [str(x) for shape in STREAMK_EXPECT for x in shape]
+    r = subprocess.run([driver, *args], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    got = {}
+    for line in r.stdout.splitlines():
+        f = line.split()
+        got[(int(f[0]), int(f[1]), int(f[2]))] = (int(f[20]), int(f[21]))
+    for shape, want in STREAMK_EXPECT.items():
+        assert got[shape] == want, (shape, got[shape], want)
+
+
 def _shape_grid():
     dims = [1, 7, 33, 64, 65, 100, 128, 129, 200, 256, 257, 500, 1000, 1024, 2047, 4096, 8192,
             20000]
