@@ -112,6 +112,14 @@ bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B);
 cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const float *B, float *C,
                                  const SimtTma &tma, long long tile_count, cudaStream_t stream);
 
+// The same tiles with K split over `splits` (1, 2, 4 or 8) CTAs of a cluster,
+// kchunk of K each (a multiple of 32), the partial tiles added through
+// distributed shared memory in rank order; tiles tile_first .. +tile_count - 1
+// (tile_count < 0: to the end); spread: one CTA per SM (sgemm_tma.cu).
+cudaError_t launch_sgemm_f32_tma_cluster(int M, int N, int K, const float *A, const float *B,
+                                         float *C, const SimtTma &tma, int splits, int kchunk,
+                                         bool spread, long long tile_first, long long tile_count,
+                                         cudaStream_t stream);
 // Stream-K over the TMA-fed 128 x 128 tiles (sgemm_tma.cu): `ctas` CTAs take
 // equal ranges of the tiles x K-slices iterations; tiles split between CTAs
 // are added by a fixup kernel in a fixed order (repeatable bit for bit).
@@ -201,7 +209,8 @@ struct F32Schedule {
 int sgemm_streamk_plan(int M, int N, int K, int sm_count, double *est);
 F32Schedule sgemm_ws_schedule(int M, int N, int K, int sm_count);
 cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const float *B, float *C,
-                                     const SplitK &plan, cudaStream_t stream);
+                                     const SplitK &plan, cudaStream_t stream,
+                                     const SimtTma *tma = nullptr);
 
 // The page's ablation ladder (sgemm_ladder.cu): rung 0 naive, 1 shared-memory
 // tiled (TILE 32), 2 register tiled (64 x 64 block, 4 x 4 per thread).

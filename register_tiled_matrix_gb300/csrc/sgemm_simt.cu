@@ -784,10 +784,14 @@ F32Schedule sgemm_ws_schedule(int M, int N, int K, int sm_count)
 }
 
 cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const float *B, float *C,
-                                     const SplitK &plan, cudaStream_t stream)
+                                     const SplitK &plan, cudaStream_t stream, const SimtTma *tma)
 {
-    return launch_tile<simt::kSplitCluster>(simt_resolve_tile(plan.tile, M, N), M, N, K, A, B, C,
-                                            stream, plan.splits, plan.kchunk, plan.spread);
+    const SimtTile t = simt_resolve_tile(plan.tile, M, N);
+    if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B))
+        return launch_sgemm_f32_tma_cluster(M, N, K, A, B, C, *tma, plan.splits, plan.kchunk,
+                                            plan.spread, 0, -1, stream);
+    return launch_tile<simt::kSplitCluster>(t, M, N, K, A, B, C, stream, plan.splits, plan.kchunk,
+                                            plan.spread);
 }
 
 cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const float *B, float *C,
@@ -797,13 +801,17 @@ cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const flo
     if (M <= kShortTileM || N <= kNarrowN || plan.tail.splits < 2)
         return cudaErrorInvalidValue;
     cudaError_t e = cudaSuccess;
-    if (plan.plain_tiles > 0 && tma && sgemm_tma_eligible(M, N, K, A, B))
+    const bool use_tma = tma && sgemm_tma_eligible(M, N, K, A, B);
+    if (plan.plain_tiles > 0 && use_tma)
         e = launch_sgemm_f32_tma(M, N, K, A, B, C, *tma, plan.plain_tiles, stream);
     else if (plan.plain_tiles > 0)
         e = simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1>(M, N, K, A, B, C, stream, 1, 0, false,
                                                                0, plan.plain_tiles);
     if (e != cudaSuccess)
         return e;
+    if (use_tma)
+        return launch_sgemm_f32_tma_cluster(M, N, K, A, B, C, *tma, plan.tail.splits,
+                                            plan.tail.kchunk, false, plan.plain_tiles, -1, stream);
     return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
         M, N, K, A, B, C, stream, plan.tail.splits, plan.tail.kchunk, false, plan.plain_tiles);
 }
@@ -813,7 +821,7 @@ cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const fl
                                    const SimtTma *tma)
 {
     if (cluster.splits > 1)
-        return launch_sgemm_f32_cluster(M, N, K, A, B, C, cluster, stream);
+        return launch_sgemm_f32_cluster(M, N, K, A, B, C, cluster, stream, tma);
     const TailPlan tail = sgemm_tail_plan(M, N, K, sm_count);
     if (tail.tail.splits > 1)
         return launch_sgemm_f32_tail(M, N, K, A, B, C, tail, stream, tma);

@@ -272,6 +272,209 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
+// K split over the S CTAs of a thread-block cluster, as the cp.async kernel's
+// cluster mode (sgemm_simt.cu) but with this file's TMA-fed, packed-FMA loop:
+// grid (tiles, S), cluster (1, S, 1); CTA y of a cluster multiplies K-slices
+// [y * kchunk, +kchunk) of tile tile_first + blockIdx.x, parks its partial tile
+// in its own shared memory (rows padded to BN + 4 floats), and after a cluster
+// barrier adds rows [y * BM / S, +BM / S) of the S partials, read through
+// distributed shared memory in rank order (the same sum on every call), and
+// stores them. A second barrier keeps every partial alive until it is read.
+constexpr int kPartPitch = BN + 4;
+static_assert(BM * kPartPitch * 4 <= OFF_BAR, "the partial tile fits below the barriers");
+
+template <bool C_VEC, int S>
+__device__ __forceinline__ void cluster_add_parts(const float *part, int M, int N, float *C,
+                                                  int m0, int n0, uint32_t rank)
+{
+    constexpr int ROWS = BM / S;
+    constexpr int COUNT4 = ROWS * (BN / 4);
+    constexpr int ITERS = COUNT4 / kThreads;
+    static_assert(COUNT4 % kThreads == 0, "every thread adds whole float4s");
+    float4 v[ITERS][S];
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+        const int f = (int)threadIdx.x + it * kThreads;
+        const int r = (int)rank * ROWS + f / (BN / 4), c = (f % (BN / 4)) * 4;
+        const uint32_t local = smem_u32(part + r * kPartPitch + c);
+#pragma unroll
+        for (int q = 0; q < S; ++q)
+            v[it][q] = ld_shared_cluster_v4(mapa_shared(local, (uint32_t)q));
+    }
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+        float4 sum = v[it][0];
+#pragma unroll
+        for (int q = 1; q < S; ++q) {
+            sum.x += v[it][q].x;
+            sum.y += v[it][q].y;
+            sum.z += v[it][q].z;
+            sum.w += v[it][q].w;
+        }
+        const int f = (int)threadIdx.x + it * kThreads;
+        const int gm = m0 + (int)rank * ROWS + f / (BN / 4), gn = n0 + (f % (BN / 4)) * 4;
+        if (gm >= M)
+            continue;
+        float *crow = C + (size_t)gm * N;
+        if constexpr (C_VEC) {
+            if (gn < N)
+                *reinterpret_cast<float4 *>(crow + gn) = sum;
+        } else {
+            const float w[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gn + j < N)
+                    crow[gn + j] = w[j];
+        }
+    }
+}
+
+template <bool C_VEC>
+__global__ void __launch_bounds__(kThreads, 2)
+    sgemm_tma_cluster_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
+                             int kchunk, int tile_first, float *__restrict__ C, int *err,
+                             uint64_t wait_limit_ns)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    float *stA = reinterpret_cast<float *>(base + OFF_ST);
+    float *sB = reinterpret_cast<float *>(base + OFF_B);
+    float *sA = reinterpret_cast<float *>(base + OFF_A);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + OFF_BAR);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    int tile_m, tile_n;
+    tile_of_block((int)blockIdx.x + tile_first, (M + BM - 1) / BM, (N + BN - 1) / BN, tile_m,
+                  tile_n);
+    const int m0 = tile_m * BM, n0 = tile_n * BN;
+    const int tm = (warp >> 1) * 4 + (((lane >> 2) & 1) | ((lane >> 3) & 2));
+    const int tn = (warp & 1) * 8 + ((lane & 3) | ((lane >> 1) & 4));
+    const int ks_begin = (int)blockIdx.y * (kchunk / BK);
+    const int ktiles = max(0, min((K + BK - 1) / BK - ks_begin, kchunk / BK));
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fence_mbarrier_init();
+        abort_flag = 0;
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    __syncthreads();
+
+    int issued = 0, confirmed = 0;
+    auto issue = [&](int s) {
+        uint64_t *bar = &full[s & 1];
+        mbar_arrive_expect_tx(bar, kSliceBytes);
+        tma_load_2d(smem_u32(stA), &tmA, bar, (ks_begin + s) * BK, m0);
+        tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, n0, (ks_begin + s) * BK);
+        ++issued;
+    };
+    const int r4 = warp * 4 + (lane & 3);
+    const int q = ((lane >> 3) << 1) | ((lane >> 2) & 1);
+    const uint32_t st_base = smem_u32(stA);
+    const uint32_t a_dst = smem_u32(sA + (4 * q) * LDA + 4 * r4);
+    auto transpose = [&](int s) {
+        if (mbar_wait_bounded(&full[s & 1], (uint32_t)((s >> 1) & 1), wait_limit_ns, &abort_flag)) {
+            if (tid == 0 && confirmed == s)
+                confirmed = s + 1;
+        } else {
+            atomicCAS(err, 0, kDevErrTimeout);
+            abort_flag = 1;
+        }
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 4 * r4 + i;
+            v[i] = lds128(st_base + (uint32_t)(row * (BK * 4) + ((q ^ (row & 7)) * 16)));
+        }
+        const uint32_t d = a_dst + (uint32_t)((s & 1) * A_STAGE * 4);
+        sts128(d + 0 * LDA * 4, v[0].x, v[1].x, v[2].x, v[3].x);
+        sts128(d + 1 * LDA * 4, v[0].y, v[1].y, v[2].y, v[3].y);
+        sts128(d + 2 * LDA * 4, v[0].z, v[1].z, v[2].z, v[3].z);
+        sts128(d + 3 * LDA * 4, v[0].w, v[1].w, v[2].w, v[3].w);
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            acc[i][j] = 0.0f;
+
+    if (ktiles > 0) {
+        if (tid == 0)
+            issue(0);
+        transpose(0);
+        __syncthreads();
+        if (tid == 0 && ktiles > 1)
+            issue(1);
+    }
+    for (int kt = 0; kt < ktiles; ++kt) {
+        const float *cA = sA + (kt & 1) * A_STAGE + tm * 4;
+        const float *cB = sB + (kt & 1) * B_STAGE + tn * 4;
+        const bool next = kt + 1 < ktiles;
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            float a[8], b[8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 v = *reinterpret_cast<const float4 *>(cA + k * LDA + h * 64);
+                a[h * 4 + 0] = v.x;
+                a[h * 4 + 1] = v.y;
+                a[h * 4 + 2] = v.z;
+                a[h * 4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const float4 v = *reinterpret_cast<const float4 *>(cB + k * BN + p * 64);
+                b[p * 4 + 0] = v.x;
+                b[p * 4 + 1] = v.y;
+                b[p * 4 + 2] = v.z;
+                b[p * 4 + 3] = v.w;
+            }
+            outer_product_step(acc, a, b);
+            if (k == BK - 1 && next)
+                transpose(kt + 1);
+        }
+        __syncthreads();
+        if (tid == 0 && kt + 2 < ktiles)
+            issue(kt + 2);
+    }
+    if (tid == 0 && confirmed < issued) {
+        int never = 0;
+        for (int s = confirmed; s < issued; ++s)
+            mbar_wait_bounded(&full[s & 1], (uint32_t)((s >> 1) & 1), wait_limit_ns, &never);
+    }
+
+    // Park the partial tile (the stages are free: the last barrier above).
+    float *part = reinterpret_cast<float *>(base);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const float *v = &acc[h * 4 + i][p * 4];
+                *reinterpret_cast<float4 *>(part + (h * 64 + tm * 4 + i) * kPartPitch + p * 64 +
+                                            tn * 4) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+    cluster_sync();
+    const uint32_t rank = blockIdx.y;  // cluster (1, S, 1)
+    switch (gridDim.y) {
+    case 2: cluster_add_parts<C_VEC, 2>(part, M, N, C, m0, n0, rank); break;
+    case 4: cluster_add_parts<C_VEC, 4>(part, M, N, C, m0, n0, rank); break;
+    case 8: cluster_add_parts<C_VEC, 8>(part, M, N, C, m0, n0, rank); break;
+    default: cluster_add_parts<C_VEC, 1>(part, M, N, C, m0, n0, rank); break;
+    }
+    cluster_sync();
+}
+
 // Stream-K ("寄存器Tiling跨架构解析", sections 2.4 and 7.2: work per block
 // and how many blocks keep the SMs busy). The product's tiles x K-slices
 // iterations I are cut into gridDim.x equal ranges, one per CTA: CTA c takes
@@ -601,6 +804,51 @@ cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const floa
     kernel<<<(unsigned)tiles, kThreads, SMEM_BYTES, stream>>>(ta, tb, M, N, K, C, tma.err,
                                                                tma.wait_limit_ns);
     return cudaGetLastError();
+}
+
+cudaError_t launch_sgemm_f32_tma_cluster(int M, int N, int K, const float *A, const float *B,
+                                         float *C, const SimtTma &tma, int splits, int kchunk,
+                                         bool spread, long long tile_first, long long tile_count,
+                                         cudaStream_t stream)
+{
+    using namespace simt_tma;
+    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B) ||
+        (splits != 1 && splits != 2 && splits != 4 && splits != 8) || kchunk % BK != 0 ||
+        (long long)splits * kchunk < K)
+        return cudaErrorInvalidValue;
+    const long long all_tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (all_tiles > 0x7fffffffLL || tile_first < 0 || tile_first > all_tiles)
+        return cudaErrorInvalidValue;
+    const long long tiles = tile_count < 0 || tile_first + tile_count > all_tiles
+                                ? all_tiles - tile_first
+                                : tile_count;
+    if (tiles == 0)
+        return cudaSuccess;
+    auto fn = reinterpret_cast<EncodeTiledFn>(tma.encode_tiled);
+    CUtensorMap ta, tb;
+    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+    auto kernel = c_vec ? sgemm_tma_cluster_kernel<true> : sgemm_tma_cluster_kernel<false>;
+    static std::atomic<uint64_t> done_vec{0}, done_any{0};
+    const cudaError_t e = set_smem_limit_once(kernel, kSpreadSmem, c_vec ? done_vec : done_any);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles, (unsigned)splits, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = spread ? kSpreadSmem : SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, kchunk, (int)tile_first, C, tma.err,
+                              tma.wait_limit_ns);
 }
 
 int64_t sgemm_streamk_workspace_floats(int M, int N, int ctas)

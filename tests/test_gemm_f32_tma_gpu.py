@@ -22,10 +22,15 @@ DEV = "cuda:0"
 
 # Shapes whose gemm_f32 schedule is unsplit 128 x 128 tiles (more tiles than
 # SMs, or K too short to split): ragged M, N and K (K not a multiple of the
-# 32-deep slice, down to one partial slice), and one whose ragged last wave
-# is split over clusters after whole waves of plain tiles (2304^2 x 1024).
+# 32-deep slice, down to one partial slice); one whose ragged last wave is
+# split over clusters after whole waves of plain tiles (2304^2 x 1024); and
+# 128 x 128 tiles with K split over clusters of 2, 4 or 8 CTAs (8: one CTA per
+# SM, 512 x 384 x 8192; TMA-fed
+# cluster kernel; the same chunks added in the same rank order as the
+# cp.async kernel's cluster mode).
 SHAPES = [(2000, 2004, 100), (1664, 1920, 260), (4100, 1028, 36), (3000, 1000, 8),
-          (1500, 2600, 700), (2304, 2304, 1024)]
+          (1500, 2600, 700), (2304, 2304, 1024), (1024, 1024, 1024), (1000, 1000, 1000),
+          (300, 3000, 700), (512, 384, 8192)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -64,19 +69,20 @@ def kernel_names(fn) -> list:
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_tma_kernel_matches_oracle_and_cp_async_bits(M, N, K):
-    assert rtm.gemm_f32_schedule(M, N, K)[0] in ("tiles", "tiles+tail-cluster-split")
+    assert rtm.gemm_f32_schedule(M, N, K)[0] in ("tiles", "tiles+tail-cluster-split",
+                                                 "tiles+cluster-split")
     A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=M + 7 * N + K)
     Ad, Bd = A.to(DEV), B.to(DEV)
     buf, C = guarded_output(M, N, DEV)
     names = kernel_names(lambda: rtm.gemm_f32(Ad, Bd, out=C))
-    assert any("sgemm_tma_kernel" in n for n in names), names
+    assert any("simt_tma::" in n for n in names), names
     torch.cuda.synchronize()
     assert rtm.get_device_error() == 0
     assert guard_intact(buf, M, N)
     assert_close_to_oracle(C, A, B, "f32")
     Bo = offset_copy(Bd)
     names_cp = kernel_names(lambda: rtm.gemm_f32(Ad, Bo))
-    assert not any("sgemm_tma_kernel" in n for n in names_cp), names_cp
+    assert not any("simt_tma::" in n for n in names_cp), names_cp
     C_cp = rtm.gemm_f32(Ad, Bo)
     torch.cuda.synchronize()
     assert torch.equal(C, C_cp), "TMA-fed and cp.async kernels differ"
