@@ -164,14 +164,17 @@ class ClockSampler:
 
         sm, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
         nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM = 1
-        while not self.stop_flag.is_set():
-            if nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(sm)) == 0:
-                power = mw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(handle, ctypes.byref(mw)) == 0 \
-                    else None
-                bits = rs.value if reasons is not None and reasons(handle, ctypes.byref(rs)) == 0 \
-                    else 0
-                self.samples.append((float(sm.value), float(mx.value), power, bits))
-            self.stop_flag.wait(self.period_ms / 1e3)
+        try:
+            while not self.stop_flag.is_set():
+                if nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(sm)) == 0:
+                    power = (mw.value / 1e3
+                             if nv.nvmlDeviceGetPowerUsage(handle, ctypes.byref(mw)) == 0 else None)
+                    bits = (rs.value
+                            if reasons is not None and reasons(handle, ctypes.byref(rs)) == 0 else 0)
+                    self.samples.append((float(sm.value), float(mx.value), power, bits))
+                self.stop_flag.wait(self.period_ms / 1e3)
+        finally:
+            nv.nvmlShutdown()
 
     def start(self):
         nvml = None

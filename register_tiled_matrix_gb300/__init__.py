@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     gemm_bf16f32_selftest_timeout,
     gemm_f32,
     gemm_f32_ladder,
+    gemm_f32_selftest_timeout,
     gemm_f32_schedule,
     gemm_f32_workspace_bytes,
     F32_KINDS,

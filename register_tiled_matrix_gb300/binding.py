@@ -72,6 +72,8 @@ def load_library() -> ctypes.CDLL:
         lib.gemm_f32_ladder.restype = ctypes.c_int
         lib.gemm_bf16f32_selftest_timeout.argtypes = [i64, i64, i64, p, p, p, i64, p]
         lib.gemm_bf16f32_selftest_timeout.restype = ctypes.c_int
+        lib.gemm_f32_selftest_timeout.argtypes = [i64, i64, i64, p, p, p, i64, p]
+        lib.gemm_f32_selftest_timeout.restype = ctypes.c_int
         lib.gemm_fp32_pipe_peak.argtypes = [i64, ctypes.c_int, p, ctypes.POINTER(ctypes.c_double),
                                             p]
         lib.gemm_fp32_pipe_peak.restype = ctypes.c_int
@@ -285,6 +287,19 @@ def gemm_bf16f32_selftest_timeout(A: torch.Tensor, B: torch.Tensor, out: torch.T
     N = B.shape[1]
     with torch.cuda.device(A.device):
         _check(load_library().gemm_bf16f32_selftest_timeout(
+            M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), int(wait_limit_ns),
+            _stream_handle(stream)))
+
+
+def gemm_f32_selftest_timeout(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor,
+                              wait_limit_ns: int,
+                              stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Launch gemm_f32's TMA-fed kernel with its loads muted so every bounded wait runs out."""
+    C = _prepare(A, B, torch.float32, out)
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        _check(load_library().gemm_f32_selftest_timeout(
             M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), int(wait_limit_ns),
             _stream_handle(stream)))
 

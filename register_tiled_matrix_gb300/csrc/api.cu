@@ -580,6 +580,31 @@ int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K, const uint16_
     return run_bf16(M, N, K, A, B, C, stream, (uint64_t)wait_limit_ns, 1);
 }
 
+int gemm_f32_selftest_timeout(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
+                              float *C, int64_t wait_limit_ns, void *stream)
+{
+    if (wait_limit_ns < 1000000 || wait_limit_ns > 10000000000LL)
+        return GEMM_ERR_INVALID_ARG;
+    bool nothing = false;
+    int st = rtm::check_f32_args(M, N, K, A, B, C, &nothing);
+    if (st != GEMM_OK)
+        return st;
+    if (nothing || K == 0 || !rtm::sgemm_tma_eligible((int)M, (int)N, (int)K, A, B))
+        return GEMM_ERR_INVALID_ARG;  // the self-test runs the TMA-fed kernel
+    DeviceInfo d;
+    st = current_device(&d);
+    if (st != GEMM_OK)
+        return st;
+    rtm::SimtTma tma;
+    tma.encode_tiled = encode_tiled_fn();
+    tma.err = d.err;
+    tma.wait_limit_ns = (uint64_t)wait_limit_ns;
+    if (!tma.encode_tiled)
+        return GEMM_ERR_LAUNCH;
+    return finish(rtm::launch_sgemm_f32_tma((int)M, (int)N, (int)K, A, B, C, tma, -1,
+                                            static_cast<cudaStream_t>(stream), true));
+}
+
 int gemm_get_device_error(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {

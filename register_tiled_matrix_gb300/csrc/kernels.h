@@ -109,8 +109,11 @@ struct SimtTma {
 // Needs sgemm_tma_eligible: K % 4 == 0, N % 4 == 0, A and B 16-byte aligned.
 // Same sums in the same order as the cp.async kernel (same bits).
 bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B);
+// mute: the failure-detection self-test (no loads are issued; every bounded
+// wait runs out; C is left unspecified).
 cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const float *B, float *C,
-                                 const SimtTma &tma, long long tile_count, cudaStream_t stream);
+                                 const SimtTma &tma, long long tile_count, cudaStream_t stream,
+                                 bool mute = false);
 
 // The same tiles with K split over `splits` (1, 2, 4 or 8) CTAs of a cluster,
 // kchunk of K each (a multiple of 32), the partial tiles added through

@@ -29,7 +29,8 @@
 // slice s+2 into them. Every mbarrier wait is bounded; a wait that gives up
 // records GEMM_ERR_TIMEOUT in the device error word and raises the CTA's
 // abort flag, so every thread still reaches every barrier and the kernel
-// ends.
+// ends; once the flag is up thread 0 issues no further slice (a barrier whose
+// phase never completed must not be armed again).
 //
 // Requirements (checked by the launcher): K % 4 == 0 and N % 4 == 0 (TMA row
 // strides are multiples of 16 bytes), A and B 16-byte aligned. The sum over k
@@ -117,7 +118,9 @@ __device__ __forceinline__ void outer_product_step(float (&acc)[8][8], const flo
     }
 }
 
-template <bool C_VEC>
+// MUTE (the failure-detection self-test only): thread 0 announces each slice's
+// bytes on its barrier but issues no load, so every wait runs out.
+template <bool C_VEC, bool MUTE = false>
 __global__ void __launch_bounds__(kThreads, 2)
     sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      int M, int N, int K, float *__restrict__ C, int *err, uint64_t wait_limit_ns)
@@ -157,8 +160,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto issue = [&](int s) {
         uint64_t *bar = &full[s & 1];
         mbar_arrive_expect_tx(bar, kSliceBytes);
-        tma_load_2d(smem_u32(stA), &tmA, bar, s * BK, m0);
-        tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, n0, s * BK);
+        if constexpr (!MUTE) {
+            tma_load_2d(smem_u32(stA), &tmA, bar, s * BK, m0);
+            tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, n0, s * BK);
+        }
         ++issued;
     };
 
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         issue(0);
     transpose(0);
     __syncthreads();
-    if (tid == 0 && ktiles > 1)
+    if (tid == 0 && ktiles > 1 && !abort_flag)
         issue(1);
 
     for (int kt = 0; kt < ktiles; ++kt) {
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 transpose(kt + 1);
         }
         __syncthreads();  // stage kt and the staging tile are free
-        if (tid == 0 && kt + 2 < ktiles)
+        if (tid == 0 && kt + 2 < ktiles && !abort_flag)
             issue(kt + 2);
     }
 
@@ -412,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             issue(0);
         transpose(0);
         __syncthreads();
-        if (tid == 0 && ktiles > 1)
+        if (tid == 0 && ktiles > 1 && !abort_flag)
             issue(1);
     }
     for (int kt = 0; kt < ktiles; ++kt) {
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 transpose(kt + 1);
         }
         __syncthreads();
-        if (tid == 0 && kt + 2 < ktiles)
+        if (tid == 0 && kt + 2 < ktiles && !abort_flag)
             issue(kt + 2);
     }
     if (tid == 0 && confirmed < issued) {
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             issue(0);
         transpose(0);
         __syncthreads();
-        if (tid == 0 && n > 1)
+        if (tid == 0 && n > 1 && !abort_flag)
             issue(1);
     }
     // Tile segments of the range: [s, s + len) is K-slices ks0 .. ks0 + len - 1
@@ -637,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     transpose(s + 1);
             }
             __syncthreads();  // stage s % 2 and the staging tile are free
-            if (tid == 0 && s + 2 < n)
+            if (tid == 0 && s + 2 < n && !abort_flag)
                 issue(s + 2);
         }
         // The segment's accumulators: a whole tile to C, a part to its slot.
@@ -779,7 +784,8 @@ bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B)
 }
 
 cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const float *B, float *C,
-                                 const SimtTma &tma, long long tile_count, cudaStream_t stream)
+                                 const SimtTma &tma, long long tile_count, cudaStream_t stream,
+                                 bool mute)
 {
     using namespace simt_tma;
     if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B))
@@ -796,9 +802,12 @@ cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const floa
         !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;  // N % 4 == 0 already
-    auto kernel = c_vec ? sgemm_tma_kernel<true> : sgemm_tma_kernel<false>;
-    static std::atomic<uint64_t> done_vec{0}, done_any{0};
-    const cudaError_t e = set_smem_limit_once(kernel, SMEM_BYTES, c_vec ? done_vec : done_any);
+    auto kernel = mute    ? sgemm_tma_kernel<true, true>
+                  : c_vec ? sgemm_tma_kernel<true>
+                          : sgemm_tma_kernel<false>;
+    static std::atomic<uint64_t> done_vec{0}, done_any{0}, done_mute{0};
+    const cudaError_t e =
+        set_smem_limit_once(kernel, SMEM_BYTES, mute ? done_mute : c_vec ? done_vec : done_any);
     if (e != cudaSuccess)
         return e;
     kernel<<<(unsigned)tiles, kThreads, SMEM_BYTES, stream>>>(ta, tb, M, N, K, C, tma.err,

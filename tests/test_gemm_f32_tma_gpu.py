@@ -118,3 +118,25 @@ def test_tma_kernel_repeats_bit_for_bit():
     first = rtm.gemm_f32(Ad, Bd)
     for _ in range(3):
         assert torch.equal(rtm.gemm_f32(Ad, Bd), first)
+
+
+@pytest.mark.parametrize("M,N,K", [(2000, 2004, 100), (256, 256, 4096)])
+def test_tma_kernel_bounded_wait_gives_up_and_context_survives(M, N, K):
+    """With the loads muted, every CTA's first wait runs out after 50 ms; the
+    kernel records a timeout and returns (every thread still reaches every
+    barrier), and the next product on the same context is correct."""
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=31)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = torch.empty(M, N, device=DEV)
+    assert rtm.get_device_error() == 0
+    rtm.gemm_f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
+    assert rtm.get_device_error() == -4
+    assert rtm.get_device_error() == 0, "reading the error word clears it"
+    assert_close_to_oracle(rtm.gemm_f32(Ad, Bd), A, B, "f32")
+
+
+def test_tma_selftest_rejects_shapes_off_the_tma_path():
+    A = torch.zeros(64, 99, device=DEV)  # K % 4 != 0
+    B = torch.zeros(99, 64, device=DEV)
+    with pytest.raises(rtm.GemmError):
+        rtm.gemm_f32_selftest_timeout(A, B, torch.empty(64, 64, device=DEV), 50_000_000)
