@@ -262,9 +262,12 @@ GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * aligned) the operands are staged by the tensor-memory-access unit (for
  * M <= 128 C must be 16-byte aligned with N % 8 == 0 as well; for M > 128 C
  * rows may start anywhere 4-byte aligned); otherwise by producer warps that
- * load them element by element into the same swizzled layout (slower, same
- * arithmetic; gemm_bf16f32_ws avoids this for M > 128). Ragged M, N and K
- * tiles are handled by zero-filled loads and masked stores.
+ * load them 2, 4 or 8 bytes at a time into the same swizzled layout (for
+ * M > 128 on CTA pairs as well; slower than the TMA staging, same
+ * arithmetic: for M > 128 the results equal gemm_bf16f32_ws's bit for bit
+ * unless that call adds two K halves of a tile, which it may do only when C
+ * rows are 16-byte aligned and K >= 4096). Ragged M, N and K tiles are
+ * handled by zero-filled loads and masked stores.
  *
  * Every wait inside the kernel is bounded (a few seconds); if one gives up
  * the kernel records GEMM_ERR_TIMEOUT in the device error word and returns

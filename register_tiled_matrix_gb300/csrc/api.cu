@@ -204,8 +204,9 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
                    (reinterpret_cast<uintptr_t>(B) & 1) != 0)))
         return GEMM_ERR_ALIGNMENT;
     // Rows on 16-byte boundaries (the TMA stride rule) take the TMA kernels;
-    // anything else the kernel with load-and-swizzle producer warps, unless a
-    // workspace allows re-pitched copies for the CTA-pair kernel.
+    // anything else the kernels with load-and-swizzle producer warps (CTA
+    // pairs for M > 128), unless a workspace allows re-pitched copies for the
+    // CTA-pair TMA kernel.
     const bool a_rows16 = rows_on_16_bytes(A, K);
     const bool b_rows16 = rows_on_16_bytes(B, N);
     const bool c_rows16 = rows_on_16_bytes(C, N);
@@ -279,7 +280,7 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
             }
             return finish(rtm::launch_gemm_tc_pair(L, s));
         }
-        return finish(rtm::launch_gemm_tc_any(L, s));
+        return finish(rtm::launch_gemm_tc_any_pair(L, s));
     }
     if (!tma_ok)
         return finish(rtm::launch_gemm_tc_any(L, s));

@@ -12,8 +12,12 @@ namespace rtm {
 // launched on the current device. `done` is one bit per device (a static of
 // the call site); concurrent first callers may both set the attribute, which
 // is harmless, and no flag is read or written without atomics.
+// With `carveout_pct` >= 0 it also states the preferred shared-memory
+// carve-out (percent of the SM's maximum), so that kernels whose loads pass
+// through L1 leave it the rest of the SM's unified memory.
 template <typename Kernel>
-cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> &done)
+cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> &done,
+                                int carveout_pct = -1)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -23,6 +27,9 @@ cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t> 
     if (bit && (done.load(std::memory_order_acquire) & bit))
         return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && carveout_pct >= 0)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 carveout_pct);
     if (e == cudaSuccess && bit)
         done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
@@ -271,6 +278,9 @@ cudaError_t launch_gemm_tc_t(const TcLaunch &p, int splits, bool swap, cudaStrea
 // The same product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu):
 // operands loaded by producer warps instead of TMA. mute_producer unused.
 cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);
+// The same on CTA pairs (256 x 256 tiles, each CTA staging half of the
+// operands), for M > 128. Same operand rules; any 4-byte-aligned C.
+cudaError_t launch_gemm_tc_any_pair(const TcLaunch &p, cudaStream_t stream);
 
 // The host-side argument checks of the fp32 entry points (api.cu), made
 // before any CUDA call: GEMM_OK with *nothing_to_do set when M or N is zero,

@@ -53,7 +53,10 @@ constexpr int BM = 128, BN = 128, BK = 32;
 constexpr int LDA = BM + 4;          // k-major A rows, padded (conflict-free stores and reads)
 constexpr int A_STAGE = BK * LDA;    // floats per A stage
 constexpr int B_STAGE = BK * BN;     // floats per B stage
-constexpr int kGroupM = 8;           // tile-rows per L2 group (as the cp.async kernel)
+// Tile-rows per L2 group. At 4096^3 (32 x 32 tiles, 304 CTAs resident) the
+// DRAM reads per launch measured 346 MB with groups of 8 rows, 281 MB with
+// 16 and 506 MB with 32 (A and B hold 134 MB), at the same speed.
+constexpr int kGroupM = 16;
 // Shared-memory layout in bytes from a 1024-byte-aligned base (the 128-byte
 // swizzle repeats every 1024 bytes): staging tile, two B stages, two A
 // stages, two mbarriers.

@@ -72,3 +72,22 @@ def guard_intact(buf: torch.Tensor, M: int, N: int, pad: int = 4096) -> bool:
     head = buf[:pad]
     tail = buf[pad + M * N:]
     return bool(torch.isnan(head).all().item() and torch.isnan(tail).all().item())
+
+
+def kernel_names(fn) -> list:
+    """Names of the kernels one call of fn launches (profiler kernel records;
+    the first session of a process may start its tracer after the launches,
+    so sessions repeat until one records any)."""
+    from torch.profiler import ProfilerActivity, profile
+
+    for _ in range(3):
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events()
+                 if str(getattr(e, "device_type", "")).endswith("CUDA")
+                 and not e.name.startswith(("Memcpy", "Memset"))]
+        if names:
+            return names
+    return names

@@ -15,7 +15,8 @@ import torch
 import oracle
 import register_tiled_matrix_gb300 as rtm
 import workloads
-from tests.parity import assert_bit_exact, assert_close_to_oracle, guard_intact, guarded_output
+from tests.parity import (assert_bit_exact, assert_close_to_oracle, guard_intact, guarded_output,
+                          kernel_names)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -46,25 +47,6 @@ def offset_copy(t: torch.Tensor, floats: int = 1) -> torch.Tensor:
     view.copy_(t)
     assert view.data_ptr() % 16 == 4 * floats % 16
     return view
-
-
-def kernel_names(fn) -> list:
-    """Names of the kernels one call of fn launches (profiler kernel records;
-    the first session of a process may start its tracer after the launches,
-    so sessions repeat until one records any)."""
-    from torch.profiler import ProfilerActivity, profile
-
-    for _ in range(3):
-        torch.cuda.synchronize()
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            fn()
-            torch.cuda.synchronize()
-        names = [e.name for e in prof.events()
-                 if str(getattr(e, "device_type", "")).endswith("CUDA")
-                 and not e.name.startswith(("Memcpy", "Memset"))]
-        if names:
-            return names
-    return names
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
