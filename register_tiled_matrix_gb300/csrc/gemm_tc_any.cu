@@ -25,6 +25,7 @@
 // For M > 128 a second kernel runs the same producers on CTA pairs (256 x 256
 // tiles, tcgen05 cta_group::2; see the section "CTA pairs" below).
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -616,6 +617,70 @@ struct Staged {
     }
 };
 
+// The same for 2-byte accesses (V = 1): lane per element, coalesced along k
+// for A and along n for B; warp w holds rows AR w .. AR w + AR - 1 of A and
+// k-rows BR w .. of B (AR a multiple of 8, so a row's swizzle phase is fixed).
+template <int PT>
+struct Staged1 {
+    static constexpr int PW = PT / 32;
+    static constexpr int AR = HM / PW, AE = BK / 32;
+    static constexpr int BR = BK / PW, BE = HN / 32;
+    static_assert(AR % 8 == 0, "swizzle phase fixed per row");
+    uint16_t a[AR][AE], b[BR][BE];
+
+    __device__ __forceinline__ void load(const Params &p, int tid, int r0, int c0, int k0)
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        const uint16_t *pa = p.A + (size_t)(r0 + warp * AR) * p.K + (k0 + lane);
+        const uint16_t *pb = p.B + (size_t)(k0 + warp * BR) * p.N + (c0 + lane);
+        if (r0 + HM <= p.M && c0 + HN <= p.N && k0 + BK <= p.K) {
+#pragma unroll
+            for (int rr = 0; rr < AR; ++rr)
+#pragma unroll
+                for (int e = 0; e < AE; ++e)
+                    a[rr][e] = __ldg(pa + (size_t)rr * p.K + e * 32);
+#pragma unroll
+            for (int kr = 0; kr < BR; ++kr)
+#pragma unroll
+                for (int e = 0; e < BE; ++e)
+                    b[kr][e] = __ldg(pb + (size_t)kr * p.N + e * 32);
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < AR; ++rr)
+#pragma unroll
+                for (int e = 0; e < AE; ++e)
+                    a[rr][e] = (r0 + warp * AR + rr < p.M && k0 + e * 32 + lane < p.K)
+                                   ? __ldg(pa + (size_t)rr * p.K + e * 32)
+                                   : (uint16_t)0;
+#pragma unroll
+            for (int kr = 0; kr < BR; ++kr)
+#pragma unroll
+                for (int e = 0; e < BE; ++e)
+                    b[kr][e] = (k0 + warp * BR + kr < p.K && c0 + e * 32 + lane < p.N)
+                                   ? __ldg(pb + (size_t)kr * p.N + e * 32)
+                                   : (uint16_t)0;
+        }
+    }
+
+    __device__ __forceinline__ void store(uint8_t *sA, uint8_t *sB, int tid) const
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+        for (int rr = 0; rr < AR; ++rr)
+#pragma unroll
+            for (int e = 0; e < AE; ++e)
+                *reinterpret_cast<uint16_t *>(sA + swz(warp * AR + rr, e * 32 + lane)) = a[rr][e];
+#pragma unroll
+        for (int kr = 0; kr < BR; ++kr)
+#pragma unroll
+            for (int e = 0; e < BE; ++e) {
+                const int n = e * 32 + lane;
+                *reinterpret_cast<uint16_t *>(sB + (n >> 6) * B_ATOM_BYTES + swz(warp * BR + kr, n & 63)) =
+                    b[kr][e];
+            }
+    }
+};
+
 template <bool F16, int V, bool ASYNC, int PW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(PW), 1)
     gemm_tc_any_pair_kernel(const Params p)
@@ -751,77 +816,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(PW), 1)
                 mbar_arrive(&full[oldest]);
                 oldest = oldest + 1 == PSTAGES ? 0 : oldest + 1;
             }
-        } else if constexpr (V == 1) {
-            for (int t = cluster_id; t < ntiles && ok; t += num_clusters) {
-                int m0, n0;
-                pair_tile_coords(t, tiles_m, tiles_n, m0, n0);
-                const int r0 = m0 + (int)rank * HM, c0 = n0 + (int)rank * HN;
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!warp_wait(&empty[stage], phase ^ 1, limit, abort)) {
-                        give_up(p.err, abort);
-                        ok = false;
-                        break;
-                    }
-                    const int k0 = kb * BK;
-                    uint8_t *sA = smem + stage * PSTAGE_BYTES;
-                    uint8_t *sB = sA + PA_BYTES;
-                    {
-                        // Lane per element; all loads of the slice before any store.
-                        // A: warp w fills rows 8w .. 8w+7, lanes along k.
-                        // B: warp w fills k-rows 4w .. 4w+3, lanes along n (two atoms).
-                        constexpr int AR = HM / kPairProducerWarps, AE = BK / 32;
-                        constexpr int BR = BK / kPairProducerWarps, BE = HN / 32;
-                        uint16_t va[AR][AE], vb[BR][BE];
-#pragma unroll
-                        for (int rr = 0; rr < AR; ++rr) {
-                            const int gm = r0 + warp * AR + rr;
-#pragma unroll
-                            for (int e = 0; e < AE; ++e) {
-                                const int gk = k0 + e * 32 + lane;
-                                va[rr][e] = (gm < M && gk < K) ? __ldg(p.A + (size_t)gm * K + gk)
-                                                               : (uint16_t)0;
-                            }
-                        }
-#pragma unroll
-                        for (int kr = 0; kr < BR; ++kr) {
-                            const int gk = k0 + warp * BR + kr;
-#pragma unroll
-                            for (int e = 0; e < BE; ++e) {
-                                const int gn = c0 + e * 32 + lane;
-                                vb[kr][e] = (gk < K && gn < N) ? __ldg(p.B + (size_t)gk * N + gn)
-                                                               : (uint16_t)0;
-                            }
-                        }
-#pragma unroll
-                        for (int rr = 0; rr < AR; ++rr)
-#pragma unroll
-                            for (int e = 0; e < AE; ++e)
-                                *reinterpret_cast<uint16_t *>(
-                                    sA + swz(warp * AR + rr, e * 32 + lane)) = va[rr][e];
-#pragma unroll
-                        for (int kr = 0; kr < BR; ++kr)
-#pragma unroll
-                            for (int e = 0; e < BE; ++e) {
-                                const int n = e * 32 + lane;
-                                *reinterpret_cast<uint16_t *>(sB + (n >> 6) * B_ATOM_BYTES +
-                                                              swz(warp * BR + kr, n & 63)) =
-                                    vb[kr][e];
-                            }
-                    }
-                    fence_proxy_async_shared();
-                    mbar_arrive(&full[stage]);
-                    if (++stage == PSTAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
         } else {
-            // V = 2: register-staged, a ring of three slices per thread — the
-            // loads of the slice two ahead (possibly of a later tile) are issued
-            // before this slice is stored, so a warp keeps up to three slices'
-            // loads in flight.
+            // V = 1 or 2: register-staged. For V = 2 a ring of three slices per
+            // thread: the loads of the slice two ahead (possibly of a later tile)
+            // are issued before this slice is stored, so a warp keeps three
+            // slices' loads in flight. A 2-byte slice takes twice the registers:
+            // two in flight spill (240 bytes) under the 80 registers a thread of
+            // this 672-thread CTA can have, so V = 1 keeps one.
             const int tid = threadIdx.x;
+            using Slice = std::conditional_t<V == 1, Staged1<kPairProducerThreads>,
+                                             Staged<V, kPairProducerThreads>>;
             int lt = cluster_id, lkb = 0, lr0 = 0, lc0 = 0;  // next slice to load
             auto origin = [&](int t) {
                 int m0, n0;
@@ -829,7 +833,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(PW), 1)
                 lr0 = m0 + (int)rank * HM;
                 lc0 = n0 + (int)rank * HN;
             };
-            using Slice = Staged<V, kPairProducerThreads>;
             auto load_next = [&](Slice &buf) {
                 if (lt >= ntiles)
                     return;
@@ -845,12 +848,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(PW), 1)
             long long remaining =
                 (long long)((ntiles - 1 - cluster_id) / num_clusters + 1) * kblocks;
             origin(lt);
-            Slice s0, s1, s2;
-            load_next(s0);
-            load_next(s1);
-            // Store `cur` (the oldest slice loaded) after loading the next one into `fut`.
-            auto step = [&](Slice &cur, Slice &fut) {
-                load_next(fut);
+            // Store `cur` (the oldest slice loaded) into the next stage and announce it.
+            auto publish = [&](Slice &cur) {
                 if (!warp_wait(&empty[stage], phase ^ 1, limit, abort)) {
                     give_up(p.err, abort);
                     return false;
@@ -865,7 +864,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(PW), 1)
                 }
                 return --remaining > 0;
             };
-            while (step(s0, s2) && step(s1, s0) && step(s2, s1)) {
+            if constexpr (V == 1) {
+                Slice s0;
+                do
+                    load_next(s0);
+                while (publish(s0));
+            } else {
+                // load the slice two ahead into `fut`, then publish `cur`
+                auto step = [&](Slice &cur, Slice &fut) {
+                    load_next(fut);
+                    return publish(cur);
+                };
+                Slice s0, s1, s2;
+                load_next(s0);
+                load_next(s1);
+                while (step(s0, s2) && step(s1, s0) && step(s2, s1)) {
+                }
             }
         }
     } else if (warp == kPairMmaWarp) {
