@@ -331,14 +331,15 @@ GEMM_API int gemm_get_device_error(void *stream);
 
 /*
  * gemm_bf16f32_selftest_timeout — failure-detection check for the bounded
- * waits. Launches the gemm_bf16f32 TMA kernel the shape selects (CTA pair for
- * M > 128, single CTA otherwise) on the given buffers with its tensor-memory-
- * access producer muted, so that nothing ever arrives on the stage barriers,
- * and with every wait limited to `wait_limit_ns`. Each waiting warp gives up,
- * the kernel frees its tensor memory, records GEMM_ERR_TIMEOUT in the device
+ * waits. Launches the gemm_bf16f32 kernel the shape and pointers select (CTA
+ * pair for M > 128, single CTA or the transposed K-split kernel otherwise;
+ * for rows off 16-byte boundaries the load-and-swizzle kernels) on the given
+ * buffers with its producer muted (the tensor-memory-access thread, or the
+ * producer warps), so that nothing ever arrives on the stage barriers, and
+ * with every wait limited to `wait_limit_ns`. Each waiting warp gives up, the
+ * kernel frees its tensor memory, records GEMM_ERR_TIMEOUT in the device
  * error word and returns; the GPU context stays usable. C is left
- * unspecified. Same argument rules as gemm_bf16f32, and the shape must take
- * the TMA path (K % 8 == 0, N % 8 == 0, 16-byte-aligned pointers) else
+ * unspecified. Same argument rules as gemm_bf16f32, K > 0, else
  * GEMM_ERR_INVALID_ARG; wait_limit_ns must be in [1e6, 1e10].
  */
 GEMM_API int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K,

@@ -42,7 +42,6 @@ constexpr int UMMA_K = 16;
 constexpr int kProducerWarps = 8;
 constexpr int kProducerThreads = kProducerWarps * 32;
 constexpr int kMmaWarp = kProducerWarps;               // warp 8
-constexpr int kFirstEpilogueWarp = kProducerWarps + 1;  // warps 9..12 (quarters 1,2,3,0)
 constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
 constexpr int kGroupM = 16;
 constexpr int kAsyncDepth = 3;  // K-slices in flight per producer thread (cp.async path)
@@ -73,6 +72,7 @@ struct Params {
     float *C;
     int *err;
     unsigned long long limit_ns;
+    int mute_producer;  // failure-detection self-test: the producer warps load nothing
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &n0)
@@ -172,7 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_any_kernel(const Params p
     const uint64_t limit = p.limit_ns;
 
     if (warp < kProducerWarps) {
-      if constexpr (ASYNC) {
+      if (p.mute_producer) {
+          // nothing arrives on full[]: every wait below gives up
+      } else if constexpr (ASYNC) {
         // ------------------------------------------------ producers (cp.async)
         // V = 2 or 4 (4- or 8-byte copies straight into the swizzled layout,
         // zero-filled outside M, N, K). A thread's copies for a K-slice form
@@ -741,7 +743,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(PW), 1)
         // ------------------------------------------------ producers (both CTAs)
         uint32_t stage = 0, phase = 0;
         bool ok = true;
-        if constexpr (ASYNC) {
+        if (p.mute_producer) {
+            // failure-detection self-test: nothing arrives on full[], every wait gives up
+        } else if constexpr (ASYNC) {
             // V = 4: 8-byte cp.async straight into the swizzled layout, zero-
             // filled outside M, N, K; kPairAsyncDepth slices in flight per thread,
             // a slice announced once the warp's copies of it have landed.
@@ -1047,7 +1051,8 @@ static cudaError_t launch_pair(const TcLaunch &L, cudaStream_t stream)
     }
     const long long ntiles = (long long)((L.M + PM - 1) / PM) * ((L.N + PN - 1) / PN);
     const int clusters = (int)(ntiles < clusters_max ? ntiles : clusters_max);
-    Params p{L.M, L.N, L.K, L.A, L.B, L.C, L.err, (unsigned long long)L.wait_limit_ns};
+    Params p{L.M, L.N, L.K, L.A, L.B, L.C, L.err, (unsigned long long)L.wait_limit_ns,
+             L.mute_producer};
     kernel<<<2 * clusters, kPairThreads, PSMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
@@ -1064,7 +1069,8 @@ static cudaError_t launch(const TcLaunch &L, cudaStream_t stream)
         return e;
     const long long ntiles = (long long)((L.M + BM - 1) / BM) * ((L.N + BN - 1) / BN);
     const int grid = (int)(ntiles < L.sm_count ? ntiles : L.sm_count);
-    Params p{L.M, L.N, L.K, L.A, L.B, L.C, L.err, (unsigned long long)L.wait_limit_ns};
+    Params p{L.M, L.N, L.K, L.A, L.B, L.C, L.err, (unsigned long long)L.wait_limit_ns,
+             L.mute_producer};
     kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }

@@ -276,7 +276,8 @@ int tct_rows(int M);
 int tcs_cols(int N);
 cudaError_t launch_gemm_tc_t(const TcLaunch &p, int splits, bool swap, cudaStream_t stream);
 // The same product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu):
-// operands loaded by producer warps instead of TMA. mute_producer unused.
+// operands loaded by producer warps instead of TMA (mute_producer: they load
+// nothing, so every wait gives up).
 cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);
 // The same on CTA pairs (256 x 256 tiles, each CTA staging half of the
 // operands), for M > 128. Same operand rules; any 4-byte-aligned C.

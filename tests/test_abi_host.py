@@ -96,10 +96,10 @@ def test_tensor_core_alignment_rules(lib, fn):
     assert f(16, 16, 16, A, B, C + 2, None) == -2  # C not 4-byte aligned
 
 
-def test_selftest_needs_tma_shape(lib):
+def test_selftest_needs_k(lib):
     f = lib.gemm_bf16f32_selftest_timeout
     A, B, C = 0x10000000, 0x20000000, 0x30000000
-    assert f(16, 16, 12, A, B, C, 10 ** 8, None) == -1  # K % 8: not a TMA shape
+    assert f(16, 16, 0, A, B, C, 10 ** 8, None) == -1  # K == 0 launches no waiting kernel
 
 
 def test_f32_alignment_rule(lib):

@@ -123,3 +123,22 @@ def test_short_products_keep_the_single_cta_kernel():
     names = kernel_names(lambda: rtm.gemm_bf16f32(Ad, Bd))
     assert any("gemm_tc_any_kernel" in n for n in names), names
     assert not any(PAIR in n for n in names), names
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 258, 130), (520, 1004, 996), (257, 129, 77), (100, 258, 130)],
+                         ids=["pair_4byte", "pair_8byte_cp_async", "pair_2byte", "single_cta_4byte"])
+def test_muted_producers_every_wait_gives_up(M, N, K):
+    """The producer warps load nothing: every bounded wait (stage barriers, the
+    odd CTA's forwarder, the accumulator barriers) runs out after 50 ms, the
+    kernel records a timeout and returns, and the next product is correct."""
+    A, B = workloads.make_inputs(M, N, K, "normal", "bf16", seed=M + N)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = torch.empty(M, N, device=DEV)
+    assert rtm.get_device_error() == 0
+    rtm.gemm_bf16f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
+    assert rtm.get_device_error() == -4
+    assert rtm.get_device_error() == 0, "reading the error word clears it"
+    C = rtm.gemm_bf16f32(Ad, Bd)
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_close_to_oracle(C, A, B, "bf16")
