@@ -1,0 +1,367 @@
+// SIMT FP32 product C = A.B on tall 256 x 64 C tiles (products with N <= 64),
+// fed by the tensor-memory-access (TMA) unit, K split over the CTAs of a
+// thread-block cluster.
+//
+// The register level is the 256 x 64 tile of the cp.async kernel
+// (sgemm_simt.cu, "tall tiles"): 16 x 16 threads, 16 x 4 accumulators per
+// thread as four 4 x 4 sub-blocks spaced 64 rows apart, 32-deep K slices,
+// and per k 4 LDS.128 of A and 1 of B feeding 64 FMAs, here as 32 packed
+// two-wide FMAs ("理解 Register Tiling", section "关键循环"; "寄存器Tiling跨架构解析",
+// sections 1.1 and 6.3). As in sgemm_tma.cu, one thread issues two TMA loads
+// per slice — a 256 m x 32 k box of A (row-major, 128-byte swizzle) into a
+// staging tile and a 32 k x 64 n box of B into a B stage — and the threads
+// transpose A into the k-major layout the fragment loads read (each thread
+// two 4 x 4 blocks: 8 LDS.128 + 8 STS.128 per slice). In the cp.async kernel
+// every thread issued 34 copies per slice for the same data.
+//
+// One k-major A stage (not two): with two the CTA would need 114 KB of shared
+// memory and one CTA per SM; with one it needs 83 KB, two CTAs share an SM,
+// and each covers the other's transpose. Per slice: wait for the slice's
+// loads, transpose A, a CTA barrier, thread 0 issues the next slice (its A
+// into the free staging tile, its B into the other B stage), the k loop, a
+// CTA barrier (the A stage is free again).
+//
+// K is split over the S CTAs of a cluster (grid (tiles, S), cluster (1, S, 1),
+// S in {1, 2, 4, 8}); each parks its partial tile in its shared memory and,
+// after a cluster barrier, adds rows [rank * 256 / S, +256 / S) of the S
+// partials read through distributed shared memory in rank order (the same
+// sum on every call), then stores them; a second barrier keeps the partials
+// alive until read. Every mbarrier wait is bounded; a wait that gives up
+// records GEMM_ERR_TIMEOUT and raises the CTA's abort flag, after which
+// thread 0 issues nothing more, and every thread still reaches every barrier.
+//
+// Requirements (checked by the launcher): K % 4 == 0, N % 4 == 0, A and B
+// 16-byte aligned (TMA row strides and bases).
+#include <atomic>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace rtm {
+namespace simt_tma_tall {
+
+constexpr int kThreads = 256;
+constexpr int BM = 256, BN = 64, BK = 32;
+constexpr int LDA = BM + 4;          // k-major A rows, padded (conflict-free stores and reads)
+constexpr int A_STAGE = BK * LDA;    // floats
+constexpr int B_STAGE = BK * BN;     // floats
+constexpr int kGroupM = 16;          // tile-rows per L2 group
+// Shared-memory layout in bytes from a 1024-byte-aligned base: staging tile
+// (256 rows of 128 bytes, 128-byte swizzle), two B stages, one A stage, two
+// mbarriers.
+constexpr int OFF_ST = 0;
+constexpr int OFF_B = BM * BK * 4;
+constexpr int OFF_A = OFF_B + 2 * B_STAGE * 4;
+constexpr int OFF_BAR = OFF_A + A_STAGE * 4;
+constexpr int SMEM_BYTES = OFF_BAR + 16 + 1024;  // + room to align the base
+constexpr uint32_t kSliceBytes = (BM * BK + BK * BN) * 4;
+constexpr int kSpreadSmem = 120 * 1024;  // more than half of an SM: one CTA per SM
+constexpr int kPartPitch = BN + 4;
+static_assert(BM * kPartPitch * 4 <= OFF_BAR, "the partial tile fits below the barriers");
+static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
+
+__device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n, int &tile_m,
+                                              int &tile_n)
+{
+    const int group_size = kGroupM * tiles_n;
+    const int group = bid / group_size;
+    const int first_m = group * kGroupM;
+    const int rows = min(tiles_m - first_m, kGroupM);
+    const int in_group = bid - group * group_size;
+    tile_m = first_m + in_group % rows;
+    tile_n = in_group / rows;
+}
+
+__device__ __forceinline__ float4 lds128(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, float x, float y, float z, float w)
+{
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y), "f"(z),
+                 "f"(w)
+                 : "memory");
+}
+
+// One k-step of the 16 x 4 register tile: acc[i][j] += a[i] * b[j] as 32
+// packed two-wide FMAs on row pairs (2 i', 2 i' + 1) of column j with b[j] in
+// both halves (each half rounds like a scalar fmaf); row pairs in serpentine
+// order across columns.
+__device__ __forceinline__ void outer_product_step(float (&acc)[16][4], const float (&a)[16],
+                                                   const float (&b)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 bb = make_float2(b[j], b[j]);
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+            const int i2 = (j & 1) ? 7 - ii : ii;
+            float2 d = make_float2(acc[2 * i2][j], acc[2 * i2 + 1][j]);
+            d = __ffma2_rn(make_float2(a[2 * i2], a[2 * i2 + 1]), bb, d);
+            acc[2 * i2][j] = d.x;
+            acc[2 * i2 + 1][j] = d.y;
+        }
+    }
+}
+
+// Rows [rank * BM / S, +BM / S) of the cluster's S partial tiles, added in
+// rank order and stored to C (masked at M and N).
+template <bool C_VEC, int S>
+__device__ __forceinline__ void cluster_add_parts(const float *part, int M, int N, float *C,
+                                                  int m0, int n0, uint32_t rank)
+{
+    constexpr int ROWS = BM / S;
+    constexpr int COUNT4 = ROWS * (BN / 4);
+    constexpr int ITERS = COUNT4 / kThreads;
+    static_assert(COUNT4 % kThreads == 0, "every thread adds whole float4s");
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+        const int f = (int)threadIdx.x + it * kThreads;
+        const int r = (int)rank * ROWS + f / (BN / 4), c = (f % (BN / 4)) * 4;
+        const uint32_t local = smem_u32(part + r * kPartPitch + c);
+        float4 v[S];
+#pragma unroll
+        for (int q = 0; q < S; ++q)
+            v[q] = S == 1 ? lds128(local) : ld_shared_cluster_v4(mapa_shared(local, (uint32_t)q));
+        float4 sum = v[0];
+#pragma unroll
+        for (int q = 1; q < S; ++q) {
+            sum.x += v[q].x;
+            sum.y += v[q].y;
+            sum.z += v[q].z;
+            sum.w += v[q].w;
+        }
+        const int gm = m0 + r, gn = n0 + c;
+        if (gm >= M)
+            continue;
+        float *crow = C + (size_t)gm * N;
+        if constexpr (C_VEC) {
+            if (gn < N)
+                *reinterpret_cast<float4 *>(crow + gn) = sum;
+        } else {
+            const float w[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gn + j < N)
+                    crow[gn + j] = w[j];
+        }
+    }
+}
+
+template <bool C_VEC>
+__global__ void __launch_bounds__(kThreads, 2)
+    sgemm_tma_tall_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int kchunk,
+                          float *__restrict__ C, int *err, uint64_t wait_limit_ns)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    float *stA = reinterpret_cast<float *>(base + OFF_ST);
+    float *sB = reinterpret_cast<float *>(base + OFF_B);
+    float *sA = reinterpret_cast<float *>(base + OFF_A);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + OFF_BAR);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    int tile_m, tile_n;
+    tile_of_block((int)blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tile_m, tile_n);
+    const int m0 = tile_m * BM, n0 = tile_n * BN;
+    // 16 x 16 threads: rows h * 64 + tm * 4 + i, columns tn * 4 + j; a warp
+    // reads 4 distinct 16-byte A fragments and 8 B fragments per k.
+    const int tm = (warp >> 1) * 4 + (((lane >> 2) & 1) | ((lane >> 3) & 2));
+    const int tn = (warp & 1) * 8 + ((lane & 3) | ((lane >> 1) & 4));
+    const int ks_begin = (int)blockIdx.y * (kchunk / BK);
+    const int ktiles = max(0, min((K + BK - 1) / BK - ks_begin, kchunk / BK));
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fence_mbarrier_init();
+        abort_flag = 0;
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    __syncthreads();
+
+    int issued = 0, confirmed = 0;
+    auto issue = [&](int s) {
+        uint64_t *bar = &full[s & 1];
+        mbar_arrive_expect_tx(bar, kSliceBytes);
+        tma_load_2d(smem_u32(stA), &tmA, bar, (ks_begin + s) * BK, m0);
+        tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, n0, (ks_begin + s) * BK);
+        ++issued;
+    };
+    // Transpose: thread (r4, q) moves rows 4 r4 + 128 b .. + 3 (b = 0, 1), k
+    // 4 q .. 4 q + 3 of the staging tile (16-byte chunk c of row r at
+    // c ^ (r mod 8)) into the k-major A stage.
+    const int r4 = warp * 4 + (lane & 3);
+    const int q = ((lane >> 3) << 1) | ((lane >> 2) & 1);
+    const uint32_t st_base = smem_u32(stA);
+    const uint32_t a_dst = smem_u32(sA + (4 * q) * LDA + 4 * r4);
+    auto transpose = [&](int s) {
+        if (mbar_wait_bounded(&full[s & 1], (uint32_t)((s >> 1) & 1), wait_limit_ns, &abort_flag)) {
+            if (tid == 0 && confirmed == s)
+                confirmed = s + 1;
+        } else {
+            atomicCAS(err, 0, kDevErrTimeout);
+            abort_flag = 1;
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            float4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = 128 * b + 4 * r4 + i;
+                v[i] = lds128(st_base + (uint32_t)(row * (BK * 4) + ((q ^ (row & 7)) * 16)));
+            }
+            const uint32_t d = a_dst + (uint32_t)(128 * b * 4);
+            sts128(d + 0 * LDA * 4, v[0].x, v[1].x, v[2].x, v[3].x);
+            sts128(d + 1 * LDA * 4, v[0].y, v[1].y, v[2].y, v[3].y);
+            sts128(d + 2 * LDA * 4, v[0].z, v[1].z, v[2].z, v[3].z);
+            sts128(d + 3 * LDA * 4, v[0].w, v[1].w, v[2].w, v[3].w);
+        }
+    };
+
+    float acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            acc[i][j] = 0.0f;
+
+    if (ktiles > 0 && tid == 0)
+        issue(0);
+    for (int kt = 0; kt < ktiles; ++kt) {
+        transpose(kt);
+        __syncthreads();  // the A stage holds slice kt; the staging tile is free
+        if (tid == 0 && kt + 1 < ktiles && !abort_flag)
+            issue(kt + 1);
+        const float *cA = sA + tm * 4;
+        const float *cB = sB + (kt & 1) * B_STAGE + tn * 4;
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            float a[16], b[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float4 v = *reinterpret_cast<const float4 *>(cA + k * LDA + h * 64);
+                a[h * 4 + 0] = v.x;
+                a[h * 4 + 1] = v.y;
+                a[h * 4 + 2] = v.z;
+                a[h * 4 + 3] = v.w;
+            }
+            const float4 v = *reinterpret_cast<const float4 *>(cB + k * BN);
+            b[0] = v.x;
+            b[1] = v.y;
+            b[2] = v.z;
+            b[3] = v.w;
+            outer_product_step(acc, a, b);
+        }
+        __syncthreads();  // the A stage and B stage kt % 2 are free
+    }
+    if (tid == 0 && confirmed < issued) {
+        int never = 0;
+        for (int s = confirmed; s < issued; ++s)
+            mbar_wait_bounded(&full[s & 1], (uint32_t)((s >> 1) & 1), wait_limit_ns, &never);
+    }
+
+    // Park the partial tile (the stages are free: the last barrier above).
+    float *part = reinterpret_cast<float *>(base);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float *v = &acc[h * 4 + i][0];
+            *reinterpret_cast<float4 *>(part + (h * 64 + tm * 4 + i) * kPartPitch + tn * 4) =
+                make_float4(v[0], v[1], v[2], v[3]);
+        }
+    const uint32_t rank = blockIdx.y;  // cluster (1, S, 1)
+    if (gridDim.y == 1) {
+        __syncthreads();
+        cluster_add_parts<C_VEC, 1>(part, M, N, C, m0, n0, 0);
+        return;
+    }
+    cluster_sync();
+    switch (gridDim.y) {
+    case 2: cluster_add_parts<C_VEC, 2>(part, M, N, C, m0, n0, rank); break;
+    case 4: cluster_add_parts<C_VEC, 4>(part, M, N, C, m0, n0, rank); break;
+    default: cluster_add_parts<C_VEC, 8>(part, M, N, C, m0, n0, rank); break;
+    }
+    cluster_sync();
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// rows x cols fp32 matrix, row-major, rows cols * 4 bytes apart; box of
+// box_rows x box_cols; zeros outside the matrix.
+static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const float *base, uint64_t rows,
+                       uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+                       CUtensorMapSwizzle swizzle)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+} // namespace simt_tma_tall
+
+cudaError_t launch_sgemm_f32_tma_tall(int M, int N, int K, const float *A, const float *B,
+                                      float *C, const SimtTma &tma, int splits, int kchunk,
+                                      bool spread, cudaStream_t stream)
+{
+    using namespace simt_tma_tall;
+    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B) ||
+        (splits != 1 && splits != 2 && splits != 4 && splits != 8) || kchunk % BK != 0 ||
+        kchunk <= 0 || (long long)splits * kchunk < K)
+        return cudaErrorInvalidValue;
+    const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (tiles == 0)
+        return cudaSuccess;
+    if (tiles > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    auto fn = reinterpret_cast<EncodeTiledFn>(tma.encode_tiled);
+    CUtensorMap ta, tb;
+    if (!encode_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;  // N % 4 == 0 already
+    auto kernel = c_vec ? sgemm_tma_tall_kernel<true> : sgemm_tma_tall_kernel<false>;
+    static std::atomic<uint64_t> done_vec{0}, done_any{0};
+    const cudaError_t e = set_smem_limit_once(kernel, kSpreadSmem, c_vec ? done_vec : done_any);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles, (unsigned)splits, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = spread ? kSpreadSmem : SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, kchunk, C, tma.err,
+                              tma.wait_limit_ns);
+}
+
+} // namespace rtm
