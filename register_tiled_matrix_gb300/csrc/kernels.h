@@ -130,13 +130,14 @@ cudaError_t launch_sgemm_f32_tma_cluster(int M, int N, int K, const float *A, co
                                          float *C, const SimtTma &tma, int splits, int kchunk,
                                          bool spread, long long tile_first, long long tile_count,
                                          cudaStream_t stream);
-// The same TMA-fed loop on tall 256 x 64 tiles (16 x 4 outputs per thread;
-// sgemm_tma_tall.cu), K split over `splits` (1, 2, 4 or 8) CTAs of a cluster
-// in chunks of `kchunk` (a multiple of 32, splits * kchunk >= K); spread: one
-// CTA per SM. Same operand rules as launch_sgemm_f32_tma.
-cudaError_t launch_sgemm_f32_tma_tall(int M, int N, int K, const float *A, const float *B,
-                                      float *C, const SimtTma &tma, int splits, int kchunk,
-                                      bool spread, cudaStream_t stream);
+// The same TMA-fed loop on rectangular tiles (sgemm_tma_rect.cu): `tile` 256 x 64
+// (16 x 4 outputs per thread, tall, narrow products) or 64 x 256 (4 x 16,
+// products of 33-64 rows), K split over `splits` (1, 2, 4 or 8) CTAs of a
+// cluster in chunks of `kchunk` (a multiple of 32, splits * kchunk >= K);
+// spread: one CTA per SM. Same operand rules as launch_sgemm_f32_tma.
+cudaError_t launch_sgemm_f32_tma_rect(SimtTile tile, int M, int N, int K, const float *A,
+                                      const float *B, float *C, const SimtTma &tma, int splits,
+                                      int kchunk, bool spread, cudaStream_t stream);
 // Stream-K over the TMA-fed 128 x 128 tiles (sgemm_tma.cu): `ctas` CTAs take
 // equal ranges of the tiles x K-slices iterations; tiles split between CTAs
 // are added by a fixup kernel in a fixed order (repeatable bit for bit).

@@ -685,9 +685,10 @@ cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B
     const SimtTile t = simt_resolve_tile(tile, M, N);
     if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B))
         return launch_sgemm_f32_tma(M, N, K, A, B, C, *tma, -1, stream);
-    if (tma && t.m == kTallTileM && t.n == kNarrowN && sgemm_tma_eligible(M, N, K, A, B))
-        return launch_sgemm_f32_tma_tall(M, N, K, A, B, C, *tma, 1, (K + kSliceK - 1) / kSliceK * kSliceK,
-                                         false, stream);
+    if (tma && ((t.m == kTallTileM && t.n == kNarrowN) || (t.m == kShortTileM && t.n == kWideTileN)) &&
+        sgemm_tma_eligible(M, N, K, A, B))
+        return launch_sgemm_f32_tma_rect(t, M, N, K, A, B, C, *tma, 1,
+                                         (K + kSliceK - 1) / kSliceK * kSliceK, false, stream);
     return launch_tile<simt::kPlain>(t, M, N, K, A, B, C, stream);
 }
 
@@ -793,8 +794,9 @@ cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const 
     if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B))
         return launch_sgemm_f32_tma_cluster(M, N, K, A, B, C, *tma, plan.splits, plan.kchunk,
                                             plan.spread, 0, -1, stream);
-    if (tma && t.m == kTallTileM && t.n == kNarrowN && sgemm_tma_eligible(M, N, K, A, B))
-        return launch_sgemm_f32_tma_tall(M, N, K, A, B, C, *tma, plan.splits, plan.kchunk,
+    if (tma && ((t.m == kTallTileM && t.n == kNarrowN) || (t.m == kShortTileM && t.n == kWideTileN)) &&
+        sgemm_tma_eligible(M, N, K, A, B))
+        return launch_sgemm_f32_tma_rect(t, M, N, K, A, B, C, *tma, plan.splits, plan.kchunk,
                                          plan.spread, stream);
     return launch_tile<simt::kSplitCluster>(t, M, N, K, A, B, C, stream, plan.splits, plan.kchunk,
                                             plan.spread);

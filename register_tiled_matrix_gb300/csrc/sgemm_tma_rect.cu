@@ -1,29 +1,30 @@
-// SIMT FP32 product C = A.B on tall 256 x 64 C tiles (products with N <= 64),
-// fed by the tensor-memory-access (TMA) unit, K split over the CTAs of a
-// thread-block cluster.
+// SIMT FP32 product C = A.B on rectangular C tiles fed by the tensor-memory-
+// access (TMA) unit: 256 x 64 tiles for tall, narrow products (N <= 64) and
+// 64 x 256 tiles for short ones (33 <= M <= 64), K split over the CTAs of a
+// thread-block cluster or not.
 //
-// The register level is the 256 x 64 tile of the cp.async kernel
-// (sgemm_simt.cu, "tall tiles"): 16 x 16 threads, 16 x 4 accumulators per
-// thread as four 4 x 4 sub-blocks spaced 64 rows apart, 32-deep K slices,
-// and per k 4 LDS.128 of A and 1 of B feeding 64 FMAs, here as 32 packed
+// The register level is the cp.async kernel's (sgemm_simt.cu) for the same
+// tiles: 16 x 16 threads, (BM / 16) x (BN / 16) accumulators per thread as
+// 4 x 4 sub-blocks spaced 64 rows or columns apart, 32-deep K slices, and per
+// k BM / 64 LDS.128 of A and BN / 64 of B feeding 64 FMAs, here as 32 packed
 // two-wide FMAs ("理解 Register Tiling", section "关键循环"; "寄存器Tiling跨架构解析",
 // sections 1.1 and 6.3). As in sgemm_tma.cu, one thread issues two TMA loads
-// per slice — a 256 m x 32 k box of A (row-major, 128-byte swizzle) into a
-// staging tile and a 32 k x 64 n box of B into a B stage — and the threads
-// transpose A into the k-major layout the fragment loads read (each thread
-// two 4 x 4 blocks: 8 LDS.128 + 8 STS.128 per slice). In the cp.async kernel
-// every thread issued 34 copies per slice for the same data.
+// per slice — a BM m x 32 k box of A (row-major, 128-byte swizzle) into a
+// staging tile and a 32 k x BN n box of B into a B stage — and the threads
+// transpose A into the k-major layout the fragment loads read (4 x 4 blocks,
+// 4 LDS.128 + 4 STS.128 each). In the cp.async kernel every thread issued
+// 34 (tall) or 24 (short) copies per slice for the same data.
 //
-// One k-major A stage (not two): with two the CTA would need 114 KB of shared
-// memory and one CTA per SM; with one it needs 83 KB, two CTAs share an SM,
-// and each covers the other's transpose. Per slice: wait for the slice's
-// loads, transpose A, a CTA barrier, thread 0 issues the next slice (its A
-// into the free staging tile, its B into the other B stage), the k loop, a
-// CTA barrier (the A stage is free again).
+// One k-major A stage (not two): for 256-row tiles two stages would need
+// 114 KB of shared memory and one CTA per SM; with one the CTA needs 81 KB,
+// two CTAs share an SM, and each covers the other's transpose. Per slice:
+// wait for the slice's loads, transpose A, a CTA barrier, thread 0 issues the
+// next slice (its A into the free staging tile, its B into the other B
+// stage), the k loop, a CTA barrier (the A stage is free again).
 //
 // K is split over the S CTAs of a cluster (grid (tiles, S), cluster (1, S, 1),
 // S in {1, 2, 4, 8}); each parks its partial tile in its shared memory and,
-// after a cluster barrier, adds rows [rank * 256 / S, +256 / S) of the S
+// after a cluster barrier, adds rows [rank * BM / S, +BM / S) of the S
 // partials read through distributed shared memory in rank order (the same
 // sum on every call), then stores them; a second barrier keeps the partials
 // alive until read. Every mbarrier wait is bounded; a wait that gives up
@@ -42,27 +43,35 @@
 #include "ptx.cuh"
 
 namespace rtm {
-namespace simt_tma_tall {
+namespace simt_tma_rect {
 
 constexpr int kThreads = 256;
-constexpr int BM = 256, BN = 64, BK = 32;
-constexpr int LDA = BM + 4;          // k-major A rows, padded (conflict-free stores and reads)
-constexpr int A_STAGE = BK * LDA;    // floats
-constexpr int B_STAGE = BK * BN;     // floats
+constexpr int BK = 32;
 constexpr int kGroupM = 16;          // tile-rows per L2 group
-// Shared-memory layout in bytes from a 1024-byte-aligned base: staging tile
-// (256 rows of 128 bytes, 128-byte swizzle), two B stages, one A stage, two
-// mbarriers.
-constexpr int OFF_ST = 0;
-constexpr int OFF_B = BM * BK * 4;
-constexpr int OFF_A = OFF_B + 2 * B_STAGE * 4;
-constexpr int OFF_BAR = OFF_A + A_STAGE * 4;
-constexpr int SMEM_BYTES = OFF_BAR + 16 + 1024;  // + room to align the base
-constexpr uint32_t kSliceBytes = (BM * BK + BK * BN) * 4;
 constexpr int kSpreadSmem = 120 * 1024;  // more than half of an SM: one CTA per SM
-constexpr int kPartPitch = BN + 4;
-static_assert(BM * kPartPitch * 4 <= OFF_BAR, "the partial tile fits below the barriers");
-static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
+
+// Shared-memory layout in bytes from a 1024-byte-aligned base: staging tile
+// (BM rows of 128 bytes, 128-byte swizzle), two B stages, one k-major A stage
+// (rows padded to BM + 4 floats: conflict-free stores and reads), two
+// mbarriers; the partial tile of the cluster split (rows padded to BN + 4)
+// reuses the stages.
+template <int BM, int BN>
+struct Shape {
+    static_assert((BM == 256 && BN == 64) || (BM == 64 && BN == 256), "tall or short tiles");
+    static constexpr int TM = BM / 16, TN = BN / 16;  // accumulators per thread
+    static constexpr int LDA = BM + 4;
+    static constexpr int A_STAGE = BK * LDA;          // floats
+    static constexpr int B_STAGE = BK * BN;           // floats
+    static constexpr int OFF_ST = 0;
+    static constexpr int OFF_B = BM * BK * 4;
+    static constexpr int OFF_A = OFF_B + 2 * B_STAGE * 4;
+    static constexpr int OFF_BAR = OFF_A + A_STAGE * 4;
+    static constexpr int SMEM_BYTES = OFF_BAR + 16 + 1024;  // + room to align the base
+    static constexpr uint32_t kSliceBytes = (BM * BK + BK * BN) * 4;
+    static constexpr int kPartPitch = BN + 4;
+    static_assert(BM * kPartPitch * 4 <= OFF_BAR, "the partial tile fits below the barriers");
+    static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
+};
 
 __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n, int &tile_m,
                                               int &tile_n)
@@ -92,19 +101,20 @@ __device__ __forceinline__ void sts128(uint32_t addr, float x, float y, float z,
                  : "memory");
 }
 
-// One k-step of the 16 x 4 register tile: acc[i][j] += a[i] * b[j] as 32
-// packed two-wide FMAs on row pairs (2 i', 2 i' + 1) of column j with b[j] in
-// both halves (each half rounds like a scalar fmaf); row pairs in serpentine
-// order across columns.
-__device__ __forceinline__ void outer_product_step(float (&acc)[16][4], const float (&a)[16],
-                                                   const float (&b)[4])
+// One k-step of the TM x TN register tile: acc[i][j] += a[i] * b[j] as
+// TM * TN / 2 packed two-wide FMAs on row pairs (2 i', 2 i' + 1) of column j
+// with b[j] in both halves (each half rounds like a scalar fmaf); row pairs in
+// serpentine order across columns.
+template <int TM, int TN>
+__device__ __forceinline__ void outer_product_step(float (&acc)[TM][TN], const float (&a)[TM],
+                                                   const float (&b)[TN])
 {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < TN; ++j) {
         const float2 bb = make_float2(b[j], b[j]);
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii) {
-            const int i2 = (j & 1) ? 7 - ii : ii;
+        for (int ii = 0; ii < TM / 2; ++ii) {
+            const int i2 = (j & 1) ? TM / 2 - 1 - ii : ii;
             float2 d = make_float2(acc[2 * i2][j], acc[2 * i2 + 1][j]);
             d = __ffma2_rn(make_float2(a[2 * i2], a[2 * i2 + 1]), bb, d);
             acc[2 * i2][j] = d.x;
@@ -115,10 +125,11 @@ __device__ __forceinline__ void outer_product_step(float (&acc)[16][4], const fl
 
 // Rows [rank * BM / S, +BM / S) of the cluster's S partial tiles, added in
 // rank order and stored to C (masked at M and N).
-template <bool C_VEC, int S>
+template <int BM, int BN, bool C_VEC, int S>
 __device__ __forceinline__ void cluster_add_parts(const float *part, int M, int N, float *C,
                                                   int m0, int n0, uint32_t rank)
 {
+    constexpr int kPartPitch = Shape<BM, BN>::kPartPitch;
     constexpr int ROWS = BM / S;
     constexpr int COUNT4 = ROWS * (BN / 4);
     constexpr int ITERS = COUNT4 / kThreads;
@@ -157,20 +168,22 @@ __device__ __forceinline__ void cluster_add_parts(const float *part, int M, int 
     }
 }
 
-template <bool C_VEC>
+template <int BM, int BN, bool C_VEC>
 __global__ void __launch_bounds__(kThreads, 2)
-    sgemm_tma_tall_kernel(const __grid_constant__ CUtensorMap tmA,
+    sgemm_tma_rect_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int kchunk,
                           float *__restrict__ C, int *err, uint64_t wait_limit_ns)
 {
+    using Sh = Shape<BM, BN>;
+    constexpr int TM = Sh::TM, TN = Sh::TN, LDA = Sh::LDA;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int abort_flag;
     const uint32_t raw = smem_u32(smem_raw);
     unsigned char *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    float *stA = reinterpret_cast<float *>(base + OFF_ST);
-    float *sB = reinterpret_cast<float *>(base + OFF_B);
-    float *sA = reinterpret_cast<float *>(base + OFF_A);
-    uint64_t *full = reinterpret_cast<uint64_t *>(base + OFF_BAR);
+    float *stA = reinterpret_cast<float *>(base + Sh::OFF_ST);
+    float *sB = reinterpret_cast<float *>(base + Sh::OFF_B);
+    float *sA = reinterpret_cast<float *>(base + Sh::OFF_A);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + Sh::OFF_BAR);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -178,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     int tile_m, tile_n;
     tile_of_block((int)blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tile_m, tile_n);
     const int m0 = tile_m * BM, n0 = tile_n * BN;
-    // 16 x 16 threads: rows h * 64 + tm * 4 + i, columns tn * 4 + j; a warp
-    // reads 4 distinct 16-byte A fragments and 8 B fragments per k.
+    // 16 x 16 threads: rows rh * 64 + tm * 4 + i, columns ch * 64 + tn * 4 + j;
+    // a warp reads 4 distinct 16-byte A fragments and 8 B fragments per load.
     const int tm = (warp >> 1) * 4 + (((lane >> 2) & 1) | ((lane >> 3) & 2));
     const int tn = (warp & 1) * 8 + ((lane & 3) | ((lane >> 1) & 4));
     const int ks_begin = (int)blockIdx.y * (kchunk / BK);
@@ -198,14 +211,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     int issued = 0, confirmed = 0;
     auto issue = [&](int s) {
         uint64_t *bar = &full[s & 1];
-        mbar_arrive_expect_tx(bar, kSliceBytes);
+        mbar_arrive_expect_tx(bar, Sh::kSliceBytes);
         tma_load_2d(smem_u32(stA), &tmA, bar, (ks_begin + s) * BK, m0);
-        tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, n0, (ks_begin + s) * BK);
+        tma_load_2d(smem_u32(sB + (s & 1) * Sh::B_STAGE), &tmB, bar, n0, (ks_begin + s) * BK);
         ++issued;
     };
-    // Transpose: thread (r4, q) moves rows 4 r4 + 128 b .. + 3 (b = 0, 1), k
-    // 4 q .. 4 q + 3 of the staging tile (16-byte chunk c of row r at
-    // c ^ (r mod 8)) into the k-major A stage.
+    // Transpose: thread (r4, q) moves rows 4 r4 + 128 b .. + 3, k 4 q .. 4 q + 3
+    // of the staging tile (16-byte chunk c of row r at c ^ (r mod 8)) into the
+    // k-major A stage; 64-row tiles need only the threads with r4 < 16.
     const int r4 = warp * 4 + (lane & 3);
     const int q = ((lane >> 3) << 1) | ((lane >> 2) & 1);
     const uint32_t st_base = smem_u32(stA);
@@ -218,8 +231,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             atomicCAS(err, 0, kDevErrTimeout);
             abort_flag = 1;
         }
+        if (4 * r4 >= BM)
+            return;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < (BM + 127) / 128; ++b) {
             float4 v[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -234,11 +249,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     };
 
-    float acc[16][4];
+    float acc[TM][TN];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < TN; ++j)
             acc[i][j] = 0.0f;
 
     if (ktiles > 0 && tid == 0)
@@ -249,24 +264,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (tid == 0 && kt + 1 < ktiles && !abort_flag)
             issue(kt + 1);
         const float *cA = sA + tm * 4;
-        const float *cB = sB + (kt & 1) * B_STAGE + tn * 4;
+        const float *cB = sB + (kt & 1) * Sh::B_STAGE + tn * 4;
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-            float a[16], b[4];
+            float a[TM], b[TN];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < TM / 4; ++h) {
                 const float4 v = *reinterpret_cast<const float4 *>(cA + k * LDA + h * 64);
                 a[h * 4 + 0] = v.x;
                 a[h * 4 + 1] = v.y;
                 a[h * 4 + 2] = v.z;
                 a[h * 4 + 3] = v.w;
             }
-            const float4 v = *reinterpret_cast<const float4 *>(cB + k * BN);
-            b[0] = v.x;
-            b[1] = v.y;
-            b[2] = v.z;
-            b[3] = v.w;
-            outer_product_step(acc, a, b);
+#pragma unroll
+            for (int h = 0; h < TN / 4; ++h) {
+                const float4 v = *reinterpret_cast<const float4 *>(cB + k * BN + h * 64);
+                b[h * 4 + 0] = v.x;
+                b[h * 4 + 1] = v.y;
+                b[h * 4 + 2] = v.z;
+                b[h * 4 + 3] = v.w;
+            }
+            outer_product_step<TM, TN>(acc, a, b);
         }
         __syncthreads();  // the A stage and B stage kt % 2 are free
     }
@@ -279,24 +297,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Park the partial tile (the stages are free: the last barrier above).
     float *part = reinterpret_cast<float *>(base);
 #pragma unroll
-    for (int h = 0; h < 4; ++h)
+    for (int rh = 0; rh < TM / 4; ++rh)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float *v = &acc[h * 4 + i][0];
-            *reinterpret_cast<float4 *>(part + (h * 64 + tm * 4 + i) * kPartPitch + tn * 4) =
-                make_float4(v[0], v[1], v[2], v[3]);
-        }
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int ch = 0; ch < TN / 4; ++ch) {
+                const float *v = &acc[rh * 4 + i][ch * 4];
+                *reinterpret_cast<float4 *>(part + (rh * 64 + tm * 4 + i) * Sh::kPartPitch + ch * 64 +
+                                            tn * 4) = make_float4(v[0], v[1], v[2], v[3]);
+            }
     const uint32_t rank = blockIdx.y;  // cluster (1, S, 1)
     if (gridDim.y == 1) {
         __syncthreads();
-        cluster_add_parts<C_VEC, 1>(part, M, N, C, m0, n0, 0);
+        cluster_add_parts<BM, BN, C_VEC, 1>(part, M, N, C, m0, n0, 0);
         return;
     }
     cluster_sync();
     switch (gridDim.y) {
-    case 2: cluster_add_parts<C_VEC, 2>(part, M, N, C, m0, n0, rank); break;
-    case 4: cluster_add_parts<C_VEC, 4>(part, M, N, C, m0, n0, rank); break;
-    default: cluster_add_parts<C_VEC, 8>(part, M, N, C, m0, n0, rank); break;
+    case 2: cluster_add_parts<BM, BN, C_VEC, 2>(part, M, N, C, m0, n0, rank); break;
+    case 4: cluster_add_parts<BM, BN, C_VEC, 4>(part, M, N, C, m0, n0, rank); break;
+    default: cluster_add_parts<BM, BN, C_VEC, 8>(part, M, N, C, m0, n0, rank); break;
     }
     cluster_sync();
 }
@@ -321,13 +341,12 @@ static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const float *base, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-} // namespace simt_tma_tall
-
-cudaError_t launch_sgemm_f32_tma_tall(int M, int N, int K, const float *A, const float *B,
-                                      float *C, const SimtTma &tma, int splits, int kchunk,
-                                      bool spread, cudaStream_t stream)
+template <int BM, int BN>
+static cudaError_t launch_rect(int M, int N, int K, const float *A, const float *B, float *C,
+                               const SimtTma &tma, int splits, int kchunk, bool spread,
+                               cudaStream_t stream)
 {
-    using namespace simt_tma_tall;
+    using Sh = Shape<BM, BN>;
     if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B) ||
         (splits != 1 && splits != 2 && splits != 4 && splits != 8) || kchunk % BK != 0 ||
         kchunk <= 0 || (long long)splits * kchunk < K)
@@ -343,7 +362,7 @@ cudaError_t launch_sgemm_f32_tma_tall(int M, int N, int K, const float *A, const
         !encode_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;  // N % 4 == 0 already
-    auto kernel = c_vec ? sgemm_tma_tall_kernel<true> : sgemm_tma_tall_kernel<false>;
+    auto kernel = c_vec ? sgemm_tma_rect_kernel<BM, BN, true> : sgemm_tma_rect_kernel<BM, BN, false>;
     static std::atomic<uint64_t> done_vec{0}, done_any{0};
     const cudaError_t e = set_smem_limit_once(kernel, kSpreadSmem, c_vec ? done_vec : done_any);
     if (e != cudaSuccess)
@@ -351,7 +370,7 @@ cudaError_t launch_sgemm_f32_tma_tall(int M, int N, int K, const float *A, const
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)tiles, (unsigned)splits, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = spread ? kSpreadSmem : SMEM_BYTES;
+    cfg.dynamicSmemBytes = spread ? kSpreadSmem : Sh::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -362,6 +381,20 @@ cudaError_t launch_sgemm_f32_tma_tall(int M, int N, int K, const float *A, const
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, kchunk, C, tma.err,
                               tma.wait_limit_ns);
+}
+
+} // namespace simt_tma_rect
+
+cudaError_t launch_sgemm_f32_tma_rect(SimtTile tile, int M, int N, int K, const float *A,
+                                      const float *B, float *C, const SimtTma &tma, int splits,
+                                      int kchunk, bool spread, cudaStream_t stream)
+{
+    using namespace simt_tma_rect;
+    if (tile.m == 256 && tile.n == 64)
+        return launch_rect<256, 64>(M, N, K, A, B, C, tma, splits, kchunk, spread, stream);
+    if (tile.m == 64 && tile.n == 256)
+        return launch_rect<64, 256>(M, N, K, A, B, C, tma, splits, kchunk, spread, stream);
+    return cudaErrorInvalidValue;
 }
 
 } // namespace rtm
