@@ -92,7 +92,12 @@ typedef enum gemm_status {
  * Any M, N, K >= 0 and any 4-byte-aligned pointers. Each output is a sum of
  * K fp32 products formed with fused multiply-add in an order fixed by the
  * tiling; the error against the exact sum is bounded by a small multiple of
- * K * 2^-24 * sum_k |A[i][k] B[k][j]|. Products with M <= 32 use a kernel
+ * K * 2^-24 * sum_k |A[i][k] B[k][j]|. Where the rows of A and B start on
+ * 16-byte boundaries (K % 4 == 0, N % 4 == 0, A and B 16-byte aligned) the
+ * tensor-memory-access unit stages each K-slice in shared memory (A through
+ * a swizzled staging tile that the threads transpose to k-major order);
+ * otherwise per-thread asynchronous copies do. Each output's sum runs in the
+ * same order either way, so both give the same bits. Products with M <= 32 use a kernel
  * whose threads keep a column strip of C in registers and, where that leaves
  * SMs idle, split K over the CTAs of a cluster, adding the partial sums in a
  * fixed order (results repeat exactly from call to call); no workspace.
