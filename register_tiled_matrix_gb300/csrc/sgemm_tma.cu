@@ -44,6 +44,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "simt_tma_common.cuh"
 
 namespace rtm {
 namespace simt_tma {
@@ -68,32 +69,15 @@ constexpr int SMEM_BYTES = OFF_BAR + 16 + 1024;  // + room to align the base
 constexpr uint32_t kSliceBytes = (BM * BK + BK * BN) * 4;
 constexpr int kSpreadSmem = 120 * 1024;  // more than half of an SM's 228 KB
 
+using simt_tma_common::EncodeTiledFn;
+using simt_tma_common::encode_f32_map;
+using simt_tma_common::lds128;
+using simt_tma_common::sts128;
+
 __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n, int &tile_m,
                                               int &tile_n)
 {
-    const int group_size = kGroupM * tiles_n;
-    const int group = bid / group_size;
-    const int first_m = group * kGroupM;
-    const int rows = min(tiles_m - first_m, kGroupM);
-    const int in_group = bid - group * group_size;
-    tile_m = first_m + in_group % rows;
-    tile_n = in_group / rows;
-}
-
-__device__ __forceinline__ float4 lds128(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, float x, float y, float z, float w)
-{
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y), "f"(z),
-                 "f"(w)
-                 : "memory");
+    simt_tma_common::grouped_tile<kGroupM>(bid, tiles_m, tiles_n, tile_m, tile_n);
 }
 
 // One k-step of the 8 x 8 register tile: acc[i][j] += a[i] * b[j], as 32
@@ -756,25 +740,6 @@ __global__ void __launch_bounds__(kThreads)
             if (gn + j < N)
                 crow[gn + j] = w[j];
     }
-}
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// A rows x cols fp32 matrix (row-major, rows cols * 4 bytes apart) as a 2-D
-// tensor map with box box_cols x box_rows.
-bool encode_f32_map(EncodeTiledFn fn, CUtensorMap *map, const float *base, uint64_t rows,
-                    uint64_t cols, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle)
-{
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 4};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 } // namespace simt_tma

@@ -41,6 +41,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "simt_tma_common.cuh"
 
 namespace rtm {
 namespace simt_tma_rect {
@@ -73,32 +74,15 @@ struct Shape {
     static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
+using simt_tma_common::EncodeTiledFn;
+using simt_tma_common::encode_f32_map;
+using simt_tma_common::lds128;
+using simt_tma_common::sts128;
+
 __device__ __forceinline__ void tile_of_block(int bid, int tiles_m, int tiles_n, int &tile_m,
                                               int &tile_n)
 {
-    const int group_size = kGroupM * tiles_n;
-    const int group = bid / group_size;
-    const int first_m = group * kGroupM;
-    const int rows = min(tiles_m - first_m, kGroupM);
-    const int in_group = bid - group * group_size;
-    tile_m = first_m + in_group % rows;
-    tile_n = in_group / rows;
-}
-
-__device__ __forceinline__ float4 lds128(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, float x, float y, float z, float w)
-{
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y), "f"(z),
-                 "f"(w)
-                 : "memory");
+    simt_tma_common::grouped_tile<kGroupM>(bid, tiles_m, tiles_n, tile_m, tile_n);
 }
 
 // One k-step of the TM x TN register tile: acc[i][j] += a[i] * b[j] as
@@ -321,26 +305,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     cluster_sync();
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// rows x cols fp32 matrix, row-major, rows cols * 4 bytes apart; box of
-// box_rows x box_cols; zeros outside the matrix.
-static bool encode_map(EncodeTiledFn fn, CUtensorMap *map, const float *base, uint64_t rows,
-                       uint64_t cols, uint32_t box_cols, uint32_t box_rows,
-                       CUtensorMapSwizzle swizzle)
-{
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 4};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BM, int BN>
 static cudaError_t launch_rect(int M, int N, int K, const float *A, const float *B, float *C,
                                const SimtTma &tma, int splits, int kchunk, bool spread,
@@ -358,8 +322,8 @@ static cudaError_t launch_rect(int M, int N, int K, const float *A, const float 
         return cudaErrorInvalidValue;
     auto fn = reinterpret_cast<EncodeTiledFn>(tma.encode_tiled);
     CUtensorMap ta, tb;
-    if (!encode_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;  // N % 4 == 0 already
     auto kernel = c_vec ? sgemm_tma_rect_kernel<BM, BN, true> : sgemm_tma_rect_kernel<BM, BN, false>;
