@@ -102,9 +102,41 @@ def _check(status: int) -> None:
         raise GemmError(status, status_string(status))
 
 
-def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return int(s.cuda_stream)
+# The current stream's handle without building a torch.cuda.Stream object
+# (about a microsecond per call); the public API where the accessor is absent.
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: Optional[int] = None) -> int:
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if _raw_current_stream is not None:
+        return int(_raw_current_stream(torch.cuda.current_device() if device is None else device))
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
+class _SameDevice:
+    """The device guard of a call whose tensors are on the current device: none."""
+
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
+_SAME_DEVICE = _SameDevice()
+
+
+def _on_device(t: torch.Tensor):
+    """A context that makes t's device current for the call (switching only when
+    it is not current already: the switch and switch back cost microseconds)."""
+    idx = t.get_device()
+    return _SAME_DEVICE if idx == torch.cuda.current_device() else torch.cuda.device(idx)
+
+
+def _library() -> ctypes.CDLL:
+    return _lib if _lib is not None else load_library()
 
 
 def _prepare(A: torch.Tensor, B: torch.Tensor, dtype: torch.dtype,
@@ -136,9 +168,9 @@ def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = Non
     C = _prepare(A, B, torch.float32, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
-        _check(load_library().gemm_f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                       _stream_handle(stream)))
+    with _on_device(A):
+        _check(_library().gemm_f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                       _stream_handle(stream, A.get_device())))
     return C
 
 
@@ -174,15 +206,16 @@ def gemm_f32_ws(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = 
     C = _prepare(A, B, torch.float32, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
+    with _on_device(A):
         if workspace is None:
             need = gemm_f32_workspace_bytes(M, N, K)
             workspace = torch.empty(max(need // 4, 1), dtype=torch.float32, device=A.device)
         if not workspace.is_cuda or workspace.device != A.device or not workspace.is_contiguous():
             raise ValueError("workspace must be a contiguous CUDA tensor on A's device")
         nbytes = workspace.numel() * workspace.element_size()
-        _check(load_library().gemm_f32_ws(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                          workspace.data_ptr(), nbytes, _stream_handle(stream)))
+        _check(_library().gemm_f32_ws(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                      workspace.data_ptr(), nbytes,
+                                      _stream_handle(stream, A.get_device())))
     return C
 
 
@@ -200,9 +233,9 @@ def gemm_f32_ladder(rung: int, A: torch.Tensor, B: torch.Tensor,
     C = _prepare(A, B, torch.float32, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
+    with _on_device(A):
         _check(load_library().gemm_f32_ladder(int(rung), M, N, K, A.data_ptr(), B.data_ptr(),
-                                              C.data_ptr(), _stream_handle(stream)))
+                                              C.data_ptr(), _stream_handle(stream, A.get_device())))
     return C
 
 
@@ -212,9 +245,9 @@ def gemm_bf16f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] =
     C = _prepare(A, B, torch.bfloat16, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
-        _check(load_library().gemm_bf16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                           _stream_handle(stream)))
+    with _on_device(A):
+        _check(_library().gemm_bf16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                           _stream_handle(stream, A.get_device())))
     return C
 
 
@@ -224,9 +257,9 @@ def gemm_f16f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = 
     C = _prepare(A, B, torch.float16, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
-        _check(load_library().gemm_f16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                          _stream_handle(stream)))
+    with _on_device(A):
+        _check(_library().gemm_f16f32(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                          _stream_handle(stream, A.get_device())))
     return C
 
 
@@ -247,7 +280,7 @@ def _gemm_2byte_ws(entry: str, A: torch.Tensor, B: torch.Tensor, dtype: torch.dt
     C = _prepare(A, B, dtype, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
+    with _on_device(A):
         if workspace is None and M > 128 and not (_rows_on_16_bytes(A) and _rows_on_16_bytes(B)):
             workspace = torch.empty(gemm_bf16f32_workspace_bytes(M, N, K), dtype=torch.uint8,
                                     device=A.device)
@@ -257,8 +290,8 @@ def _gemm_2byte_ws(entry: str, A: torch.Tensor, B: torch.Tensor, dtype: torch.dt
                     or not workspace.is_contiguous()):
                 raise ValueError("workspace must be a contiguous CUDA tensor on A's device")
             ptr, nbytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-        _check(getattr(load_library(), entry)(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                              ptr, nbytes, _stream_handle(stream)))
+        _check(getattr(_library(), entry)(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                          ptr, nbytes, _stream_handle(stream, A.get_device())))
     return C
 
 
@@ -285,7 +318,7 @@ def gemm_bf16f32_selftest_timeout(A: torch.Tensor, B: torch.Tensor, out: torch.T
     C = _prepare(A, B, torch.bfloat16, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
+    with _on_device(A):
         _check(load_library().gemm_bf16f32_selftest_timeout(
             M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), int(wait_limit_ns),
             _stream_handle(stream)))
@@ -298,7 +331,7 @@ def gemm_f32_selftest_timeout(A: torch.Tensor, B: torch.Tensor, out: torch.Tenso
     C = _prepare(A, B, torch.float32, out)
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
+    with _on_device(A):
         _check(load_library().gemm_f32_selftest_timeout(
             M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), int(wait_limit_ns),
             _stream_handle(stream)))
