@@ -15,12 +15,13 @@
 // 4 LDS.128 + 4 STS.128 each). In the cp.async kernel every thread issued
 // 34 (tall) or 24 (short) copies per slice for the same data.
 //
-// One k-major A stage (not two): for 256-row tiles two stages would need
-// 114 KB of shared memory and one CTA per SM; with one the CTA needs 81 KB,
-// two CTAs share an SM, and each covers the other's transpose. Per slice:
-// wait for the slice's loads, transpose A, a CTA barrier, thread 0 issues the
-// next slice (its A into the free staging tile, its B into the other B
-// stage), the k loop, a CTA barrier (the A stage is free again).
+// The 256-row tiles have one k-major A stage: two would need 114 KB of
+// shared memory and one CTA per SM; with one the CTA needs 81 KB, two CTAs
+// share an SM, and each covers the other's transpose. Per slice: wait for the
+// slice's loads, transpose A, a CTA barrier, thread 0 issues the next slice
+// (its A into the free staging tile, its B into the other B stage), the k
+// loop, a CTA barrier (the A stage is free again). The 64-row tiles have two
+// A stages (90 KB) and the pipeline of sgemm_tma.cu: one barrier per slice.
 //
 // K is split over the S CTAs of a cluster (grid (tiles, S), cluster (1, S, 1),
 // S in {1, 2, 4, 8}); each parks its partial tile in its shared memory and,
@@ -63,10 +64,14 @@ struct Shape {
     static constexpr int LDA = BM + 4;
     static constexpr int A_STAGE = BK * LDA;          // floats
     static constexpr int B_STAGE = BK * BN;           // floats
+    // Two A stages where two CTAs still fit on an SM (the 64-row tiles): the
+    // transpose of slice s + 1 then overlaps slice s's k loop, one barrier
+    // per slice; the 256-row tiles keep one.
+    static constexpr int A_STAGES = (BM * BK + 2 * BK * BN + 2 * BK * LDA) * 4 + 2048 <= 113 * 1024 ? 2 : 1;
     static constexpr int OFF_ST = 0;
     static constexpr int OFF_B = BM * BK * 4;
     static constexpr int OFF_A = OFF_B + 2 * B_STAGE * 4;
-    static constexpr int OFF_BAR = OFF_A + A_STAGE * 4;
+    static constexpr int OFF_BAR = OFF_A + A_STAGES * A_STAGE * 4;
     static constexpr int SMEM_BYTES = OFF_BAR + 16 + 1024;  // + room to align the base
     static constexpr uint32_t kSliceBytes = (BM * BK + BK * BN) * 4;
     static constexpr int kPartPitch = BN + 4;
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = ((lane >> 3) << 1) | ((lane >> 2) & 1);
     const uint32_t st_base = smem_u32(stA);
     const uint32_t a_dst = smem_u32(sA + (4 * q) * LDA + 4 * r4);
-    auto transpose = [&](int s) {
+    auto transpose = [&](int s, int stage) {
         if (mbar_wait_bounded(&full[s & 1], (uint32_t)((s >> 1) & 1), wait_limit_ns, &abort_flag)) {
             if (tid == 0 && confirmed == s)
                 confirmed = s + 1;
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int row = 128 * b + 4 * r4 + i;
                 v[i] = lds128(st_base + (uint32_t)(row * (BK * 4) + ((q ^ (row & 7)) * 16)));
             }
-            const uint32_t d = a_dst + (uint32_t)(128 * b * 4);
+            const uint32_t d = a_dst + (uint32_t)((stage * Sh::A_STAGE + 128 * b) * 4);
             sts128(d + 0 * LDA * 4, v[0].x, v[1].x, v[2].x, v[3].x);
             sts128(d + 1 * LDA * 4, v[0].y, v[1].y, v[2].y, v[3].y);
             sts128(d + 2 * LDA * 4, v[0].z, v[1].z, v[2].z, v[3].z);
@@ -240,37 +245,66 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int j = 0; j < TN; ++j)
             acc[i][j] = 0.0f;
 
-    if (ktiles > 0 && tid == 0)
-        issue(0);
-    for (int kt = 0; kt < ktiles; ++kt) {
-        transpose(kt);
-        __syncthreads();  // the A stage holds slice kt; the staging tile is free
-        if (tid == 0 && kt + 1 < ktiles && !abort_flag)
-            issue(kt + 1);
-        const float *cA = sA + tm * 4;
-        const float *cB = sB + (kt & 1) * Sh::B_STAGE + tn * 4;
+    // One k-step of the register tile from A stage `as` and B stage `kt % 2`.
+    auto k_step = [&](const float *cA, const float *cB, int k) {
+        float a[TM], b[TN];
 #pragma unroll
-        for (int k = 0; k < BK; ++k) {
-            float a[TM], b[TN];
-#pragma unroll
-            for (int h = 0; h < TM / 4; ++h) {
-                const float4 v = *reinterpret_cast<const float4 *>(cA + k * LDA + h * 64);
-                a[h * 4 + 0] = v.x;
-                a[h * 4 + 1] = v.y;
-                a[h * 4 + 2] = v.z;
-                a[h * 4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int h = 0; h < TN / 4; ++h) {
-                const float4 v = *reinterpret_cast<const float4 *>(cB + k * BN + h * 64);
-                b[h * 4 + 0] = v.x;
-                b[h * 4 + 1] = v.y;
-                b[h * 4 + 2] = v.z;
-                b[h * 4 + 3] = v.w;
-            }
-            outer_product_step<TM, TN>(acc, a, b);
+        for (int h = 0; h < TM / 4; ++h) {
+            const float4 v = *reinterpret_cast<const float4 *>(cA + k * LDA + h * 64);
+            a[h * 4 + 0] = v.x;
+            a[h * 4 + 1] = v.y;
+            a[h * 4 + 2] = v.z;
+            a[h * 4 + 3] = v.w;
         }
-        __syncthreads();  // the A stage and B stage kt % 2 are free
+#pragma unroll
+        for (int h = 0; h < TN / 4; ++h) {
+            const float4 v = *reinterpret_cast<const float4 *>(cB + k * BN + h * 64);
+            b[h * 4 + 0] = v.x;
+            b[h * 4 + 1] = v.y;
+            b[h * 4 + 2] = v.z;
+            b[h * 4 + 3] = v.w;
+        }
+        outer_product_step<TM, TN>(acc, a, b);
+    };
+    if constexpr (Sh::A_STAGES == 1) {
+        if (ktiles > 0 && tid == 0)
+            issue(0);
+        for (int kt = 0; kt < ktiles; ++kt) {
+            transpose(kt, 0);
+            __syncthreads();  // the A stage holds slice kt; the staging tile is free
+            if (tid == 0 && kt + 1 < ktiles && !abort_flag)
+                issue(kt + 1);
+            const float *cA = sA + tm * 4;
+            const float *cB = sB + (kt & 1) * Sh::B_STAGE + tn * 4;
+#pragma unroll
+            for (int k = 0; k < BK; ++k)
+                k_step(cA, cB, k);
+            __syncthreads();  // the A stage and B stage kt % 2 are free
+        }
+    } else {
+        // As in sgemm_tma.cu: slice s + 1 is loaded while slice s is multiplied
+        // and transposed into the other A stage once slice s's k loop is done.
+        if (ktiles > 0) {
+            if (tid == 0)
+                issue(0);
+            transpose(0, 0);
+            __syncthreads();
+            if (tid == 0 && ktiles > 1 && !abort_flag)
+                issue(1);
+        }
+        for (int kt = 0; kt < ktiles; ++kt) {
+            const float *cA = sA + (kt & 1) * Sh::A_STAGE + tm * 4;
+            const float *cB = sB + (kt & 1) * Sh::B_STAGE + tn * 4;
+            const bool next = kt + 1 < ktiles;
+#pragma unroll
+            for (int k = 0; k < BK; ++k)
+                k_step(cA, cB, k);
+            if (next)
+                transpose(kt + 1, (kt + 1) & 1);
+            __syncthreads();  // stage kt % 2 and the staging tile are free
+            if (tid == 0 && kt + 2 < ktiles && !abort_flag)
+                issue(kt + 2);
+        }
     }
     if (tid == 0 && confirmed < issued) {
         int never = 0;
