@@ -353,15 +353,18 @@ GEMM_API int gemm_bf16f32_selftest_timeout(int64_t M, int64_t N, int64_t K,
 
 /*
  * gemm_f32_selftest_timeout — failure-detection check for the bounded waits
- * of gemm_f32's TMA-fed kernel. Launches it on the given buffers with its
- * loads muted (each K-slice's bytes are announced on its barrier but never
- * loaded) and every wait limited to `wait_limit_ns`: each CTA's first wait
- * gives up, records GEMM_ERR_TIMEOUT in the device error word and raises the
- * CTA's abort flag; every thread still reaches every barrier and the kernel
- * returns, leaving the GPU context usable. C is left unspecified. Same
- * argument rules as gemm_f32; the shape must take the TMA-fed kernel (K > 0,
- * K % 4 == 0, N % 4 == 0, A and B 16-byte aligned) else GEMM_ERR_INVALID_ARG;
- * wait_limit_ns must be in [1e6, 1e10].
+ * of gemm_f32's TMA-fed kernels. Runs gemm_f32's schedule for the shape (128
+ * x 128 tiles plain, with K split over a cluster or with a split last wave;
+ * 256 x 64 or 64 x 256 tiles) on the given buffers with every TMA load muted
+ * (each K-slice's bytes are announced on its barrier but never loaded) and
+ * every wait limited to `wait_limit_ns`: each CTA's first wait gives up,
+ * records GEMM_ERR_TIMEOUT in the device error word and raises the CTA's
+ * abort flag; every thread still reaches every barrier (the cluster barriers
+ * too) and the kernel returns, leaving the GPU context usable. C is left
+ * unspecified. Same argument rules as gemm_f32; the shape must run on those
+ * kernels (K > 0, M > 32, K % 4 == 0, N % 4 == 0, A and B 16-byte aligned,
+ * not 64-row or 64 x 64 tiles) else GEMM_ERR_INVALID_ARG; wait_limit_ns must
+ * be in [1e6, 1e10].
  */
 GEMM_API int gemm_f32_selftest_timeout(int64_t M, int64_t N, int64_t K,
                                        const float *A, const float *B, float *C,

@@ -588,20 +588,32 @@ int gemm_f32_selftest_timeout(int64_t M, int64_t N, int64_t K, const float *A, c
     int st = rtm::check_f32_args(M, N, K, A, B, C, &nothing);
     if (st != GEMM_OK)
         return st;
-    if (nothing || K == 0 || !rtm::sgemm_tma_eligible((int)M, (int)N, (int)K, A, B))
-        return GEMM_ERR_INVALID_ARG;  // the self-test runs the TMA-fed kernel
+    if (nothing || K == 0 || M <= rtm::kShortMaxM ||
+        !rtm::sgemm_tma_eligible((int)M, (int)N, (int)K, A, B))
+        return GEMM_ERR_INVALID_ARG;  // the self-test runs TMA-fed kernels only
     DeviceInfo d;
     st = current_device(&d);
     if (st != GEMM_OK)
         return st;
+    // gemm_f32's own schedule for the shape, every TMA-fed launch muted; shapes
+    // it runs on tiles that have no TMA-fed kernel (64-row or 64 x 64 tiles)
+    // are refused.
+    const rtm::SplitK plan = rtm::sgemm_cluster_schedule((int)M, (int)N, (int)K, d.sms);
+    const rtm::SimtTile t = rtm::simt_resolve_tile(plan.tile, (int)M, (int)N);
+    const bool tma_tile = (t.m == rtm::simt_tiles::kTileM && t.n == rtm::simt_tiles::kTileN) ||
+                          (t.m == rtm::simt_tiles::kTallTileM && t.n == rtm::simt_tiles::kNarrowN) ||
+                          (t.m == rtm::simt_tiles::kShortTileM && t.n == rtm::simt_tiles::kWideTileN);
+    if (!tma_tile)
+        return GEMM_ERR_INVALID_ARG;
     rtm::SimtTma tma;
     tma.encode_tiled = encode_tiled_fn();
     tma.err = d.err;
     tma.wait_limit_ns = (uint64_t)wait_limit_ns;
+    tma.mute = true;
     if (!tma.encode_tiled)
         return GEMM_ERR_LAUNCH;
-    return finish(rtm::launch_sgemm_f32_tma((int)M, (int)N, (int)K, A, B, C, tma, -1,
-                                            static_cast<cudaStream_t>(stream), true));
+    return finish(rtm::launch_sgemm_f32_tiles((int)M, (int)N, (int)K, A, B, C, plan, d.sms,
+                                              static_cast<cudaStream_t>(stream), &tma));
 }
 
 int gemm_get_device_error(void *stream)

@@ -110,6 +110,7 @@ struct SimtTma {
     void *encode_tiled = nullptr;
     int *err = nullptr;
     uint64_t wait_limit_ns = 0;
+    bool mute = false;  // failure-detection self-test: announce the slices, load nothing
 };
 // The plain 128 x 128 product with its K slices loaded by TMA (sgemm_tma.cu):
 // tiles 0 .. tile_count - 1 of the grouped raster (tile_count < 0: all).

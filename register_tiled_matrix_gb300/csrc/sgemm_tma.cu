@@ -321,8 +321,10 @@ __device__ __forceinline__ void cluster_add_parts(const float *part, int M, int 
     }
 }
 
-template <bool C_VEC>
-__global__ void __launch_bounds__(kThreads, 2)
+// MUTE (the self-test): as in sgemm_tma_kernel; one CTA per SM is enough
+// there, and the register budget that gives keeps the variant free of spills.
+template <bool C_VEC, bool MUTE = false>
+__global__ void __launch_bounds__(kThreads, MUTE ? 1 : 2)
     sgemm_tma_cluster_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
                              int kchunk, int tile_first, float *__restrict__ C, int *err,
@@ -363,8 +365,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto issue = [&](int s) {
         uint64_t *bar = &full[s & 1];
         mbar_arrive_expect_tx(bar, kSliceBytes);
-        tma_load_2d(smem_u32(stA), &tmA, bar, (ks_begin + s) * BK, m0);
-        tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, n0, (ks_begin + s) * BK);
+        if constexpr (!MUTE) {
+            tma_load_2d(smem_u32(stA), &tmA, bar, (ks_begin + s) * BK, m0);
+            tma_load_2d(smem_u32(sB + (s & 1) * B_STAGE), &tmB, bar, n0, (ks_begin + s) * BK);
+        }
         ++issued;
     };
     const int r4 = warp * 4 + (lane & 3);
@@ -770,12 +774,12 @@ cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const floa
         !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;  // N % 4 == 0 already
-    auto kernel = mute    ? sgemm_tma_kernel<true, true>
-                  : c_vec ? sgemm_tma_kernel<true>
-                          : sgemm_tma_kernel<false>;
-    static std::atomic<uint64_t> done_vec{0}, done_any{0}, done_mute{0};
-    const cudaError_t e =
-        set_smem_limit_once(kernel, SMEM_BYTES, mute ? done_mute : c_vec ? done_vec : done_any);
+    // Muted (the self-test) or not, the epilogue stores whatever C's alignment allows.
+    const bool m = mute || tma.mute;
+    auto kernel = m ? (c_vec ? sgemm_tma_kernel<true, true> : sgemm_tma_kernel<false, true>)
+                    : (c_vec ? sgemm_tma_kernel<true> : sgemm_tma_kernel<false>);
+    static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
+    const cudaError_t e = set_smem_limit_once(kernel, SMEM_BYTES, done[(m ? 2 : 0) + (c_vec ? 0 : 1)]);
     if (e != cudaSuccess)
         return e;
     kernel<<<(unsigned)tiles, kThreads, SMEM_BYTES, stream>>>(ta, tb, M, N, K, C, tma.err,
@@ -807,9 +811,12 @@ cudaError_t launch_sgemm_f32_tma_cluster(int M, int N, int K, const float *A, co
         !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
-    auto kernel = c_vec ? sgemm_tma_cluster_kernel<true> : sgemm_tma_cluster_kernel<false>;
-    static std::atomic<uint64_t> done_vec{0}, done_any{0};
-    const cudaError_t e = set_smem_limit_once(kernel, kSpreadSmem, c_vec ? done_vec : done_any);
+    auto kernel = tma.mute ? (c_vec ? sgemm_tma_cluster_kernel<true, true>
+                                    : sgemm_tma_cluster_kernel<false, true>)
+                           : (c_vec ? sgemm_tma_cluster_kernel<true> : sgemm_tma_cluster_kernel<false>);
+    static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
+    const cudaError_t e =
+        set_smem_limit_once(kernel, kSpreadSmem, done[(tma.mute ? 2 : 0) + (c_vec ? 0 : 1)]);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

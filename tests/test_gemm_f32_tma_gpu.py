@@ -102,11 +102,23 @@ def test_tma_kernel_repeats_bit_for_bit():
         assert torch.equal(rtm.gemm_f32(Ad, Bd), first)
 
 
-@pytest.mark.parametrize("M,N,K", [(2000, 2004, 100), (256, 256, 4096)])
-def test_tma_kernel_bounded_wait_gives_up_and_context_survives(M, N, K):
+# Every schedule gemm_f32 runs on TMA-fed kernels: 128 x 128 tiles plain, split
+# over a cluster, or with a split last wave; 256 x 64 and 64 x 256 tiles.
+SELFTEST_SHAPES = [(2000, 2004, 100, ("tiles", "tiles+tail-cluster-split")),
+                   (1024, 1024, 1024, ("tiles+cluster-split",)),
+                   (2048, 2048, 1024, ("tiles+tail-cluster-split",)),
+                   (8192, 64, 4096, ("tall-tiles+cluster-split",)),
+                   (64, 8192, 4096, ("wide-tiles+cluster-split",)),
+                   (32768, 64, 512, ("tall-tiles",))]
+
+
+@pytest.mark.parametrize("M,N,K,kinds", SELFTEST_SHAPES)
+def test_tma_kernel_bounded_wait_gives_up_and_context_survives(M, N, K, kinds):
     """With the loads muted, every CTA's first wait runs out after 50 ms; the
     kernel records a timeout and returns (every thread still reaches every
-    barrier), and the next product on the same context is correct."""
+    barrier, the cluster barriers too), and the next product on the same
+    context is correct."""
+    assert rtm.gemm_f32_schedule(M, N, K)[0] in kinds
     A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=31)
     Ad, Bd = A.to(DEV), B.to(DEV)
     C = torch.empty(M, N, device=DEV)
@@ -114,11 +126,30 @@ def test_tma_kernel_bounded_wait_gives_up_and_context_survives(M, N, K):
     rtm.gemm_f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
     assert rtm.get_device_error() == -4
     assert rtm.get_device_error() == 0, "reading the error word clears it"
+    assert_close_to_oracle(rtm.gemm_f32(Ad, Bd), A, B, "f32", full=M * N * K <= (1 << 31), seed=M)
+
+
+def test_tma_selftest_with_c_off_16_byte_boundaries():
+    # C 4 bytes past a 16-byte boundary: the muted kernels store C with 4-byte
+    # stores as the product kernels do; the guard band stays untouched.
+    M, N, K = 1024, 1024, 1024
+    A, B = workloads.make_inputs(M, N, K, "uniform", "f32", seed=32)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf = torch.full((M * N + 4,), float("nan"), device=DEV)
+    C = buf[1:1 + M * N].view(M, N)
+    rtm.gemm_f32_selftest_timeout(Ad, Bd, C, wait_limit_ns=50_000_000)
+    assert rtm.get_device_error() == -4
+    assert torch.isnan(buf[0]) and torch.isnan(buf[1 + M * N:]).all()
     assert_close_to_oracle(rtm.gemm_f32(Ad, Bd), A, B, "f32")
 
 
-def test_tma_selftest_rejects_shapes_off_the_tma_path():
-    A = torch.zeros(64, 99, device=DEV)  # K % 4 != 0
-    B = torch.zeros(99, 64, device=DEV)
+@pytest.mark.parametrize("M,N,K", [(64, 64, 99), (16, 4096, 4096), (256, 256, 256)],
+                         ids=["rows_off_16_bytes", "column_strips", "small_tiles"])
+def test_tma_selftest_rejects_shapes_off_the_tma_path(M, N, K):
+    # K % 4 != 0 (cp.async kernel), M <= 32 (column strips), 64 x 64 tiles
+    if M > 32 and K % 4 == 0:
+        assert rtm.gemm_f32_schedule(M, N, K)[0] in ("tiles+cluster-split", "tiles")
+    A = torch.zeros(M, K, device=DEV)
+    B = torch.zeros(K, N, device=DEV)
     with pytest.raises(rtm.GemmError):
-        rtm.gemm_f32_selftest_timeout(A, B, torch.empty(64, 64, device=DEV), 50_000_000)
+        rtm.gemm_f32_selftest_timeout(A, B, torch.empty(M, N, device=DEV), 50_000_000)
