@@ -280,20 +280,27 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
         }
         return finish(rtm::launch_gemm_tc_any_pair(L, s));
     }
-    if (!tma_ok)
-        return finish(rtm::launch_gemm_tc_any(L, s));
     // Long K with at most one 128-column tile per SM: the product streams B
     // and is bound by how much of it is in flight, so compute C^T = B^T.A^T
     // (B fills the MMA's 128-row side) and split K over up to 8 CTAs of a
     // cluster while that keeps at most one CTA per SM and >= 1024 of K per
     // CTA (1..128 x 8192 x 8192: 41-56 us before, 27-33 us; 64 x 1024 x 8192:
-    // 39.7 -> 14.5 us).
+    // 39.7 -> 14.5 us). That kernel stores C one float at a time, so C rows
+    // need no 16-byte alignment there.
     const int64_t t_tiles = (N + 127) / 128;
-    if (K >= 2048 && t_tiles <= d.sms) {
-        int splits = 1;
-        while (splits < 8 && t_tiles * splits * 2 <= d.sms && K / (splits * 2) >= 1024)
-            splits *= 2;
+    const bool long_k = K >= 2048 && t_tiles <= d.sms;
+    int splits = 1;
+    while (long_k && splits < 8 && t_tiles * splits * 2 <= d.sms && K / (splits * 2) >= 1024)
+        splits *= 2;
+    if (long_k && a_rows16 && b_rows16)
         return finish(rtm::launch_gemm_tc_t(L, splits, true, s));
+    // A or B rows off 16-byte boundaries: the transposed kernel with producer
+    // warps in place of TMA (the same K-splits), while the column tiles fit
+    // on the SMs at once; wider products take the persistent 128 x 256 tiles.
+    if (!tma_ok) {
+        if (t_tiles <= d.sms)
+            return finish(rtm::launch_gemm_tc_any_t(L, splits, s));
+        return finish(rtm::launch_gemm_tc_any(L, s));
     }
     // One CTA per 128 x BN tile. With M <= 128 there is one row of tiles, so
     // the widest BN that still gives 60 % of the SMs a tile is used (a sweep

@@ -30,15 +30,14 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tc_any_common.cuh"
 
 namespace rtm {
 namespace tcany {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;
 constexpr int STAGES = 4;
-constexpr int UMMA_K = 16;
 constexpr int kProducerWarps = 8;
 constexpr int kProducerThreads = kProducerWarps * 32;
 constexpr int kMmaWarp = kProducerWarps;               // warp 8
@@ -46,7 +45,6 @@ constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
 constexpr int kGroupM = 16;
 constexpr int kAsyncDepth = 3;  // K-slices in flight per producer thread (cp.async path)
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;
-constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;
 constexpr uint32_t B_STAGE_BYTES = BK * BN * 2;
 constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -57,12 +55,6 @@ __host__ __device__ constexpr uint32_t idesc()
 {
     return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) | (0u << 15) |
            (1u << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-}
-
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
-{
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 struct Params {
@@ -84,45 +76,6 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     const int in_group = t - group * group_size;
     m0 = (first_m + in_group % rows) * BM;
     n0 = (in_group / rows) * BN;
-}
-
-__device__ __forceinline__ void give_up(int *err, volatile int *abort)
-{
-    atomicCAS(err, 0, kDevErrTimeout);
-    *abort = 1;
-}
-
-// Byte offset of element (row, col) in a 128-byte-swizzled tile of 64-element
-// rows (one row = 128 bytes; the tile base is 1024-byte aligned).
-__device__ __forceinline__ uint32_t swz(int row, int col)
-{
-    return (uint32_t)row * 128u + ((((uint32_t)col >> 3) ^ ((uint32_t)row & 7u)) << 4) +
-           ((uint32_t)col & 7u) * 2u;
-}
-
-// V consecutive 16-bit values (V = 1, 2 or 4) as one register-sized word.
-template <int V>
-struct Vec;
-template <>
-struct Vec<1> {
-    using T = uint16_t;
-};
-template <>
-struct Vec<2> {
-    using T = uint32_t;
-};
-template <>
-struct Vec<4> {
-    using T = uint2;
-};
-
-template <int V>
-__device__ __forceinline__ typename Vec<V>::T vzero()
-{
-    if constexpr (V == 4)
-        return make_uint2(0u, 0u);
-    else
-        return typename Vec<V>::T(0);
 }
 
 template <bool F16, bool C_VEC, int V, bool ASYNC>
@@ -538,17 +491,6 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
     const int in_group = t - group * group_size;
     m0 = (first_m + in_group % rows) * PM;
     n0 = (in_group / rows) * PN;
-}
-
-// A bounded wait whose outcome every lane of the warp shares: true only when
-// the phase completed for all lanes and no warp has given up. Producer and
-// epilogue warps synchronise inside their loops, so no lane may leave a loop
-// that the others stay in.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit,
-                                          volatile int *abort)
-{
-    const bool got = mbar_wait_bounded(bar, parity, limit, abort);
-    return __all_sync(0xffffffffu, got && !*abort);
 }
 
 // One K-slice of this CTA's operands held in registers by a producer thread:
@@ -1088,16 +1030,6 @@ static cudaError_t launch_v(const TcLaunch &L, int v, cudaStream_t stream)
 }
 
 } // namespace tcany
-
-// Widest access (values) that keeps every row of A and B aligned to it.
-static int access_width(const TcLaunch &L)
-{
-    const uintptr_t a = reinterpret_cast<uintptr_t>(L.A), b = reinterpret_cast<uintptr_t>(L.B);
-    int v = 4;
-    while (v > 1 && (L.K % v != 0 || L.N % v != 0 || (a % (2 * v)) != 0 || (b % (2 * v)) != 0))
-        v /= 2;
-    return v;
-}
 
 cudaError_t launch_gemm_tc_any_pair(const TcLaunch &L, cudaStream_t stream)
 {

@@ -291,6 +291,11 @@ cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);
 // The same on CTA pairs (256 x 256 tiles, each CTA staging half of the
 // operands), for M > 128. Same operand rules; any 4-byte-aligned C.
 cudaError_t launch_gemm_tc_any_pair(const TcLaunch &p, cudaStream_t stream);
+// Short products (M <= 128) on the same producers, computed as the transpose
+// like launch_gemm_tc_t with swap (gemm_tc_any_t.cu): CTAs own 128 columns and
+// tct_rows(M) rows, `splits` (1, 2, 4 or 8) CTAs of a cluster split K. Same
+// operand rules as launch_gemm_tc_any; any 4-byte-aligned C.
+cudaError_t launch_gemm_tc_any_t(const TcLaunch &p, int splits, cudaStream_t stream);
 
 // The host-side argument checks of the fp32 entry points (api.cu), made
 // before any CUDA call: GEMM_OK with *nothing_to_do set when M or N is zero,

@@ -26,7 +26,7 @@ PTXAS_LOG = os.path.join(BUILD, "ptxas.log")
 SOURCES = ["api.cu", "sgemm_simt.cu", "sgemm_ladder.cu", "gemm_tc.cu", "gemm_tc2.cu",
            "gemm_tc_any.cu", "noalloc.cu", "pack.cu", "sgemm_plan.cu", "tc_plan.cu",
            "gemm_tc_t.cu", "sgemm_short.cu", "fp32_peak.cu", "sgemm_tma.cu",
-           "sgemm_tma_rect.cu"]
+           "sgemm_tma_rect.cu", "gemm_tc_any_t.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v",
