@@ -256,7 +256,8 @@ GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * register tile; "寄存器Tiling跨架构解析", sections 2.1 and 6). For M > 128 a
  * cluster of two CTAs computes each 256 x 256 tile with the two-SM MMA
  * (each SM stages half of A and half of B); for M <= 128 one CTA per
- * 128 x 256, 128 x 128 or 128 x 64 tile, or, when K >= 2048, the transposed
+ * 128 x 256, 128 x 128 or 128 x 64 tile, or, when K has at least 32 64-deep
+ * blocks and the 128-column tiles of C fit on the SMs, the transposed
  * product C^T = B^T.A^T with K split over the CTAs of a cluster (the long
  * operand B on the MMA's 128-row side; the partial sums are added in a fixed
  * order, so results repeat exactly from call to call).
@@ -264,15 +265,19 @@ GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * A and B hold raw bfloat16 bit patterns (uint16_t), 2-byte aligned; C is
  * 4-byte aligned (else GEMM_ERR_ALIGNMENT). Any M, N, K. When the rows of A
  * and B start on 16-byte boundaries (K % 8 == 0, N % 8 == 0, A and B 16-byte
- * aligned) the operands are staged by the tensor-memory-access unit (for
- * M <= 128 C must be 16-byte aligned with N % 8 == 0 as well; for M > 128 C
- * rows may start anywhere 4-byte aligned); otherwise by producer warps that
- * load them 2, 4 or 8 bytes at a time into the same swizzled layout (for
- * M > 128 on CTA pairs as well; slower than the TMA staging, same
- * arithmetic: for M > 128 the results equal gemm_bf16f32_ws's bit for bit
- * unless that call adds two K halves of a tile, which it may do only when C
- * rows are 16-byte aligned and K >= 4096). Ragged M, N and K tiles are
- * handled by zero-filled loads and masked stores.
+ * aligned) the operands are staged by the tensor-memory-access unit (C rows
+ * may start anywhere 4-byte aligned, except for M <= 128 with fewer than 32
+ * K-blocks or more column tiles than SMs, where C must be 16-byte aligned
+ * with N % 8 == 0 as well); otherwise by producer warps that copy them 2, 4
+ * or 8 bytes at a time into the same swizzled layout (for M > 128 on CTA
+ * pairs; for M <= 128 on the transposed product while its 128-column tiles
+ * fit on the SMs, with the same K-split). This is slower than the TMA
+ * staging, with the same arithmetic: for M > 128 the results equal
+ * gemm_bf16f32_ws's bit for bit unless that call adds two K halves of a
+ * tile, which it may do only when C rows are 16-byte aligned and K >= 4096;
+ * for M <= 128 with at least 32 K-blocks they equal, bit for bit, those of
+ * the same values zero-padded to rows of a multiple of 8 values. Ragged M, N
+ * and K tiles are handled by zero-filled loads and masked stores.
  *
  * Every wait inside the kernel is bounded (a few seconds); if one gives up
  * the kernel records GEMM_ERR_TIMEOUT in the device error word and returns

@@ -13,15 +13,19 @@
 // Nearly every staged byte is B, and B is read once, so the product is bound
 // by how fast B reaches shared memory.
 //
-// The TMA producer thread is replaced by PW producer warps that load the
-// slice with 2-, 4- or 8-byte accesses (the widest V for which every row of
-// A and B starts on a 2V-byte boundary) into registers, then store it into
-// the swizzled layouts above (16-byte chunk c of a 128-byte row r at chunk
-// c ^ (r mod 8)), zeros outside M, N, K. A producer thread keeps up to three
-// slices in registers (the loads of the slice two ahead are issued before it
-// stores the oldest), so each SM has several slices of B in flight; the
-// shared-memory ring is only four stages deep, because the loads in flight
-// are staged in L1, which gets what the shared-memory carve-out leaves.
+// The TMA producer thread is replaced by producer warps that copy the slice
+// with 2-, 4- or 8-byte accesses (the widest V for which every row of A and B
+// starts on a 2V-byte boundary) into the swizzled layouts above (16-byte
+// chunk c of a 128-byte row r at chunk c ^ (r mod 8)), zeros outside M, N, K.
+// With 4- and 8-byte accesses eight warps issue cp.async copies straight into
+// a 4-stage ring and keep three slices in flight per thread; 2-byte values
+// (which cp.async cannot copy) are loaded into registers by sixteen warps
+// and stored after they arrive. On GB300 the copies measured faster than
+// register staging with three slices per thread (16 x 8190 x 8190: 48.2 ->
+// 41.6 us; 16 x 8188 x 8188: 55.0 -> 34.8 us); a deeper ring (6 stages), 16
+// copying warps or two CTAs per SM gained nothing. The ring stays small
+// because the copies in flight pass through L1, which gets what the
+// shared-memory carve-out leaves.
 //
 // Columns of C are TMEM lanes, rows of C TMEM columns: with S = 1 four
 // epilogue warps store the accumulator directly (for each row of C the 32
@@ -37,7 +41,6 @@
 // GEMM_ERR_TIMEOUT in the device error word and every thread still reaches
 // the cluster barriers.
 #include <cstdint>
-#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -49,13 +52,13 @@ namespace tcany {
 namespace tshort {
 
 constexpr int BNT = 128;  // columns of C per CTA: the MMA's M
-constexpr int STAGES = 4;
 constexpr uint32_t BT_BYTES = BK * BNT * 2;  // 16 KB: 64 k-rows x 128 columns of B
 constexpr int kEpilogueWarps = 4;
 constexpr int threads_of(int pw) { return (pw + 1 + kEpilogueWarps) * 32; }
 
-template <int MN>
+template <int MN, int STG>
 struct Cfg {
+    static constexpr int STAGES = STG;
     static constexpr uint32_t AT_BYTES = MN * BK * 2;  // 4, 8 or 16 KB of A per stage
     static constexpr uint32_t STAGE_BYTES = BT_BYTES + AT_BYTES;
     static constexpr uint32_t RING_BYTES = STAGES * STAGE_BYTES;
@@ -85,77 +88,12 @@ struct Params {
     int mute_producer;  // failure-detection self-test: the producer warps load nothing
 };
 
-// One K-slice in a producer thread's registers, V = 2 or 4 values per access:
-// consecutive threads take consecutive vectors along a row, and a thread's
-// vectors share one column and step A_STEP (B_STEP) rows down. Both steps are
-// multiples of 8, so every vector of a thread has the same swizzle phase and
-// one base offset serves all its stores. A and B check their bounds apart:
-// B's columns are interior for all but the last column tile whatever M is.
-template <int V, int PT, int MN>
-struct SliceV {
-    using W = typename Vec<V>::T;
-    static constexpr int A_ROW = BK / V, A_PER = MN * A_ROW / PT, A_STEP = PT / A_ROW;
-    static constexpr int B_ROW = BNT / V, B_PER = BK * B_ROW / PT, B_STEP = PT / B_ROW;
-    static_assert(A_PER >= 1 && A_PER * PT == MN * A_ROW && B_PER * PT == BK * B_ROW,
-                  "every producer thread holds whole vectors of both operands");
-    static_assert(A_STEP % 8 == 0 && B_STEP % 8 == 0, "swizzle phase fixed per vector");
-    W a[A_PER], b[B_PER];
-
-    // A rows m0 .., columns k0 .. k0+63; B rows k0 .. k0+63, columns n0 ..
-    // n0+127; zeros outside M, N, K (K % V == 0 and N % V == 0: a vector is
-    // all in or all out).
-    __device__ __forceinline__ void load(const Params &p, int tid, int m0, int n0, int k0)
-    {
-        const int ar = tid / A_ROW, ac = (tid % A_ROW) * V;
-        const int br = tid / B_ROW, bc = (tid % B_ROW) * V;
-        const uint16_t *pa = p.A + (size_t)(m0 + ar) * p.K + (k0 + ac);
-        const uint16_t *pb = p.B + (size_t)(k0 + br) * p.N + (n0 + bc);
-        const size_t sa = (size_t)A_STEP * p.K, sb = (size_t)B_STEP * p.N;
-        const bool k_in = k0 + BK <= p.K;
-        if (k_in && n0 + BNT <= p.N) {
-#pragma unroll
-            for (int j = 0; j < B_PER; ++j)
-                b[j] = __ldg(reinterpret_cast<const W *>(pb + j * sb));
-        } else {
-            const bool nb = n0 + bc < p.N;
-#pragma unroll
-            for (int j = 0; j < B_PER; ++j)
-                b[j] = (nb && k0 + br + j * B_STEP < p.K)
-                           ? __ldg(reinterpret_cast<const W *>(pb + j * sb))
-                           : vzero<V>();
-        }
-        if (k_in && m0 + MN <= p.M) {
-#pragma unroll
-            for (int j = 0; j < A_PER; ++j)
-                a[j] = __ldg(reinterpret_cast<const W *>(pa + j * sa));
-        } else {
-            const bool ka = k0 + ac < p.K;
-#pragma unroll
-            for (int j = 0; j < A_PER; ++j)
-                a[j] = (ka && m0 + ar + j * A_STEP < p.M)
-                           ? __ldg(reinterpret_cast<const W *>(pa + j * sa))
-                           : vzero<V>();
-        }
-    }
-
-    __device__ __forceinline__ void store(uint8_t *sA, uint8_t *sB, int tid) const
-    {
-        const int ar = tid / A_ROW, ac = (tid % A_ROW) * V;
-        const int br = tid / B_ROW, bc = (tid % B_ROW) * V;
-        uint8_t *da = sA + swz(ar, ac);
-        uint8_t *db = sB + (bc >> 6) * B_ATOM_BYTES + swz(br, bc & 63);
-#pragma unroll
-        for (int j = 0; j < A_PER; ++j)
-            *reinterpret_cast<W *>(da + j * A_STEP * 128) = a[j];
-#pragma unroll
-        for (int j = 0; j < B_PER; ++j)
-            *reinterpret_cast<W *>(db + j * B_STEP * 128) = b[j];
-    }
-};
-
-// The same with 2-byte accesses (V = 1): a lane per element, coalesced along
-// k for A and along n for B; warp w holds rows AR w .. AR w + AR - 1 of A and
-// k-rows BR w .. BR w + BR - 1 of B.
+// One K-slice of 2-byte values (V = 1) in a producer thread's registers: MN
+// rows of A (k0 .. k0+63) and 64 k-rows of B (columns n0 .. n0+127), a lane
+// per element, coalesced along k for A and along n for B; warp w holds rows
+// AR w .. AR w + AR - 1 of A and k-rows BR w .. BR w + BR - 1 of B. A and B
+// check their bounds apart: B's columns are interior for all but the last
+// column tile whatever M is.
 template <int PT, int MN>
 struct Slice1 {
     static constexpr int PW = PT / 32;
@@ -213,24 +151,60 @@ struct Slice1 {
     }
 };
 
-// Slices a producer thread keeps in registers: three for 4- and 8-byte
-// accesses (at most 16 registers each); a 2-byte slice takes a register per
-// value, so two for MN = 32 (20 values each) and one above, within the 80
-// registers a thread of a 672-thread CTA can have (two of MN = 64 spill).
-template <int V, int MN>
-constexpr int ring_depth()
+// Producer warps: 8 issuing cp.async copies, 16 loading 2-byte values.
+constexpr int producer_warps(int v) { return v == 1 ? 16 : 8; }
+constexpr int kStages = 4;
+
+// 2-byte slices a producer thread keeps in registers (a register per value):
+// two for MN = 32 (20 values each), one above, within the 80 registers a
+// thread of a 672-thread CTA can have (two of MN = 64 spill).
+template <int MN>
+constexpr int ring_depth_2byte()
 {
-    return V > 1 ? 3 : (MN <= 32 ? 2 : 1);
+    return MN <= 32 ? 2 : 1;
 }
 
-template <bool F16, int MN, int V, int PW>
-__global__ void __launch_bounds__(threads_of(PW), 1)
+template <int V>
+__device__ __forceinline__ void cp_async_v(uint32_t dst, const void *src, uint32_t bytes)
+{
+    if constexpr (V == 4)
+        cp_async_8(dst, src, bytes);
+    else
+        cp_async_4(dst, src, bytes);
+}
+
+// The copies of one producer thread for V = 2 or 4 values per copy:
+// consecutive threads take consecutive vectors along a row, and a thread's
+// vectors share one column and step A_STEP (B_STEP) rows down, A_STEP a
+// multiple of 8 and B_STEP of 4, so a vector's swizzled offset is one of two
+// per thread (every other vector of B has the first one's swizzle phase, the
+// others that of row + 4).
+template <int V, int PT, int MN>
+struct AsyncPlan {
+    static constexpr int A_ROW = BK / V, A_PER = MN * A_ROW / PT, A_STEP = PT / A_ROW;
+    static constexpr int B_ROW = BNT / V, B_PER = BK * B_ROW / PT, B_STEP = PT / B_ROW;
+    static_assert(A_PER >= 1 && A_PER * PT == MN * A_ROW && B_PER * PT == BK * B_ROW,
+                  "every producer thread copies whole vectors of both operands");
+    static_assert(A_STEP % 8 == 0 && B_STEP % 4 == 0, "swizzle phase fixed per vector");
+    // Byte offset of B vector j from the offsets of rows br and br + 4.
+    static __device__ __forceinline__ uint32_t b_off(int j, uint32_t db0, uint32_t db1)
+    {
+        if constexpr (B_STEP % 8 == 0)
+            return db0 + (uint32_t)(j * B_STEP * 128);
+        else
+            return ((j & 1) ? db1 : db0) + (uint32_t)((j >> 1) * 8 * 128);
+    }
+};
+
+template <bool F16, int MN, int V>
+__global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
     gemm_tc_any_t_kernel(const Params p)
 {
-    using Cf = Cfg<MN>;
+    using Cf = Cfg<MN, kStages>;
+    constexpr int STAGES = Cf::STAGES;
+    constexpr int PW = producer_warps(V);
     constexpr int PT = PW * 32;
     constexpr int kMmaWarp = PW;
-    using Slice = std::conditional_t<V == 1, Slice1<PT, MN>, SliceV<V, PT, MN>>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -275,8 +249,87 @@ __global__ void __launch_bounds__(threads_of(PW), 1)
 
     if (warp < PW) {
         // ------------------------------------------------ producers
-        if (!p.mute_producer && nslices > 0) {
-            constexpr int R = ring_depth<V, MN>();
+        if (p.mute_producer || nslices == 0) {
+            // nothing to stage (the self-test mutes the loads: every wait gives up)
+        } else if constexpr (V > 1) {
+            // V = 2 or 4: cp.async copies straight into the swizzled layout
+            // (zero-filled outside M, N, K), a thread's copies for a slice one
+            // group; STAGES - 1 slices in flight per thread, each announced on
+            // full[] once the thread's own copies of it have landed and been
+            // fenced for the tensor core. No registers hold operands, so the
+            // ring depth, not the register file, sets the bytes in flight.
+            using SV = AsyncPlan<V, PT, MN>;
+            constexpr int DEPTH = STAGES - 1;
+            constexpr uint32_t VB = 2 * V;
+            const int tid = threadIdx.x;
+            const int ar = tid / SV::A_ROW, ac = (tid % SV::A_ROW) * V;
+            const int br = tid / SV::B_ROW, bc = (tid % SV::B_ROW) * V;
+            const uint32_t da = swz(ar, ac);
+            const uint32_t db0 = (bc >> 6) * B_ATOM_BYTES + swz(br, bc & 63);
+            const uint32_t db1 = (bc >> 6) * B_ATOM_BYTES + swz(br + 4, bc & 63);
+            const size_t sa = (size_t)SV::A_STEP * p.K, sb = (size_t)SV::B_STEP * p.N;
+            uint32_t stage = 0, phase = 0, pending = 0, oldest = 0;
+            for (int s = 0; s < nslices; ++s) {
+                if (!warp_wait(&empty[stage], phase ^ 1, limit, abort)) {
+                    give_up(p.err, abort);
+                    break;
+                }
+                const int k0 = (kb_begin + s) * BK;
+                const uint32_t sB = smem_u32(smem + stage * Cf::STAGE_BYTES);
+                const uint32_t sA = sB + BT_BYTES + da;
+                const uint16_t *pa = p.A + (size_t)(m0 + ar) * p.K + (k0 + ac);
+                const uint16_t *pb = p.B + (size_t)(k0 + br) * p.N + (n0 + bc);
+                const bool k_in = k0 + BK <= p.K;
+                if (k_in && n0 + BNT <= p.N) {
+#pragma unroll
+                    for (int j = 0; j < SV::B_PER; ++j)
+                        cp_async_v<V>(sB + SV::b_off(j, db0, db1), pb + j * sb, VB);
+                } else {
+                    const bool nb = n0 + bc < p.N;
+#pragma unroll
+                    for (int j = 0; j < SV::B_PER; ++j) {
+                        const bool in = nb && k0 + br + j * SV::B_STEP < p.K;
+                        cp_async_v<V>(sB + SV::b_off(j, db0, db1), in ? pb + j * sb : p.B,
+                                      in ? VB : 0u);
+                    }
+                }
+                if (k_in && m0 + MN <= p.M) {
+#pragma unroll
+                    for (int j = 0; j < SV::A_PER; ++j)
+                        cp_async_v<V>(sA + j * SV::A_STEP * 128, pa + j * sa, VB);
+                } else {
+                    const bool ka = k0 + ac < p.K;
+#pragma unroll
+                    for (int j = 0; j < SV::A_PER; ++j) {
+                        const bool in = ka && m0 + ar + j * SV::A_STEP < p.M;
+                        cp_async_v<V>(sA + j * SV::A_STEP * 128, in ? pa + j * sa : p.A,
+                                      in ? VB : 0u);
+                    }
+                }
+                cp_async_commit();
+                if (++pending == DEPTH) {
+                    cp_async_wait<DEPTH - 1>();  // the oldest slice has landed
+                    fence_proxy_async_shared();
+                    mbar_arrive(&full[oldest]);
+                    oldest = oldest + 1 == STAGES ? 0 : oldest + 1;
+                    --pending;
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            // Announce the slices still in flight; on every path (including a
+            // give-up) every copy lands before this thread goes on.
+            cp_async_wait<0>();
+            fence_proxy_async_shared();
+            for (; pending > 0; --pending) {
+                mbar_arrive(&full[oldest]);
+                oldest = oldest + 1 == STAGES ? 0 : oldest + 1;
+            }
+        } else {
+            using Slice = Slice1<PT, MN>;
+            constexpr int R = ring_depth_2byte<MN>();
             const int tid = threadIdx.x;
             uint32_t stage = 0, phase = 0;
             int next = 0, left = nslices;
@@ -312,16 +365,11 @@ __global__ void __launch_bounds__(threads_of(PW), 1)
                 do
                     load_next(s0);
                 while (publish(s0));
-            } else if constexpr (R == 2) {
+            } else {
+                static_assert(R == 2, "one or two slices in registers");
                 Slice s0, s1;
                 load_next(s0);
                 while (step(s0, s1) && step(s1, s0)) {
-                }
-            } else {
-                Slice s0, s1, s2;
-                load_next(s0);
-                load_next(s1);
-                while (step(s0, s2) && step(s1, s0) && step(s2, s1)) {
                 }
             }
         }
@@ -451,15 +499,15 @@ __global__ void __launch_bounds__(threads_of(PW), 1)
     }
 }
 
-template <bool F16, int MN, int V, int PW>
+template <bool F16, int MN, int V>
 static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
 {
-    using Cf = Cfg<MN>;
-    auto kernel = gemm_tc_any_t_kernel<F16, MN, V, PW>;
-    constexpr int kThreadsT = threads_of(PW);
+    using Cf = Cfg<MN, kStages>;
+    auto kernel = gemm_tc_any_t_kernel<F16, MN, V>;
+    constexpr int kThreadsT = threads_of(producer_warps(V));
     static std::atomic<uint64_t> done{0};  // per instantiation
     // The smallest carve-out that holds the ring (of the SM's 228 KB): the
-    // producers' loads in flight are staged in L1, which gets the rest.
+    // producers' copies in flight pass through L1, which gets the rest.
     cudaError_t e = set_smem_limit_once(
         kernel, (int)Cf::SMEM_BYTES, done,
         (int)((Cf::SMEM_BYTES * 100 + 228 * 1024 - 1) / (228 * 1024)));
@@ -493,16 +541,12 @@ static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-// 16 producer warps: with 672 threads a thread has 80 registers, which hold
-// three 4- or 8-byte slices.
-constexpr int kProducerWarpsT = 16;
-
 template <bool F16, int MN>
 static cudaError_t launch_v(const TcLaunch &L, int v, int splits, cudaStream_t stream)
 {
-    return v == 4 ? launch_mn<F16, MN, 4, kProducerWarpsT>(L, splits, stream)
-           : v == 2 ? launch_mn<F16, MN, 2, kProducerWarpsT>(L, splits, stream)
-                    : launch_mn<F16, MN, 1, kProducerWarpsT>(L, splits, stream);
+    return v == 4 ? launch_mn<F16, MN, 4>(L, splits, stream)
+           : v == 2 ? launch_mn<F16, MN, 2>(L, splits, stream)
+                    : launch_mn<F16, MN, 1>(L, splits, stream);
 }
 
 template <bool F16>

@@ -4,8 +4,8 @@ boundaries (tcany::tshort::gemm_tc_any_t_kernel).
 
 The kernel computes C^T = B^T.A^T: a CTA owns 128 columns of C and 32, 64 or
 128 rows, K is split over S CTAs of a cluster (the same S as the TMA-fed
-transposed kernel), and producer warps stage the operands with 2-, 4- or
-8-byte accesses. Checked: the kernel that runs, the oracle (|C - C_oracle| <=
+transposed kernel), and producer warps stage the operands with 4- or 8-byte
+cp.async copies or 2-byte loads through registers. Checked: the kernel that runs, the oracle (|C - C_oracle| <=
 1e-3 * sum_k |A[i][k] B[k][j]|, oracle fed the same 16-bit values), a NaN
 guard band around C, small integers bit for bit, bit equality with the
 TMA-fed transposed kernel on zero-padded copies of the operands (same tiles,
@@ -34,7 +34,8 @@ SHAPES = [(16, 8190, 8190),    # V 2, MN 32, S 2
           (128, 1002, 998),    # V 2, MN 128, S 1 (short K)
           (40, 300, 77),       # V 1, MN 64, S 1
           (16, 10002, 2050),   # V 2, MN 32, S 1 (79 column tiles)
-          (128, 8188, 8188)]   # V 4, MN 128, S 2
+          (128, 8188, 8188),   # V 4, MN 128, S 2
+          (64, 4094, 4094)]    # V 2, MN 64, S 4 (64 K-blocks, like K = 4096)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -87,7 +88,7 @@ def test_transposed_any_small_integers_bit_exact(M, N, K):
 # Long K, and the padded K and N (multiples of 8) give the same column tiles
 # and the same K-split: the aligned copies run the TMA-fed transposed kernel.
 @pytest.mark.parametrize("M,N,K", [(16, 8190, 8190), (100, 4094, 4100), (1, 1001, 3001),
-                                   (33, 600, 16388), (16, 10002, 2050)])
+                                   (33, 600, 16388), (16, 10002, 2050), (64, 4094, 4094)])
 def test_bits_equal_tma_transposed_on_padded_copies(M, N, K):
     A, B = workloads.make_inputs(M, N, K, "uniform", "bf16", seed=3 * M + N + K)
     K8, N8 = (K + 7) // 8 * 8, (N + 7) // 8 * 8

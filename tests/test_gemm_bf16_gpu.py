@@ -202,8 +202,9 @@ def test_short_wide_guard_band(M, N, K):
     assert_close_to_oracle(C, A, B, "bf16", full=M * N * K <= (1 << 31), seed=K)
 
 
-# M <= 128, K >= 2048, at most one 128-column tile per SM: C^T = B^T.A^T on the
-# tensor cores, K split over S CTAs of a cluster (S for a 152-SM GPU noted).
+# M <= 128, K of 32 64-deep blocks or more, at most one 128-column tile per SM:
+# C^T = B^T.A^T on the tensor cores, K split over S CTAs of a cluster (S for a
+# 152-SM GPU noted).
 @pytest.mark.parametrize("M,N,K", [(1, 8192, 4096),      # S = 2
                                    (8, 1024, 8192),      # S = 8
                                    (33, 4096, 2048),     # S = 2
@@ -267,8 +268,9 @@ def test_transposed_bounded_wait_gives_up_and_context_survives():
     assert_close_to_oracle(run(A, B), A, B, "bf16", full=False, seed=52)
 
 
-# M > 128, N <= 128, K >= 2048: A on the MMA's 128-row side, B (64 or 128
-# columns) on its N side, K split over S CTAs of a cluster (S for 152 SMs).
+# M > 128, N <= 128, K of 32 64-deep blocks or more: A on the MMA's 128-row
+# side, B (64 or 128 columns) on its N side, K split over S CTAs of a cluster
+# (S for 152 SMs).
 # 128 < N <= 256 runs on the CTA pairs (K split in two where the tiles leave
 # pairs idle); those shapes stay here as the neighbouring case.
 @pytest.mark.parametrize("M,N,K", [(8192, 64, 4096),    # S = 2
