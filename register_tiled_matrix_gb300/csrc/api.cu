@@ -189,22 +189,6 @@ cudaError_t run_f32_plain(int M, int N, int K, const float *A, const float *B, f
 // Shared by the bf16 and fp16 entry points. `workspace` (may be null) lets the
 // CTA-pair kernel run on re-pitched copies of operands whose rows do not start
 // on 16-byte boundaries.
-// K-split of the kernels that stream one operand through 128-wide tiles with
-// K split over a cluster (gemm_tc_t.cu, gemm_tc_any_t.cu): 0 unless K has at
-// least 32 64-deep blocks and the `tiles` fit on the SMs at once; otherwise
-// the largest S (1, 2, 4 or 8) that keeps at most one CTA per SM and at least
-// 16 blocks per CTA. Whole blocks, so that K = 4094 splits like K = 4096.
-static int long_k_splits(int64_t tiles, int64_t K, int sms)
-{
-    const int64_t kblocks = (K + 63) / 64;
-    if (kblocks < 32 || tiles > sms)
-        return 0;
-    int splits = 1;
-    while (splits < 8 && tiles * splits * 2 <= sms && kblocks / (splits * 2) >= 16)
-        splits *= 2;
-    return splits;
-}
-
 int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, float *C,
              void *stream, uint64_t wait_limit_ns, int mute_producer, int f16 = 0,
              void *workspace = nullptr, int64_t workspace_bytes = 0)
@@ -260,7 +244,7 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
         // two when the tiles leave pairs idle) measured faster on GB300:
         // 8192 x 256 x 8192 43.1 -> 36.4 us, 16384 x 256 x 4096 53.2 -> 34.9 us.
         const int64_t s_tiles = (M + 127) / 128 * ((N + rtm::tcs_cols((int)N) - 1) / rtm::tcs_cols((int)N));
-        const int s_splits = long_k_splits(s_tiles, K, d.sms);
+        const int s_splits = rtm::long_k_splits(s_tiles, K, d.sms);
         if (need == 0 && N <= 128 && s_splits > 0)
             return finish(rtm::launch_gemm_tc_t(L, s_splits, false, s));
         if (need == 0)
@@ -300,7 +284,7 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     // 8192: 39.7 -> 14.5 us). That kernel stores C one float at a time, so C
     // rows need no 16-byte alignment there.
     const int64_t t_tiles = (N + 127) / 128;
-    const int t_splits = long_k_splits(t_tiles, K, d.sms);
+    const int t_splits = rtm::long_k_splits(t_tiles, K, d.sms);
     if (t_splits > 0 && a_rows16 && b_rows16)
         return finish(rtm::launch_gemm_tc_t(L, t_splits, true, s));
     // A or B rows off 16-byte boundaries: the transposed kernel with producer

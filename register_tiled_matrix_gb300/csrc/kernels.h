@@ -284,6 +284,10 @@ cudaError_t launch_pack_rows_2b(const uint16_t *src, int64_t rows, int64_t cols,
 int tct_rows(int M);
 int tcs_cols(int N);
 cudaError_t launch_gemm_tc_t(const TcLaunch &p, int splits, bool swap, cudaStream_t stream);
+// The K-split of those kernels for `tiles` 128-wide tiles (tc_plan.cu): 0 when
+// K has fewer than 32 64-deep blocks or the tiles outnumber the SMs, else the
+// largest S in {1, 2, 4, 8} with tiles * S <= sms and >= 16 blocks per CTA.
+int long_k_splits(long long tiles, long long K, int sms);
 // The same product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu):
 // operands loaded by producer warps instead of TMA (mute_producer: they load
 // nothing, so every wait gives up).

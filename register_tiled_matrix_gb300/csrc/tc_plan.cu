@@ -1,6 +1,8 @@
-// Host-side schedule of the CTA-pair tensor-core kernel (gemm_tc2.cu): which
-// 256 x 256 tiles split K in two. Kept apart from the kernel so the choice can
-// be tested without a GPU.
+// Host-side schedules of the tensor-core kernels, kept apart from the kernels
+// so the choices can be tested without a GPU: which 256 x 256 tiles of the
+// CTA-pair kernel (gemm_tc2.cu) split K in two, and the K-split of the kernels
+// that stream one operand through 128-wide tiles (gemm_tc_t.cu,
+// gemm_tc_any_t.cu).
 #include "kernels.h"
 
 namespace rtm {
@@ -22,6 +24,22 @@ long long pair_split_from(long long ntiles, int pairs, int kblocks, bool c_vec)
     if (ntiles > pairs && tail > 0 && 2 * tail <= pairs)
         return ntiles - tail;
     return ntiles;
+}
+
+// 0 unless K has at least 32 64-deep blocks and the `tiles` fit on the SMs at
+// once; otherwise the largest S (1, 2, 4 or 8) that keeps at most one CTA per
+// SM and at least 16 blocks per CTA. Whole blocks, so that K = 4094 splits
+// like K = 4096 (64 x 4094 x 4094 on the load-and-swizzle kernel: S 2 -> 4,
+// 26.9 -> 17.9 us).
+int long_k_splits(long long tiles, long long K, int sms)
+{
+    const long long kblocks = (K + 63) / 64;
+    if (kblocks < 32 || tiles > sms)
+        return 0;
+    int splits = 1;
+    while (splits < 8 && tiles * splits * 2 <= sms && kblocks / (splits * 2) >= 16)
+        splits *= 2;
+    return splits;
 }
 
 } // namespace rtm

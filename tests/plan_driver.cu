@@ -5,7 +5,8 @@
 // line as M,N,K triples, for a 152-SM GPU whose
 // cluster-split CTAs fit 76 clusters of 2, 36 of 4 and 15 of 8 at one CTA per
 // SM (the occupancy the library queries on GB300); with "pair" first, the
-// CTA-pair kernel's K-split choice instead. Built and run by
+// CTA-pair kernel's K-split choice instead, with "longk" first the K-split of
+// the 128-wide streaming tensor-core kernels. Built and run by
 // tests/test_plan_host.py; no GPU is needed.
 #include <cstdio>
 #include <cstdlib>
@@ -15,6 +16,14 @@
 
 int main(int argc, char **argv)
 {
+    if (argc > 1 && std::string(argv[1]) == "longk") {
+        // longk tiles K sms ...: the K-split of the 128-wide streaming kernels
+        for (int i = 2; i + 2 < argc; i += 3)
+            std::printf("%s %s %s splits %d\n", argv[i], argv[i + 1], argv[i + 2],
+                        rtm::long_k_splits(std::atoll(argv[i]), std::atoll(argv[i + 1]),
+                                           std::atoi(argv[i + 2])));
+        return 0;
+    }
     if (argc > 1 && std::string(argv[1]) == "pair") {
         // pair ntiles pairs kblocks c_vec ...: the CTA-pair kernel's first split tile
         for (int i = 2; i + 3 < argc; i += 4)

@@ -50,8 +50,14 @@ CASES = {
     "gemm_bf16f32_ws re-pitched": ("bf16", 300, 129, 77,
                                    lambda A, B, C, W: rtm.gemm_bf16f32_ws(A, B, out=C,
                                                                           workspace=W)),
-    "gemm_f16f32 load-and-swizzle": ("f16", 100, 130, 90,
-                                     lambda A, B, C, W: rtm.gemm_f16f32(A, B, out=C)),
+    "gemm_bf16f32 transposed, K split": ("bf16", 64, 4096, 4096,
+                                         lambda A, B, C, W: rtm.gemm_bf16f32(A, B, out=C)),
+    "gemm_f16f32 load-and-swizzle, transposed": ("f16", 100, 130, 90,
+                                                 lambda A, B, C, W: rtm.gemm_f16f32(A, B, out=C)),
+    "gemm_bf16f32 load-and-swizzle, transposed, K split": (
+        "bf16", 16, 4094, 4094, lambda A, B, C, W: rtm.gemm_bf16f32(A, B, out=C)),
+    "gemm_bf16f32 load-and-swizzle CTA pairs": ("bf16", 300, 258, 130,
+                                                lambda A, B, C, W: rtm.gemm_bf16f32(A, B, out=C)),
 }
 
 

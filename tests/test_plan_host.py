@@ -217,6 +217,63 @@ def test_pair_split_invariants_over_a_grid(driver):
             assert 2 * t <= p, where                       # every tile, all at once
 
 
+# (tiles, K, SMs): K-split of the 128-wide streaming tensor-core kernels
+# (transposed short products, tall narrow products; TMA-fed or load-and-swizzle).
+LONGK_EXPECT = {
+    (64, 8190, 152): 2,     # 128 x 8190 x 8190: 64 column tiles, S = 4 would need 256 SMs
+    (64, 8192, 152): 2,
+    (32, 4094, 152): 4,     # 64 x 4094 x 4094: 64 K-blocks like K = 4096
+    (32, 4096, 152): 4,
+    (32, 4032, 152): 2,     # 63 K-blocks: 15 per CTA at S = 4
+    (32, 4033, 152): 4,     # 64 K-blocks (the last one ragged)
+    (8, 8192, 152): 8,      # 64 x 1024 x 8192: 16 blocks per CTA at S = 8
+    (8, 16384, 152): 8,     # at most 8 CTAs per cluster
+    (79, 2050, 152): 1,     # 16 x 10002 x 2050: two CTAs per tile would need 158 SMs
+    (152, 8192, 152): 1,    # one tile per SM
+    (153, 8192, 152): 0,    # more tiles than SMs: not this kernel
+    (8, 1984, 152): 0,      # 31 K-blocks: too short
+    (8, 1985, 152): 2,      # 32 K-blocks (the last one ragged): 16 per CTA at S = 2
+    (8, 2048, 152): 2,
+    (1, 3001, 152): 2,      # 47 blocks: 23 per CTA at S = 2, 11 at S = 4
+}
+
+
+def test_long_k_split_choices(driver):
+    args = ["longk"] + [str(x) for key in LONGK_EXPECT for x in key]
+    r = subprocess.run([driver, *args], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    got = {tuple(int(x) for x in l.split()[:3]): int(l.split()[-1]) for l in r.stdout.splitlines()}
+    assert got == LONGK_EXPECT
+
+
+def test_long_k_split_invariants_over_a_grid(driver):
+    """For every (tiles, K) on a grid: no split below 32 K-blocks or with more
+    tiles than SMs; otherwise S is 1, 2, 4 or 8, fits one CTA per SM, leaves
+    every CTA at least 16 K-blocks (when S > 1), and is the largest such; and
+    K values with the same number of 64-deep blocks get the same S."""
+    sms = 152
+    keys = [(t, k, sms) for t in (1, 2, 5, 8, 19, 20, 38, 39, 64, 76, 77, 100, 152, 153)
+            for k in list(range(1900, 2200, 7)) + [4031, 4032, 4033, 4094, 4096, 8190, 8192,
+                                                   16383, 16384, 65536]]
+    args = ["longk"] + [str(x) for key in keys for x in key]
+    r = subprocess.run([driver, *args], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    got = {tuple(int(x) for x in l.split()[:3]): int(l.split()[-1]) for l in r.stdout.splitlines()}
+    assert len(got) == len(keys)
+    by_blocks = {}
+    for (t, k, n), s in got.items():
+        kb = (k + 63) // 64
+        by_blocks.setdefault((t, kb), set()).add(s)
+        if kb < 32 or t > n:
+            assert s == 0, (t, k, s)
+            continue
+        assert s in (1, 2, 4, 8), (t, k, s)
+        assert t * s <= n, (t, k, s)
+        assert s == 1 or kb // s >= 16, (t, k, s)
+        assert s == 8 or t * 2 * s > n or kb // (2 * s) < 16, (t, k, s)  # largest
+    assert all(len(v) == 1 for v in by_blocks.values())
+
+
 def test_schedule_kinds_cover_the_planner_outcomes():
     """Every outcome above has a name in the binding's schedule kinds."""
     assert set(rtm.F32_KINDS.values()) >= {"tiles", "tiles+cluster-split", "tiles+workspace-split",
