@@ -270,14 +270,14 @@ GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * K-blocks or more column tiles than SMs, where C must be 16-byte aligned
  * with N % 8 == 0 as well); otherwise by producer warps that copy them 2, 4
  * or 8 bytes at a time into the same swizzled layout (for M > 128 on CTA
- * pairs; for M <= 128 on the transposed product while its 128-column tiles
- * fit on the SMs, with the same K-split). This is slower than the TMA
- * staging, with the same arithmetic: for M > 128 the results equal
- * gemm_bf16f32_ws's bit for bit unless that call adds two K halves of a
- * tile, which it may do only when C rows are 16-byte aligned and K >= 4096;
- * for M <= 128 with at least 32 K-blocks they equal, bit for bit, those of
- * the same values zero-padded to rows of a multiple of 8 values. Ragged M, N
- * and K tiles are handled by zero-filled loads and masked stores.
+ * pairs; for M <= 128 on the transposed product, with the same K-split where
+ * one applies). This is slower than the TMA staging, with the same
+ * arithmetic: for M > 128 the results equal gemm_bf16f32_ws's bit for bit
+ * unless that call adds two K halves of a tile, which it may do only when C
+ * rows are 16-byte aligned and K >= 4096; for M <= 128 with at least 32
+ * K-blocks and at most one 128-column tile per SM they equal, bit for bit,
+ * those of the same values zero-padded to rows of a multiple of 8 values.
+ * Ragged M, N and K tiles are handled by zero-filled loads and masked stores.
  *
  * Every wait inside the kernel is bounded (a few seconds); if one gives up
  * the kernel records GEMM_ERR_TIMEOUT in the device error word and returns

@@ -205,8 +205,8 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
         return GEMM_ERR_ALIGNMENT;
     // Rows on 16-byte boundaries (the TMA stride rule) take the TMA kernels;
     // anything else the kernels with load-and-swizzle producer warps (CTA
-    // pairs for M > 128), unless a workspace allows re-pitched copies for the
-    // CTA-pair TMA kernel.
+    // pairs for M > 128, the transposed product for M <= 128), unless a
+    // workspace allows re-pitched copies for the CTA-pair TMA kernel.
     const bool a_rows16 = rows_on_16_bytes(A, K);
     const bool b_rows16 = rows_on_16_bytes(B, N);
     const bool c_rows16 = rows_on_16_bytes(C, N);
@@ -288,13 +288,13 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     if (t_splits > 0 && a_rows16 && b_rows16)
         return finish(rtm::launch_gemm_tc_t(L, t_splits, true, s));
     // A or B rows off 16-byte boundaries: the transposed kernel with producer
-    // warps in place of TMA (the same K-splits), while the column tiles fit
-    // on the SMs at once; wider products take the persistent 128 x 256 tiles.
-    if (!tma_ok) {
-        if (t_tiles <= d.sms)
-            return finish(rtm::launch_gemm_tc_any_t(L, t_splits > 0 ? t_splits : 1, s));
-        return finish(rtm::launch_gemm_tc_any(L, s));
-    }
+    // warps in place of TMA, with the same K-split; without one (short K, or
+    // more column tiles than SMs) one CTA per tile, in waves where the tiles
+    // outnumber the SMs. That measured faster than persistent 128 x 256 tiles
+    // at every width (32 x 20002 x 8190: 228 -> 138 us; 64 x 24002 x 4094:
+    // 129 -> 88 us; 1 x 40001 x 1001: 70 -> 47 us).
+    if (!tma_ok)
+        return finish(rtm::launch_gemm_tc_any_t(L, t_splits > 0 ? t_splits : 1, s));
     // One CTA per 128 x BN tile. With M <= 128 there is one row of tiles, so
     // the widest BN that still gives 60 % of the SMs a tile is used (a sweep
     // of BN 256/128/64 over N = 1K..32K, K = 1K..8K on GB300 found it within

@@ -288,17 +288,16 @@ cudaError_t launch_gemm_tc_t(const TcLaunch &p, int splits, bool swap, cudaStrea
 // K has fewer than 32 64-deep blocks or the tiles outnumber the SMs, else the
 // largest S in {1, 2, 4, 8} with tiles * S <= sms and >= 16 blocks per CTA.
 int long_k_splits(long long tiles, long long K, int sms);
-// The same product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu):
+// The CTA-pair product for any K, N and 2-byte-aligned A, B (gemm_tc_any.cu;
+// 256 x 256 tiles, each CTA staging half of the operands), for M > 128:
 // operands loaded by producer warps instead of TMA (mute_producer: they load
-// nothing, so every wait gives up).
-cudaError_t launch_gemm_tc_any(const TcLaunch &p, cudaStream_t stream);
-// The same on CTA pairs (256 x 256 tiles, each CTA staging half of the
-// operands), for M > 128. Same operand rules; any 4-byte-aligned C.
+// nothing, so every wait gives up); any 4-byte-aligned C.
 cudaError_t launch_gemm_tc_any_pair(const TcLaunch &p, cudaStream_t stream);
-// Short products (M <= 128) on the same producers, computed as the transpose
+// Short products (M <= 128) with producer warps, computed as the transpose
 // like launch_gemm_tc_t with swap (gemm_tc_any_t.cu): CTAs own 128 columns and
-// tct_rows(M) rows, `splits` (1, 2, 4 or 8) CTAs of a cluster split K. Same
-// operand rules as launch_gemm_tc_any; any 4-byte-aligned C.
+// tct_rows(M) rows, `splits` (1, 2, 4 or 8) CTAs of a cluster split K; with
+// splits = 1 the column tiles may outnumber the SMs (several waves). Same
+// operand rules as launch_gemm_tc_any_pair.
 cudaError_t launch_gemm_tc_any_t(const TcLaunch &p, int splits, cudaStream_t stream);
 
 // The host-side argument checks of the fp32 entry points (api.cu), made
