@@ -153,13 +153,19 @@ GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspac
 
 /*
  * gemm_f32_workspace_bytes — bytes of scratch memory gemm_f32_ws uses for an
- * M x N x K product on the current device: 0 when the product has enough C
- * tiles to fill the GPU, or when splitting K over cluster CTAs (which needs
- * no workspace, see gemm_f32) is estimated to be at least as fast (gemm_f32_ws
- * then runs what gemm_f32 runs); otherwise the size of one of the two
- * workspace schedules below, whichever is estimated faster: splits * M * N * 4
- * for the K split, (tiles + ctas - 1) * 65536 for stream-K (tiles: the
- * product's 128 x 128 C tiles; ctas: the `splits` gemm_f32_schedule reports).
+ * M x N x K product on the current device, the sum of two parts:
+ *   - the schedule's own scratch: 0 when the product has enough C tiles to
+ *     fill the GPU, or when splitting K over cluster CTAs (which needs no
+ *     workspace, see gemm_f32) is estimated to be at least as fast; otherwise
+ *     the size of one of the two workspace schedules below, whichever is
+ *     estimated faster: splits * M * N * 4 for the K split, (tiles + ctas - 1)
+ *     * 65536 for stream-K (tiles: the product's 128 x 128 C tiles; ctas: the
+ *     `splits` gemm_f32_schedule reports);
+ *   - when the schedule runs on the kernels that stage K-slices with the
+ *     tensor-memory-access unit (stream-K, or 128 x 128, 256 x 64 or 64 x 256
+ *     tiles without the K split), room for re-pitched copies of the operands
+ *     whose rows the shape puts off 16-byte boundaries: ceil256(M * ceil4(K)
+ *     * 4) when K % 4 != 0, ceil256(K * ceil4(N) * 4) when N % 4 != 0.
  * Returns a negative status on invalid sizes (GEMM_ERR_INVALID_ARG) or when
  * no usable device is current (GEMM_ERR_LAUNCH, GEMM_ERR_DEVICE).
  *
@@ -179,8 +185,17 @@ GEMM_API int gemm_f32_schedule(int64_t M, int64_t N, int64_t K, int use_workspac
  *     parts of tiles shared by several CTAs go to the workspace and a second
  *     kernel adds them in increasing K order.
  * Both give bit-for-bit the same result from call to call. Otherwise (no
- * workspace schedule planned, or the workspace too small) it runs exactly
- * what gemm_f32 runs. The workspace contents on return are unspecified; two
+ * workspace schedule planned, or the workspace too small) it runs what
+ * gemm_f32 runs. Operands whose rows do not start on 16-byte boundaries (K or
+ * N not a multiple of 4, or A or B not 16-byte aligned) are first copied into
+ * the front of the workspace with rows padded to a multiple of 4 values (A's
+ * copy first, B's after it at a 256-byte-rounded offset, the schedule's own
+ * scratch after both) when the schedule then runs on tensor-memory-access
+ * staging only and the workspace holds the copies beside the schedule's
+ * scratch (or, for stream-K, at least the copies, for the cluster schedule it
+ * then runs); the copies change no sum, so where gemm_f32 runs the same
+ * schedule the results are the same bits. Any other schedule runs on the
+ * operands as given. The workspace contents on return are unspecified; two
  * calls in flight at once must not share a workspace. The splits are the
  * pages' global tiling applied to K as well as to C tiles
  * ("寄存器Tiling跨架构解析", sections 1.1 and 2.4: global tiling decides how much
@@ -205,7 +220,9 @@ GEMM_API int gemm_f32_ws(int64_t M, int64_t N, int64_t K,
  * runs what gemm_f32_ws runs with the built-in array as its workspace: the
  * split-K schedule when that split fits in 24 MiB (splits * M * N * 4 bytes,
  * see gemm_f32_workspace_bytes), and otherwise gemm_f32's own schedule, which
- * needs no scratch memory. Every valid product therefore succeeds.
+ * needs no scratch memory; re-pitched copies of operands whose rows are off
+ * 16-byte boundaries where they fit in the array beside that. Every valid
+ * product therefore succeeds.
  *
  * The first call on each device looks up the device address of the built-in
  * array (cudaGetSymbolAddress, with that device current); make that first

@@ -157,14 +157,44 @@ int64_t padded_copy_bytes(int64_t rows, int64_t cols)
 // ragged last wave may be split over clusters (sgemm_tail_plan). Unsplit
 // 128 x 128 tiles run on the TMA-fed kernel where the operands allow it.
 cudaError_t run_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,
-                          const rtm::SplitK &cluster, const DeviceInfo &d, cudaStream_t s)
+                          const rtm::SplitK &cluster, const DeviceInfo &d, cudaStream_t s,
+                          const rtm::SimtTma *prepared = nullptr)
 {
     rtm::SimtTma tma;
     tma.encode_tiled = encode_tiled_fn();
     tma.err = d.err;
     tma.wait_limit_ns = kDefaultWaitLimitNs;
+    if (prepared)
+        tma = *prepared;
     return rtm::launch_sgemm_f32_tiles(M, N, K, A, B, C, cluster, d.sms, s,
                                        tma.encode_tiled ? &tma : nullptr);
+}
+
+// Bytes of a copy of a rows x cols fp32 matrix with every row padded to a
+// multiple of 4 values (16 bytes), rounded up to 256 bytes.
+int64_t padded_copy_bytes_f32(int64_t rows, int64_t cols)
+{
+    return (rows * ((cols + 3) / 4 * 4) * 4 + 255) / 256 * 256;
+}
+
+// Scratch a gemm_f32_ws schedule needs for itself: stream-K partial tiles or
+// the workspace split's partial products.
+int64_t f32_schedule_bytes(const rtm::F32Schedule &f, int64_t M, int64_t N)
+{
+    if (f.streamk > 0)
+        return rtm::sgemm_streamk_workspace_floats((int)M, (int)N, f.streamk) *
+               (int64_t)sizeof(float);
+    return f.workspace.splits > 1 ? (int64_t)f.workspace.splits * M * N * (int64_t)sizeof(float)
+                                  : 0;
+}
+
+// Whether gemm_f32_ws may run `f` on re-pitched copies: stream-K, or no
+// workspace split and a schedule whose kernels are all TMA-fed (the cp.async
+// kernels read A and B with row strides K and N).
+bool f32_schedule_takes_copies(const rtm::F32Schedule &f, int M, int N, int K, int sms)
+{
+    return f.streamk > 0 ||
+           (f.workspace.splits <= 1 && rtm::sgemm_tiles_use_tma(M, N, K, f.cluster, sms));
 }
 
 bool rows_on_16_bytes(const void *base, int64_t cols)
@@ -443,11 +473,10 @@ int64_t gemm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K)
     if (M <= rtm::kShortMaxM)
         return 0;  // short, wide products split K without a workspace
     const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
-    if (f.streamk > 0)
-        return rtm::sgemm_streamk_workspace_floats((int)M, (int)N, f.streamk) *
-               (int64_t)sizeof(float);
-    const rtm::SplitK &plan = f.workspace;
-    return plan.splits > 1 ? (int64_t)plan.splits * M * N * (int64_t)sizeof(float) : 0;
+    int64_t copies = 0;  // rows the shape puts off 16-byte boundaries, re-pitched
+    if (f32_schedule_takes_copies(f, (int)M, (int)N, (int)K, d.sms))
+        copies = (K % 4 ? padded_copy_bytes_f32(M, K) : 0) + (N % 4 ? padded_copy_bytes_f32(K, N) : 0);
+    return copies + f32_schedule_bytes(f, M, N);
 }
 
 int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B, float *C,
@@ -474,30 +503,78 @@ int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A, const float *B,
     if (M <= rtm::kShortMaxM)
         return finish(run_f32_plain((int)M, (int)N, (int)K, A, B, C, d, s));
     const rtm::F32Schedule f = rtm::sgemm_ws_schedule((int)M, (int)N, (int)K, d.sms);
-    if (f.streamk > 0) {
-        // Stream-K needs the TMA-fed kernel (K % 4 == 0, N % 4 == 0, 16-byte
-        // aligned A, B and workspace); otherwise gemm_f32's schedule runs.
-        const int64_t need = rtm::sgemm_streamk_workspace_floats((int)M, (int)N, f.streamk) * 4;
-        rtm::SimtTma tma;
-        tma.encode_tiled = encode_tiled_fn();
-        tma.err = d.err;
-        tma.wait_limit_ns = kDefaultWaitLimitNs;
-        if (workspace_bytes >= need && tma.encode_tiled &&
-            (reinterpret_cast<uintptr_t>(workspace) & 15) == 0 &&
-            rtm::sgemm_tma_eligible((int)M, (int)N, (int)K, A, B)) {
-            if (overlaps(workspace, need, A, M * K * 4) || overlaps(workspace, need, B, K * N * 4) ||
-                overlaps(workspace, need, C, M * N * 4))
-                return GEMM_ERR_INVALID_ARG;
-            return finish(rtm::launch_sgemm_f32_streamk((int)M, (int)N, (int)K, A, B, C, tma,
-                                                        f.streamk, f.streamk <= d.sms,
-                                                        static_cast<float *>(workspace), s));
+    rtm::SimtTma tma;
+    tma.encode_tiled = encode_tiled_fn();
+    tma.err = d.err;
+    tma.wait_limit_ns = kDefaultWaitLimitNs;
+    // Operands whose rows are off 16-byte boundaries are first re-pitched into
+    // the front of the workspace (rows padded to a multiple of 4 values), when
+    // the schedule then runs on TMA-fed kernels only and the workspace holds
+    // the copies beside the schedule's own scratch (or, for stream-K, at least
+    // the copies: the cluster schedule it falls back to reads them too). The
+    // TMA kernels read the copies through their row strides; the sums are the
+    // same as on the originals.
+    const float *Ar = A, *Br = B;
+    uint8_t *scratch = static_cast<uint8_t *>(workspace);
+    int64_t scratch_bytes = workspace_bytes;
+    const bool a_rows16 = K % 4 == 0 && (reinterpret_cast<uintptr_t>(A) & 15) == 0;
+    const bool b_rows16 = N % 4 == 0 && (reinterpret_cast<uintptr_t>(B) & 15) == 0;
+    const int64_t copy_a = a_rows16 ? 0 : padded_copy_bytes_f32(M, K);
+    const int64_t copy_b = b_rows16 ? 0 : padded_copy_bytes_f32(K, N);
+    const int64_t copies = copy_a + copy_b;
+    const int64_t own = f32_schedule_bytes(f, M, N);
+    const bool tiles_tma = rtm::sgemm_tiles_use_tma((int)M, (int)N, (int)K, f.cluster, d.sms);
+    if (copies > 0 && tma.encode_tiled && (reinterpret_cast<uintptr_t>(workspace) & 15) == 0 &&
+        f32_schedule_takes_copies(f, (int)M, (int)N, (int)K, d.sms) &&
+        (workspace_bytes >= copies + own || (workspace_bytes >= copies && tiles_tma))) {
+        if (overlaps(workspace, copies, A, M * K * 4) || overlaps(workspace, copies, B, K * N * 4) ||
+            overlaps(workspace, copies, C, M * N * 4))
+            return GEMM_ERR_INVALID_ARG;
+        if (copy_a) {
+            const int64_t lda = (K + 3) / 4 * 4;
+            cudaError_t e = rtm::launch_pack_rows_4b(A, M, K, reinterpret_cast<float *>(scratch), lda,
+                                                     d.sms, s);
+            if (e != cudaSuccess)
+                return finish(e);
+            Ar = reinterpret_cast<const float *>(scratch);
+            tma.lda = lda;
         }
-        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, d, s));
+        if (copy_b) {
+            const int64_t ldb = (N + 3) / 4 * 4;
+            cudaError_t e = rtm::launch_pack_rows_4b(B, K, N, reinterpret_cast<float *>(scratch + copy_a),
+                                                     ldb, d.sms, s);
+            if (e != cudaSuccess)
+                return finish(e);
+            Br = reinterpret_cast<const float *>(scratch + copy_a);
+            tma.ldb = ldb;
+        }
+        scratch += copies;
+        scratch_bytes -= copies;
+    }
+    const bool repitched = Ar != A || Br != B;
+    if (f.streamk > 0) {
+        // Stream-K needs the TMA-fed kernel (row strides multiples of 4 values,
+        // 16-byte aligned A, B and scratch); otherwise gemm_f32's schedule runs.
+        if (scratch_bytes >= own && tma.encode_tiled &&
+            (reinterpret_cast<uintptr_t>(scratch) & 15) == 0 &&
+            rtm::sgemm_tma_eligible((int)M, (int)N, (int)K, Ar, Br, tma.lda, tma.ldb)) {
+            if (overlaps(scratch, own, A, M * K * 4) || overlaps(scratch, own, B, K * N * 4) ||
+                overlaps(scratch, own, C, M * N * 4))
+                return GEMM_ERR_INVALID_ARG;
+            return finish(rtm::launch_sgemm_f32_streamk((int)M, (int)N, (int)K, Ar, Br, C, tma,
+                                                        f.streamk, f.streamk <= d.sms,
+                                                        reinterpret_cast<float *>(scratch), s));
+        }
+        return finish(run_f32_tiles((int)M, (int)N, (int)K, Ar, Br, C, f.cluster, d, s,
+                                    repitched ? &tma : nullptr));
     }
     const rtm::SplitK &plan = f.workspace;
-    const int64_t need = plan.splits > 1 ? (int64_t)plan.splits * M * N * 4 : 0;
-    if (need == 0 || workspace_bytes < need)
-        return finish(run_f32_tiles((int)M, (int)N, (int)K, A, B, C, f.cluster, d, s));
+    const int64_t need = own;
+    if (need == 0 || scratch_bytes < need)
+        return finish(run_f32_tiles((int)M, (int)N, (int)K, Ar, Br, C, f.cluster, d, s,
+                                    repitched ? &tma : nullptr));
+    // The workspace split runs the cp.async kernels on the operands as given
+    // (nothing is re-pitched for it).
     if (overlaps(workspace, need, A, M * K * 4) || overlaps(workspace, need, B, K * N * 4) ||
         overlaps(workspace, need, C, M * N * 4))
         return GEMM_ERR_INVALID_ARG;

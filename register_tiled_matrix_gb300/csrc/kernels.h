@@ -111,12 +111,17 @@ struct SimtTma {
     int *err = nullptr;
     uint64_t wait_limit_ns = 0;
     bool mute = false;  // failure-detection self-test: announce the slices, load nothing
+    // Row strides of A and B in elements (0: K and N), for operands re-pitched
+    // into a workspace; read only by the tensor maps.
+    int64_t lda = 0, ldb = 0;
 };
 // The plain 128 x 128 product with its K slices loaded by TMA (sgemm_tma.cu):
 // tiles 0 .. tile_count - 1 of the grouped raster (tile_count < 0: all).
-// Needs sgemm_tma_eligible: K % 4 == 0, N % 4 == 0, A and B 16-byte aligned.
-// Same sums in the same order as the cp.async kernel (same bits).
-bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B);
+// Needs sgemm_tma_eligible: row strides of A and B (lda, ldb; 0: K and N)
+// multiples of 4 elements, A and B 16-byte aligned. Same sums in the same
+// order as the cp.async kernel (same bits).
+bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B, int64_t lda = 0,
+                        int64_t ldb = 0);
 // mute: the failure-detection self-test (no loads are issued; every bounded
 // wait runs out; C is left unspecified).
 cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const float *B, float *C,
@@ -207,6 +212,11 @@ TailPlan sgemm_tail_plan(int M, int N, int K, int sm_count);
 cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const float *B, float *C,
                                   const TailPlan &plan, cudaStream_t stream,
                                   const SimtTma *tma = nullptr);
+// Whether launch_sgemm_f32_tiles runs this schedule on TMA-fed kernels when
+// the operands allow it (128 x 128, 256 x 64 or 64 x 256 tiles, or the tail
+// split); otherwise it runs the cp.async kernels, which read A and B with row
+// strides K and N.
+bool sgemm_tiles_use_tma(int M, int N, int K, const SplitK &cluster, int sm_count);
 // The register-tiled product on its own schedule: K split over clusters when
 // cluster.splits > 1, else the tail plan, else the plain product (its
 // unsplit 128 x 128 tiles on the TMA-fed kernel when `tma` is set and the
@@ -274,6 +284,9 @@ long long pair_split_from(long long ntiles, int pairs, int kblocks, bool c_vec);
 // 0, dst 16-byte aligned), so that every row starts on a 16-byte boundary
 // (pack.cu). Values in columns cols .. ld-1 of dst are unspecified.
 cudaError_t launch_pack_rows_2b(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst,
+                                int64_t ld, int sm_count, cudaStream_t stream);
+// The same for 4-byte values (fp32): ld a multiple of 4 elements.
+cudaError_t launch_pack_rows_4b(const float *src, int64_t rows, int64_t cols, float *dst,
                                 int64_t ld, int sm_count, cudaStream_t stream);
 // Products with one short side and K split over CTA clusters (gemm_tc_t.cu).
 // swap: short, wide products as C^T = B^T.A^T, CTAs own 128 columns of C and

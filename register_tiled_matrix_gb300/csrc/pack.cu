@@ -1,5 +1,6 @@
-// Row re-pitching copy for the tensor-core path: moves a row-major matrix of
-// 2-byte values whose rows do not start on 16-byte boundaries (an odd number
+// Row re-pitching copy for the TMA-fed kernels: moves a row-major matrix of
+// 2-byte (or, as pairs of them, 4-byte) values whose rows do not start on
+// 16-byte boundaries (an odd number
 // of columns modulo 8, or an offset base pointer) into a buffer whose rows do,
 // so the tensor-memory-access unit can stage it. This is the global level of
 // the pages' tiling made possible on Blackwell: a TMA box must start on a
@@ -88,6 +89,15 @@ cudaError_t launch_pack_rows_2b(const uint16_t *src, int64_t rows, int64_t cols,
         pack::pack_rows_kernel<int64_t><<<(unsigned)blocks, 256, 0, stream>>>(src, rows, cols,
                                                                                dst, ld);
     return cudaGetLastError();
+}
+
+// A row of cols 4-byte values is a row of 2 cols 2-byte values, and a stride
+// of ld (a multiple of 4) one of 2 ld (a multiple of 8): the same copy.
+cudaError_t launch_pack_rows_4b(const float *src, int64_t rows, int64_t cols, float *dst,
+                                int64_t ld, int sm_count, cudaStream_t stream)
+{
+    return launch_pack_rows_2b(reinterpret_cast<const uint16_t *>(src), rows, 2 * cols,
+                               reinterpret_cast<uint16_t *>(dst), 2 * ld, sm_count, stream);
 }
 
 } // namespace rtm

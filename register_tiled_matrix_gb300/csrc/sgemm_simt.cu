@@ -48,7 +48,10 @@ namespace rtm {
 namespace simt {
 
 constexpr int kThreads = 256;  // 16 x 16 threads
-constexpr int kGroupM = 8;     // tile-rows per L2 group
+// Tile-rows per L2 group: the TMA-fed kernels' value, so that both visit the
+// tiles in the same order and a ragged last wave split over clusters holds
+// the same tiles whichever kernel stages the operands (the same bits).
+constexpr int kGroupM = 16;
 
 // How K is split (one CTA per K chunk and C tile; the chunk index is blockIdx.y).
 enum SplitMode : int {
@@ -683,10 +686,10 @@ cudaError_t launch_sgemm_f32(int M, int N, int K, const float *A, const float *B
     // Without a choice, 64-row tiles for M <= 64 (128-row tiles would be at
     // least half empty) and 64-column tiles for N <= 64.
     const SimtTile t = simt_resolve_tile(tile, M, N);
-    if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B))
+    if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B, tma->lda, tma->ldb))
         return launch_sgemm_f32_tma(M, N, K, A, B, C, *tma, -1, stream);
     if (tma && ((t.m == kTallTileM && t.n == kNarrowN) || (t.m == kShortTileM && t.n == kWideTileN)) &&
-        sgemm_tma_eligible(M, N, K, A, B))
+        sgemm_tma_eligible(M, N, K, A, B, tma->lda, tma->ldb))
         return launch_sgemm_f32_tma_rect(t, M, N, K, A, B, C, *tma, 1,
                                          (K + kSliceK - 1) / kSliceK * kSliceK, false, stream);
     return launch_tile<simt::kPlain>(t, M, N, K, A, B, C, stream);
@@ -791,11 +794,11 @@ cudaError_t launch_sgemm_f32_cluster(int M, int N, int K, const float *A, const 
                                      const SplitK &plan, cudaStream_t stream, const SimtTma *tma)
 {
     const SimtTile t = simt_resolve_tile(plan.tile, M, N);
-    if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B))
+    if (tma && t.m == kTileM && t.n == kTileN && sgemm_tma_eligible(M, N, K, A, B, tma->lda, tma->ldb))
         return launch_sgemm_f32_tma_cluster(M, N, K, A, B, C, *tma, plan.splits, plan.kchunk,
                                             plan.spread, 0, -1, stream);
     if (tma && ((t.m == kTallTileM && t.n == kNarrowN) || (t.m == kShortTileM && t.n == kWideTileN)) &&
-        sgemm_tma_eligible(M, N, K, A, B))
+        sgemm_tma_eligible(M, N, K, A, B, tma->lda, tma->ldb))
         return launch_sgemm_f32_tma_rect(t, M, N, K, A, B, C, *tma, plan.splits, plan.kchunk,
                                          plan.spread, stream);
     return launch_tile<simt::kSplitCluster>(t, M, N, K, A, B, C, stream, plan.splits, plan.kchunk,
@@ -809,7 +812,7 @@ cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const flo
     if (M <= kShortTileM || N <= kNarrowN || plan.tail.splits < 2)
         return cudaErrorInvalidValue;
     cudaError_t e = cudaSuccess;
-    const bool use_tma = tma && sgemm_tma_eligible(M, N, K, A, B);
+    const bool use_tma = tma && sgemm_tma_eligible(M, N, K, A, B, tma->lda, tma->ldb);
     if (plan.plain_tiles > 0 && use_tma)
         e = launch_sgemm_f32_tma(M, N, K, A, B, C, *tma, plan.plain_tiles, stream);
     else if (plan.plain_tiles > 0)
@@ -822,6 +825,18 @@ cudaError_t launch_sgemm_f32_tail(int M, int N, int K, const float *A, const flo
                                             plan.tail.kchunk, false, plan.plain_tiles, -1, stream);
     return simt::launch_any<kTileM, kTileN, kSliceK, 2, 2, 1, kSplitCluster>(
         M, N, K, A, B, C, stream, plan.tail.splits, plan.tail.kchunk, false, plan.plain_tiles);
+}
+
+bool sgemm_tiles_use_tma(int M, int N, int K, const SplitK &cluster, int sm_count)
+{
+    const SimtTile t = simt_resolve_tile(cluster.tile, M, N);
+    const bool tma_tile = (t.m == kTileM && t.n == kTileN) || (t.m == kTallTileM && t.n == kNarrowN) ||
+                          (t.m == kShortTileM && t.n == kWideTileN);
+    if (cluster.splits > 1)
+        return tma_tile;
+    if (sgemm_tail_plan(M, N, K, sm_count).tail.splits > 1)
+        return true;  // 128 x 128 tiles
+    return tma_tile;
 }
 
 cudaError_t launch_sgemm_f32_tiles(int M, int N, int K, const float *A, const float *B, float *C,

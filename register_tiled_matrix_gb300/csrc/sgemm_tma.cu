@@ -748,11 +748,12 @@ __global__ void __launch_bounds__(kThreads)
 
 } // namespace simt_tma
 
-bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B)
+bool sgemm_tma_eligible(int M, int N, int K, const float *A, const float *B, int64_t lda,
+                        int64_t ldb)
 {
     (void)M;
-    return K % 4 == 0 && N % 4 == 0 && (reinterpret_cast<uintptr_t>(A) & 15) == 0 &&
-           (reinterpret_cast<uintptr_t>(B) & 15) == 0;
+    return (lda ? lda : K) % 4 == 0 && (ldb ? ldb : N) % 4 == 0 &&
+           (reinterpret_cast<uintptr_t>(A) & 15) == 0 && (reinterpret_cast<uintptr_t>(B) & 15) == 0;
 }
 
 cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const float *B, float *C,
@@ -760,7 +761,7 @@ cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const floa
                                  bool mute)
 {
     using namespace simt_tma;
-    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B))
+    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B, tma.lda, tma.ldb))
         return cudaErrorInvalidValue;
     const long long all_tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const long long tiles = tile_count < 0 || tile_count > all_tiles ? all_tiles : tile_count;
@@ -770,10 +771,12 @@ cudaError_t launch_sgemm_f32_tma(int M, int N, int K, const float *A, const floa
         return cudaSuccess;
     auto fn = reinterpret_cast<EncodeTiledFn>(tma.encode_tiled);
     CUtensorMap ta, tb;
-    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                        (uint64_t)tma.lda) ||
+        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        (uint64_t)tma.ldb))
         return cudaErrorInvalidValue;
-    const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;  // N % 4 == 0 already
+    const bool c_vec = N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0;
     // Muted (the self-test) or not, the epilogue stores whatever C's alignment allows.
     const bool m = mute || tma.mute;
     auto kernel = m ? (c_vec ? sgemm_tma_kernel<true, true> : sgemm_tma_kernel<false, true>)
@@ -793,7 +796,7 @@ cudaError_t launch_sgemm_f32_tma_cluster(int M, int N, int K, const float *A, co
                                          cudaStream_t stream)
 {
     using namespace simt_tma;
-    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B) ||
+    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B, tma.lda, tma.ldb) ||
         (splits != 1 && splits != 2 && splits != 4 && splits != 8) || kchunk % BK != 0 ||
         (long long)splits * kchunk < K)
         return cudaErrorInvalidValue;
@@ -807,10 +810,12 @@ cudaError_t launch_sgemm_f32_tma_cluster(int M, int N, int K, const float *A, co
         return cudaSuccess;
     auto fn = reinterpret_cast<EncodeTiledFn>(tma.encode_tiled);
     CUtensorMap ta, tb;
-    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                        (uint64_t)tma.lda) ||
+        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        (uint64_t)tma.ldb))
         return cudaErrorInvalidValue;
-    const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+    const bool c_vec = N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0;
     auto kernel = tma.mute ? (c_vec ? sgemm_tma_cluster_kernel<true, true>
                                     : sgemm_tma_cluster_kernel<false, true>)
                            : (c_vec ? sgemm_tma_cluster_kernel<true> : sgemm_tma_cluster_kernel<false>);
@@ -847,7 +852,7 @@ cudaError_t launch_sgemm_f32_streamk(int M, int N, int K, const float *A, const 
                                      cudaStream_t stream)
 {
     using namespace simt_tma;
-    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B) || ctas < 1 ||
+    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B, tma.lda, tma.ldb) || ctas < 1 ||
         !workspace || (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)
         return cudaErrorInvalidValue;
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
@@ -860,10 +865,12 @@ cudaError_t launch_sgemm_f32_streamk(int M, int N, int K, const float *A, const 
         ctas = (int)iters;
     auto fn = reinterpret_cast<EncodeTiledFn>(tma.encode_tiled);
     CUtensorMap ta, tb;
-    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                        (uint64_t)tma.lda) ||
+        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        (uint64_t)tma.ldb))
         return cudaErrorInvalidValue;
-    const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+    const bool c_vec = N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0;
     auto kernel = c_vec ? sgemm_tma_streamk_kernel<true> : sgemm_tma_streamk_kernel<false>;
     static std::atomic<uint64_t> done_vec{0}, done_any{0};
     cudaError_t e = set_smem_limit_once(kernel, kSpreadSmem, c_vec ? done_vec : done_any);

@@ -350,7 +350,7 @@ static cudaError_t launch_rect(int M, int N, int K, const float *A, const float 
                                cudaStream_t stream)
 {
     using Sh = Shape<BM, BN>;
-    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B) ||
+    if (!tma.encode_tiled || !tma.err || !sgemm_tma_eligible(M, N, K, A, B, tma.lda, tma.ldb) ||
         (splits != 1 && splits != 2 && splits != 4 && splits != 8) || kchunk % BK != 0 ||
         kchunk <= 0 || (long long)splits * kchunk < K)
         return cudaErrorInvalidValue;
@@ -361,10 +361,12 @@ static cudaError_t launch_rect(int M, int N, int K, const float *A, const float 
         return cudaErrorInvalidValue;
     auto fn = reinterpret_cast<EncodeTiledFn>(tma.encode_tiled);
     CUtensorMap ta, tb;
-    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_f32_map(fn, &ta, A, (uint64_t)M, (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                        (uint64_t)tma.lda) ||
+        !encode_f32_map(fn, &tb, B, (uint64_t)K, (uint64_t)N, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        (uint64_t)tma.ldb))
         return cudaErrorInvalidValue;
-    const bool c_vec = (reinterpret_cast<uintptr_t>(C) & 15) == 0;  // N % 4 == 0 already
+    const bool c_vec = N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0;
     auto kernel = tma.mute ? (c_vec ? sgemm_tma_rect_kernel<BM, BN, true, true>
                                     : sgemm_tma_rect_kernel<BM, BN, false, true>)
                            : (c_vec ? sgemm_tma_rect_kernel<BM, BN, true>

@@ -52,10 +52,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 // boxes of box_rows x box_cols; zeros outside the matrix.
 inline bool encode_f32_map(EncodeTiledFn fn, CUtensorMap *map, const float *base, uint64_t rows,
                            uint64_t cols, uint32_t box_cols, uint32_t box_rows,
-                           CUtensorMapSwizzle swizzle)
+                           CUtensorMapSwizzle swizzle, uint64_t ld = 0)
 {
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 4};
+    cuuint64_t strides[1] = {(ld ? ld : cols) * 4};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,

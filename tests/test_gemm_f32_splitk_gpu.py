@@ -25,22 +25,32 @@ def run_ws(A, B):
     return C
 
 
+def _copy_bytes(rows, cols):
+    return (rows * ((cols + 3) // 4 * 4) * 4 + 255) // 256 * 256
+
+
 # Workspace only where the schedule prices a workspace schedule below the split
 # over cluster CTAs (which needs none): the workspace split (long K over few
-# tiles of 64 rows or columns) or stream-K (few 128 x 128 tiles, K % 4 == 0,
-# N % 4 == 0). 8192 x 64 x 4096 (on 256 x 64 tiles), 1000 x 1000 x 999 (K % 4
-# != 0) and 256^3 split over clusters; 4096^3 and 4097 x 3001 x 1023 fill the
-# GPU unsplit.
+# tiles of 64 rows or columns) or stream-K (few 128 x 128 tiles); and, for a
+# schedule on TMA-fed kernels, re-pitched copies of the operands whose rows the
+# shape puts off 16-byte boundaries (A for K % 4 != 0, B for N % 4 != 0).
+# 8192 x 64 x 4096 (on 256 x 64 tiles) and 256^3 split over clusters, 4096^3
+# fills the GPU unsplit: none. 1000 x 1000 x 999 splits over clusters and
+# 4097 x 3001 x 1023 splits its last wave over clusters, both on 128 x 128
+# tiles: copies only.
 @pytest.mark.parametrize("M,N,K,kind", [(48, 2048, 8192, "ws"), (512, 512, 8192, "sk"),
                                         (8192, 64, 4096, None), (2048, 128, 4096, "sk"),
-                                        (1024, 1024, 1024, "sk"), (1000, 1000, 999, None),
+                                        (1024, 1024, 1024, "sk"), (1000, 1000, 999, "copies"),
                                         (256, 256, 256, None), (4096, 4096, 4096, None),
-                                        (4097, 3001, 1023, None)])
+                                        (4097, 3001, 1023, "copies")])
 def test_workspace_size_policy(M, N, K, kind):
     n = rtm.gemm_f32_workspace_bytes(M, N, K)
     assert (n > 0) == (kind is not None)
     sched, splits = rtm.gemm_f32_schedule(M, N, K, workspace=True)
-    if kind == "ws":
+    if kind == "copies":
+        assert sched in ("tiles+cluster-split", "tiles+tail-cluster-split")
+        assert n == (_copy_bytes(M, K) if K % 4 else 0) + (_copy_bytes(K, N) if N % 4 else 0)
+    elif kind == "ws":
         assert sched == "tiles+workspace-split"
         assert n % (M * N * 4) == 0 and n // (M * N * 4) == splits and 2 <= splits <= 32
     elif kind == "sk":
