@@ -287,8 +287,10 @@ GEMM_API int gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
  * K-blocks or more column tiles than SMs, where C must be 16-byte aligned
  * with N % 8 == 0 as well); otherwise by producer warps that copy them 2, 4
  * or 8 bytes at a time into the same swizzled layout (for M > 128 on CTA
- * pairs; for M <= 128 on the transposed product, with the same K-split where
- * one applies). This is slower than the TMA staging, with the same
+ * pairs, or for tall, narrow products, N <= 128 with at least 32 K-blocks, on
+ * 128-row tiles with the same K-split as on aligned rows; for M <= 128 on the
+ * transposed product, with the same K-split where one applies). This is
+ * slower than the TMA staging, with the same
  * arithmetic: for M > 128 the results equal gemm_bf16f32_ws's bit for bit
  * unless that call adds two K halves of a tile, which it may do only when C
  * rows are 16-byte aligned and K >= 4096; for M <= 128 with at least 32
@@ -335,7 +337,10 @@ GEMM_API int gemm_f16f32(int64_t M, int64_t N, int64_t K,
  * tiling adapted to Blackwell, whose tensor-memory-access unit can only start
  * a tile on a 16-byte boundary; the arithmetic is unchanged. When no copy is
  * needed, or the workspace is null, misaligned or smaller than the copies,
- * the call runs exactly what gemm_bf16f32 / gemm_f16f32 runs. The workspace
+ * and for tall, narrow products (N <= 128 with at least 32 K-blocks and the
+ * 128-row tiles fitting on the SMs), which the producer warps compute faster
+ * than the copies would allow, the call runs exactly what gemm_bf16f32 /
+ * gemm_f16f32 runs. The workspace
  * contents on return are unspecified; two calls in flight at once must not
  * share a workspace. A workspace that overlaps A, B or C returns
  * GEMM_ERR_INVALID_ARG.

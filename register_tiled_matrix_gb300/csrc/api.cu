@@ -279,6 +279,13 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
             return finish(rtm::launch_gemm_tc_t(L, s_splits, false, s));
         if (need == 0)
             return finish(rtm::launch_gemm_tc_pair(L, s));
+        // Tall and narrow with long K on rows off 16-byte boundaries: the
+        // tiling above with producer warps in place of TMA, with or without a
+        // workspace (a 256-wide pair tile would be mostly zero fill; on GB300,
+        // 4097 x 100 x 8190: pairs 108 us, re-pitch + TMA pairs 55 us, this
+        // 33 us; 8192 x 62 x 4094: 58, 54, 27 us).
+        if (N <= 128 && s_splits > 0)
+            return finish(rtm::launch_gemm_tc_any_t(L, s_splits, false, s));
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         if (ws && (reinterpret_cast<uintptr_t>(ws) & 15) == 0 && workspace_bytes >= need) {
             if (overlaps(ws, need, A, M * K * 2) || overlaps(ws, need, B, K * N * 2) ||
@@ -324,7 +331,7 @@ int run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t 
     // at every width (32 x 20002 x 8190: 228 -> 138 us; 64 x 24002 x 4094:
     // 129 -> 88 us; 1 x 40001 x 1001: 70 -> 47 us).
     if (!tma_ok)
-        return finish(rtm::launch_gemm_tc_any_t(L, t_splits > 0 ? t_splits : 1, s));
+        return finish(rtm::launch_gemm_tc_any_t(L, t_splits > 0 ? t_splits : 1, true, s));
     // One CTA per 128 x BN tile. With M <= 128 there is one row of tiles, so
     // the widest BN that still gives 60 % of the SMs a tile is used (a sweep
     // of BN 256/128/64 over N = 1K..32K, K = 1K..8K on GB300 found it within

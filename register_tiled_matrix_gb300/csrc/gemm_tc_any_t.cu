@@ -68,13 +68,15 @@ struct Cfg {
     static_assert(PART_BYTES <= RING_BYTES, "partial tile must fit the stage ring");
 };
 
-// kind::f16, D fp32, A and B both bf16 (1) or both fp16 (0); the MMA's A
-// (= B^T) MN-major, its B (= A^T) K-major; N = MN, M = 128.
-template <bool F16, int MN>
+// kind::f16, D fp32, A and B both bf16 (1) or both fp16 (0); N = MN, M = 128.
+// SWAP: the MMA's A (= B^T) MN-major, its B (= A^T) K-major; otherwise A
+// K-major and B MN-major.
+template <bool F16, int MN, bool SWAP>
 __host__ __device__ constexpr uint32_t idesc_t()
 {
-    return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) | (1u << 15) |
-           (0u << 16) | ((uint32_t)(MN >> 3) << 17) | ((uint32_t)(BNT >> 4) << 24);
+    return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) |
+           ((SWAP ? 1u : 0u) << 15) | ((SWAP ? 0u : 1u) << 16) | ((uint32_t)(MN >> 3) << 17) |
+           ((uint32_t)(BNT >> 4) << 24);
 }
 
 struct Params {
@@ -86,20 +88,22 @@ struct Params {
     unsigned long long limit_ns;
     int splits;         // CTAs per cluster, each summing one K-range
     int mute_producer;  // failure-detection self-test: the producer warps load nothing
+    int c_vec;          // C rows 16-byte aligned (float4 row stores without the swap)
 };
 
-// One K-slice of 2-byte values (V = 1) in a producer thread's registers: MN
-// rows of A (k0 .. k0+63) and 64 k-rows of B (columns n0 .. n0+127), a lane
-// per element, coalesced along k for A and along n for B; warp w holds rows
-// AR w .. AR w + AR - 1 of A and k-rows BR w .. BR w + BR - 1 of B. A and B
-// check their bounds apart: B's columns are interior for all but the last
+// One K-slice of 2-byte values (V = 1) in a producer thread's registers:
+// AROWS rows of A (k0 .. k0+63) and 64 k-rows of B (BCOLS columns from n0), a
+// lane per element, coalesced along k for A and along n for B; warp w holds
+// rows AR w .. AR w + AR - 1 of A and k-rows BR w .. BR w + BR - 1 of B. A and
+// B check their bounds apart: B's columns are interior for all but the last
 // column tile whatever M is.
-template <int PT, int MN>
+template <int PT, int AROWS, int BCOLS>
 struct Slice1 {
     static constexpr int PW = PT / 32;
-    static constexpr int AR = MN / PW, AE = BK / 32;
-    static constexpr int BR = BK / PW, BE = BNT / 32;
-    static_assert(AR >= 1 && AR * PW == MN && BR * PW == BK, "whole rows per producer warp");
+    static constexpr int AR = AROWS / PW, AE = BK / 32;
+    static constexpr int BR = BK / PW, BE = BCOLS / 32;
+    static_assert(AR >= 1 && AR * PW == AROWS && BR * PW == BK && BE >= 1,
+                  "whole rows per producer warp");
     uint16_t a[AR][AE], b[BR][BE];
 
     __device__ __forceinline__ void load(const Params &p, int tid, int m0, int n0, int k0)
@@ -108,7 +112,7 @@ struct Slice1 {
         const uint16_t *pa = p.A + (size_t)(m0 + warp * AR) * p.K + (k0 + lane);
         const uint16_t *pb = p.B + (size_t)(k0 + warp * BR) * p.N + (n0 + lane);
         const bool k_in = k0 + BK <= p.K;
-        if (k_in && n0 + BNT <= p.N) {
+        if (k_in && n0 + BCOLS <= p.N) {
 #pragma unroll
             for (int kr = 0; kr < BR; ++kr)
 #pragma unroll
@@ -156,12 +160,12 @@ constexpr int producer_warps(int v) { return v == 1 ? 16 : 8; }
 constexpr int kStages = 4;
 
 // 2-byte slices a producer thread keeps in registers (a register per value):
-// two for MN = 32 (20 values each), one above, within the 80 registers a
-// thread of a 672-thread CTA can have (two of MN = 64 spill).
-template <int MN>
+// two of up to 20 values (MN = 32 with the swap), one above, within the 80
+// registers a thread of a 672-thread CTA can have (two of 24 spill).
+template <typename Slice>
 constexpr int ring_depth_2byte()
 {
-    return MN <= 32 ? 2 : 1;
+    return Slice::AR * Slice::AE + Slice::BR * Slice::BE <= 20 ? 2 : 1;
 }
 
 template <int V>
@@ -179,11 +183,12 @@ __device__ __forceinline__ void cp_async_v(uint32_t dst, const void *src, uint32
 // multiple of 8 and B_STEP of 4, so a vector's swizzled offset is one of two
 // per thread (every other vector of B has the first one's swizzle phase, the
 // others that of row + 4).
-template <int V, int PT, int MN>
+template <int V, int PT, int AROWS, int BCOLS>
 struct AsyncPlan {
-    static constexpr int A_ROW = BK / V, A_PER = MN * A_ROW / PT, A_STEP = PT / A_ROW;
-    static constexpr int B_ROW = BNT / V, B_PER = BK * B_ROW / PT, B_STEP = PT / B_ROW;
-    static_assert(A_PER >= 1 && A_PER * PT == MN * A_ROW && B_PER * PT == BK * B_ROW,
+    static constexpr int A_ROW = BK / V, A_PER = AROWS * A_ROW / PT, A_STEP = PT / A_ROW;
+    static constexpr int B_ROW = BCOLS / V, B_PER = BK * B_ROW / PT, B_STEP = PT / B_ROW;
+    static_assert(A_PER >= 1 && A_PER * PT == AROWS * A_ROW && B_PER >= 1 &&
+                      B_PER * PT == BK * B_ROW,
                   "every producer thread copies whole vectors of both operands");
     static_assert(A_STEP % 8 == 0 && B_STEP % 4 == 0, "swizzle phase fixed per vector");
     // Byte offset of B vector j from the offsets of rows br and br + 4.
@@ -196,7 +201,7 @@ struct AsyncPlan {
     }
 };
 
-template <bool F16, int MN, int V>
+template <bool F16, int MN, int V, bool SWAP>
 __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
     gemm_tc_any_t_kernel(const Params p)
 {
@@ -205,6 +210,10 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
     constexpr int PW = producer_warps(V);
     constexpr int PT = PW * 32;
     constexpr int kMmaWarp = PW;
+    // The MMA's 128-row side (first in a stage) holds B^T with the swap, A
+    // without; its N side (after it) A^T or B.
+    constexpr int AROWS = SWAP ? MN : BNT, BCOLS = SWAP ? BNT : MN;
+    constexpr uint32_t A_OFF = SWAP ? BT_BYTES : 0u, B_OFF = SWAP ? 0u : BT_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -219,9 +228,16 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
     const int S = p.splits;
     const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
     const int unit = blockIdx.x / S;
-    const int tiles_n = (p.N + BNT - 1) / BNT;
-    const int n0 = (unit % tiles_n) * BNT;
-    const int m0 = (unit / tiles_n) * MN;
+    int m0, n0;
+    if constexpr (SWAP) {
+        const int tiles_n = (p.N + BNT - 1) / BNT;
+        n0 = (unit % tiles_n) * BNT;
+        m0 = (unit / tiles_n) * MN;
+    } else {
+        const int tiles_m = (p.M + BNT - 1) / BNT;
+        m0 = (unit % tiles_m) * BNT;
+        n0 = (unit / tiles_m) * MN;
+    }
     const int kblocks = (p.K + BK - 1) / BK;
     const int per = (kblocks + S - 1) / S;
     const int kb_begin = min(kblocks, (int)rank * per);
@@ -258,7 +274,7 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
             // full[] once the thread's own copies of it have landed and been
             // fenced for the tensor core. No registers hold operands, so the
             // ring depth, not the register file, sets the bytes in flight.
-            using SV = AsyncPlan<V, PT, MN>;
+            using SV = AsyncPlan<V, PT, AROWS, BCOLS>;
             constexpr int DEPTH = STAGES - 1;
             constexpr uint32_t VB = 2 * V;
             const int tid = threadIdx.x;
@@ -275,12 +291,12 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
                     break;
                 }
                 const int k0 = (kb_begin + s) * BK;
-                const uint32_t sB = smem_u32(smem + stage * Cf::STAGE_BYTES);
-                const uint32_t sA = sB + BT_BYTES + da;
+                const uint32_t sB = smem_u32(smem + stage * Cf::STAGE_BYTES) + B_OFF;
+                const uint32_t sA = smem_u32(smem + stage * Cf::STAGE_BYTES) + A_OFF + da;
                 const uint16_t *pa = p.A + (size_t)(m0 + ar) * p.K + (k0 + ac);
                 const uint16_t *pb = p.B + (size_t)(k0 + br) * p.N + (n0 + bc);
                 const bool k_in = k0 + BK <= p.K;
-                if (k_in && n0 + BNT <= p.N) {
+                if (k_in && n0 + BCOLS <= p.N) {
 #pragma unroll
                     for (int j = 0; j < SV::B_PER; ++j)
                         cp_async_v<V>(sB + SV::b_off(j, db0, db1), pb + j * sb, VB);
@@ -293,7 +309,7 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
                                       in ? VB : 0u);
                     }
                 }
-                if (k_in && m0 + MN <= p.M) {
+                if (k_in && m0 + AROWS <= p.M) {
 #pragma unroll
                     for (int j = 0; j < SV::A_PER; ++j)
                         cp_async_v<V>(sA + j * SV::A_STEP * 128, pa + j * sa, VB);
@@ -328,8 +344,8 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
                 oldest = oldest + 1 == STAGES ? 0 : oldest + 1;
             }
         } else {
-            using Slice = Slice1<PT, MN>;
-            constexpr int R = ring_depth_2byte<MN>();
+            using Slice = Slice1<PT, AROWS, BCOLS>;
+            constexpr int R = ring_depth_2byte<Slice>();
             const int tid = threadIdx.x;
             uint32_t stage = 0, phase = 0;
             int next = 0, left = nslices;
@@ -347,7 +363,7 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
                     return false;
                 }
                 uint8_t *st = smem + stage * Cf::STAGE_BYTES;
-                cur.store(st + BT_BYTES, st, tid);
+                cur.store(st + A_OFF, st + B_OFF, tid);
                 fence_proxy_async_shared();
                 mbar_arrive(&full[stage]);
                 if (++stage == STAGES) {
@@ -384,15 +400,21 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sb = smem_u32(smem + stage * Cf::STAGE_BYTES);  // B^T, MN-major
-                const uint32_t sa = sb + BT_BYTES;                               // A^T, K-major
+                const uint32_t sbig = smem_u32(smem + stage * Cf::STAGE_BYTES);  // MMA's A
+                const uint32_t ssmall = sbig + BT_BYTES;                           // MMA's B
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                     // MN-major side: 64-wide atoms B_ATOM_BYTES apart, 16 k-rows per step.
                     // K-major side: rows of 128 B, 8-row groups 1024 B apart, 32 B per step.
-                    const uint64_t adesc = sdesc_sw128(sb + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
-                    const uint64_t bdesc = sdesc_sw128(sa + kk * UMMA_K * 2, 16, 1024);
-                    umma_f16(tmem_base, adesc, bdesc, idesc_t<F16, MN>(),
+                    uint64_t adesc, bdesc;
+                    if constexpr (SWAP) {
+                        adesc = sdesc_sw128(sbig + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
+                        bdesc = sdesc_sw128(ssmall + kk * UMMA_K * 2, 16, 1024);
+                    } else {
+                        adesc = sdesc_sw128(sbig + kk * UMMA_K * 2, 16, 1024);
+                        bdesc = sdesc_sw128(ssmall + kk * UMMA_K * 128, B_ATOM_BYTES, 1024);
+                    }
+                    umma_f16(tmem_base, adesc, bdesc, idesc_t<F16, MN, SWAP>(),
                              (kb != kb_begin || kk != 0) ? 1u : 0u);
                 }
                 issued_any = true;
@@ -412,7 +434,7 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
     } else {
         // ------------------------------------------------ epilogue (warps PW+1 .. PW+4)
         const int quarter = warp & 3;         // the TMEM lanes this warp may read
-        const int col = quarter * 32 + lane;  // TMEM lane: column n0 + col of C
+        const int col = quarter * 32 + lane;  // TMEM lane: column n0 + col (swap) or row m0 + col of C
         const bool have = nslices > 0;
         bool ok = true;
         if (have && !mbar_wait_bounded(done, 0, limit, abort)) {
@@ -423,19 +445,42 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
         const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16);
         if (S == 1) {
             if (ok && have) {
-                const int gn = n0 + col;
 #pragma unroll 1
                 for (int c = 0; c < MN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, r);
                     tmem_wait_ld();
-                    const int rows = min(32, p.M - (m0 + c * 32));
-                    if (gn < p.N) {
-                        float *cp = p.C + (size_t)(m0 + c * 32) * p.N + gn;
+                    if constexpr (SWAP) {
+                        // for each row of C the warp's 32 lanes store 32 consecutive floats
+                        const int gn = n0 + col;
+                        const int rows = min(32, p.M - (m0 + c * 32));
+                        if (gn < p.N) {
+                            float *cp = p.C + (size_t)(m0 + c * 32) * p.N + gn;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < rows)
-                                cp[(size_t)j * p.N] = __uint_as_float(r[j]);
+                            for (int j = 0; j < 32; ++j)
+                                if (j < rows)
+                                    cp[(size_t)j * p.N] = __uint_as_float(r[j]);
+                        }
+                    } else {
+                        // a thread stores 32 consecutive floats of its row of C
+                        const int gm = m0 + col;
+                        const int gn0 = n0 + c * 32;
+                        if (gm < p.M) {
+                            float *cp = p.C + (size_t)gm * p.N + gn0;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                if (p.c_vec && gn0 + 4 * v + 3 < p.N) {
+                                    *reinterpret_cast<float4 *>(cp + 4 * v) = make_float4(
+                                        __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if (gn0 + 4 * v + e < p.N)
+                                            cp[4 * v + e] = __uint_as_float(r[4 * v + e]);
+                                }
+                            }
+                        }
                     }
                 }
             }
@@ -463,13 +508,13 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
     if (S > 1) {
         cluster_sync();  // every partial tile of the cluster is in shared memory
         if (warp > kMmaWarp) {
+            // TMEM lane `col` of every CTA: sum its columns [r MN / S, (r + 1) MN / S)
             const int col = (warp & 3) * 32 + lane;
-            const int gn = n0 + col;
-            const int rows = MN / S;
-            const int r0 = (int)rank * rows;
+            const int cols = MN / S;
+            const int c0 = (int)rank * cols;
             const uint32_t mine = smem_u32(smem) + (uint32_t)(col * Cf::PITCH) * 4u;
-            for (int rr = 0; rr < rows; rr += 4) {
-                const uint32_t off = (uint32_t)(r0 + rr) * 4u;
+            for (int cc = 0; cc < cols; cc += 4) {
+                const uint32_t off = (uint32_t)(c0 + cc) * 4u;
                 float4 acc = ld_shared_cluster_v4(mapa_shared(mine + off, 0));
                 for (int q = 1; q < S; ++q) {
                     const float4 v = ld_shared_cluster_v4(mapa_shared(mine + off, (uint32_t)q));
@@ -478,13 +523,28 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
                     acc.z += v.z;
                     acc.w += v.w;
                 }
-                const int gm = m0 + r0 + rr;
-                if (gn < p.N) {
-                    float *cp = p.C + (size_t)gm * p.N + gn;
-                    if (gm + 0 < p.M) cp[0] = acc.x;
-                    if (gm + 1 < p.M) cp[(size_t)p.N] = acc.y;
-                    if (gm + 2 < p.M) cp[(size_t)2 * p.N] = acc.z;
-                    if (gm + 3 < p.M) cp[(size_t)3 * p.N] = acc.w;
+                if constexpr (SWAP) {
+                    const int gn = n0 + col, gm = m0 + c0 + cc;
+                    if (gn < p.N) {
+                        float *cp = p.C + (size_t)gm * p.N + gn;
+                        if (gm + 0 < p.M) cp[0] = acc.x;
+                        if (gm + 1 < p.M) cp[(size_t)p.N] = acc.y;
+                        if (gm + 2 < p.M) cp[(size_t)2 * p.N] = acc.z;
+                        if (gm + 3 < p.M) cp[(size_t)3 * p.N] = acc.w;
+                    }
+                } else {
+                    const int gm = m0 + col, gn = n0 + c0 + cc;
+                    if (gm < p.M) {
+                        float *cp = p.C + (size_t)gm * p.N + gn;
+                        if (p.c_vec && gn + 3 < p.N) {
+                            *reinterpret_cast<float4 *>(cp) = acc;
+                        } else {
+                            if (gn + 0 < p.N) cp[0] = acc.x;
+                            if (gn + 1 < p.N) cp[1] = acc.y;
+                            if (gn + 2 < p.N) cp[2] = acc.z;
+                            if (gn + 3 < p.N) cp[3] = acc.w;
+                        }
+                    }
                 }
             }
         }
@@ -499,11 +559,11 @@ __global__ void __launch_bounds__(threads_of(producer_warps(V)), 1)
     }
 }
 
-template <bool F16, int MN, int V>
+template <bool F16, int MN, int V, bool SWAP>
 static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
 {
     using Cf = Cfg<MN, kStages>;
-    auto kernel = gemm_tc_any_t_kernel<F16, MN, V>;
+    auto kernel = gemm_tc_any_t_kernel<F16, MN, V, SWAP>;
     constexpr int kThreadsT = threads_of(producer_warps(V));
     static std::atomic<uint64_t> done{0};  // per instantiation
     // The smallest carve-out that holds the ring (of the SM's 228 KB): the
@@ -513,7 +573,8 @@ static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
         (int)((Cf::SMEM_BYTES * 100 + 228 * 1024 - 1) / (228 * 1024)));
     if (e != cudaSuccess)
         return e;
-    const long long tiles = (long long)((L.N + BNT - 1) / BNT) * ((L.M + MN - 1) / MN);
+    const long long tiles = SWAP ? (long long)((L.N + BNT - 1) / BNT) * ((L.M + MN - 1) / MN)
+                                 : (long long)((L.M + BNT - 1) / BNT) * ((L.N + MN - 1) / MN);
     // Every tile's cluster resident at once: halve the split while more
     // clusters would be launched than fit.
     static std::atomic<int> resident[4][64] = {};  // clusters of 1, 2, 4, 8
@@ -536,39 +597,43 @@ static cudaError_t launch_mn(const TcLaunch &L, int splits, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const int c_vec = (L.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0);
     Params p{L.M, L.N, L.K, L.A, L.B, L.C, L.err, (unsigned long long)L.wait_limit_ns, splits,
-             L.mute_producer};
+             L.mute_producer, c_vec};
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <bool F16, int MN>
+template <bool F16, int MN, bool SWAP>
 static cudaError_t launch_v(const TcLaunch &L, int v, int splits, cudaStream_t stream)
 {
-    return v == 4 ? launch_mn<F16, MN, 4>(L, splits, stream)
-           : v == 2 ? launch_mn<F16, MN, 2>(L, splits, stream)
-                    : launch_mn<F16, MN, 1>(L, splits, stream);
+    return v == 4 ? launch_mn<F16, MN, 4, SWAP>(L, splits, stream)
+           : v == 2 ? launch_mn<F16, MN, 2, SWAP>(L, splits, stream)
+                    : launch_mn<F16, MN, 1, SWAP>(L, splits, stream);
 }
 
 template <bool F16>
-static cudaError_t launch_f(const TcLaunch &L, int v, int splits, cudaStream_t stream)
+static cudaError_t launch_f(const TcLaunch &L, int v, int splits, bool swap, cudaStream_t stream)
 {
+    if (!swap)
+        return tcs_cols(L.N) == 64 ? launch_v<F16, 64, false>(L, v, splits, stream)
+                                   : launch_v<F16, 128, false>(L, v, splits, stream);
     const int mn = tct_rows(L.M);
-    return mn == 32 ? launch_v<F16, 32>(L, v, splits, stream)
-           : mn == 64 ? launch_v<F16, 64>(L, v, splits, stream)
-                      : launch_v<F16, 128>(L, v, splits, stream);
+    return mn == 32 ? launch_v<F16, 32, true>(L, v, splits, stream)
+           : mn == 64 ? launch_v<F16, 64, true>(L, v, splits, stream)
+                      : launch_v<F16, 128, true>(L, v, splits, stream);
 }
 
 } // namespace tshort
 } // namespace tcany
 
-cudaError_t launch_gemm_tc_any_t(const TcLaunch &L, int splits, cudaStream_t stream)
+cudaError_t launch_gemm_tc_any_t(const TcLaunch &L, int splits, bool swap, cudaStream_t stream)
 {
     using namespace tcany;
-    if (L.M > 128 || (splits != 1 && splits != 2 && splits != 4 && splits != 8))
+    if ((swap ? L.M : L.N) > 128 || (splits != 1 && splits != 2 && splits != 4 && splits != 8))
         return cudaErrorInvalidValue;
     const int v = access_width(L);
-    return L.f16 ? tshort::launch_f<true>(L, v, splits, stream)
-                 : tshort::launch_f<false>(L, v, splits, stream);
+    return L.f16 ? tshort::launch_f<true>(L, v, splits, swap, stream)
+                 : tshort::launch_f<false>(L, v, splits, swap, stream);
 }
 
 } // namespace rtm

@@ -306,12 +306,13 @@ int long_k_splits(long long tiles, long long K, int sms);
 // operands loaded by producer warps instead of TMA (mute_producer: they load
 // nothing, so every wait gives up); any 4-byte-aligned C.
 cudaError_t launch_gemm_tc_any_pair(const TcLaunch &p, cudaStream_t stream);
-// Short products (M <= 128) with producer warps, computed as the transpose
-// like launch_gemm_tc_t with swap (gemm_tc_any_t.cu): CTAs own 128 columns and
-// tct_rows(M) rows, `splits` (1, 2, 4 or 8) CTAs of a cluster split K; with
-// splits = 1 the column tiles may outnumber the SMs (several waves). Same
-// operand rules as launch_gemm_tc_any_pair.
-cudaError_t launch_gemm_tc_any_t(const TcLaunch &p, int splits, cudaStream_t stream);
+// launch_gemm_tc_t's two tilings with producer warps instead of TMA
+// (gemm_tc_any_t.cu): with swap, short products (M <= 128), CTAs own 128
+// columns and tct_rows(M) rows; without, tall, narrow products (N <= 128),
+// CTAs own 128 rows and tcs_cols(N) columns. `splits` (1, 2, 4 or 8) CTAs of a
+// cluster split K; with splits = 1 the tiles may outnumber the SMs (several
+// waves). Same operand rules as launch_gemm_tc_any_pair.
+cudaError_t launch_gemm_tc_any_t(const TcLaunch &p, int splits, bool swap, cudaStream_t stream);
 
 // The host-side argument checks of the fp32 entry points (api.cu), made
 // before any CUDA call: GEMM_OK with *nothing_to_do set when M or N is zero,

@@ -1,6 +1,7 @@
 """GPU tests of the transposed load-and-swizzle kernel: gemm_bf16f32 and
 gemm_f16f32 with M <= 128 whose A or B rows do not start on 16-byte
-boundaries (tcany::tshort::gemm_tc_any_t_kernel).
+boundaries (tcany::tshort::gemm_tc_any_t_kernel), and the same kernel without
+the swap for tall, narrow products (M > 128, N <= 128, long K).
 
 The kernel computes C^T = B^T.A^T: a CTA owns 128 columns of C and 32, 64 or
 128 rows, K is split over S CTAs of a cluster (the same S as the TMA-fed
@@ -173,9 +174,57 @@ def test_more_column_tiles_than_sms_long_k_sampled():
     assert_close_to_oracle(C, A, B, "bf16", full=False, seed=57)
 
 
+# Tall, narrow products (M > 128, N <= 128) with long K: the same kernel
+# without the swap (A on the MMA's 128-row side, B on its N side), the same
+# K-split as the TMA-fed kernel without the swap.
+TALL = [(8192, 62, 4094),    # V 2, 64 columns, S 2
+        (4097, 100, 8190),   # V 2, 128 columns, S 4, ragged M
+        (1000, 120, 8196),   # V 4 (A rows on 8-byte boundaries), S 8
+        (300, 33, 2049)]     # V 1, 64 columns, S 2
+
+
+@pytest.mark.parametrize("M,N,K", TALL)
+def test_tall_narrow_matches_oracle(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "normal", "bf16", seed=M + 11 * N + K)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    buf, C = guarded_output(M, N, DEV)
+    ran(lambda: rtm.gemm_bf16f32(Ad, Bd, out=C), ANY_T)
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert guard_intact(buf, M, N)
+    assert_close_to_oracle(C, A, B, "bf16", full=M * N * K <= (1 << 31), seed=M + N)
+
+
+@pytest.mark.parametrize("M,N,K", TALL)
+def test_tall_narrow_bits_equal_tma_kernel_on_padded_copies(M, N, K):
+    A, B = workloads.make_inputs(M, N, K, "uniform", "bf16", seed=5 * M + N + K)
+    K8, N8 = (K + 7) // 8 * 8, (N + 7) // 8 * 8
+    Ap = torch.zeros(M, K8, dtype=torch.bfloat16)
+    Bp = torch.zeros(K8, N8, dtype=torch.bfloat16)
+    Ap[:, :K] = A
+    Bp[:K, :N] = B
+    Ad, Bd, Apd, Bpd = A.to(DEV), B.to(DEV), Ap.to(DEV), Bp.to(DEV)
+    C = rtm.gemm_bf16f32(Ad, Bd)
+    holder = {}
+    ran(lambda: holder.setdefault("Cp", rtm.gemm_bf16f32(Apd, Bpd)), TCT)
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert torch.equal(C, holder["Cp"][:, :N])
+
+
+def test_tall_narrow_small_integers_bit_exact():
+    M, N, K = 1000, 100, 4100
+    A, B = workloads.make_inputs(M, N, K, "int", "f32", seed=58)
+    C = rtm.gemm_bf16f32(A.to(torch.bfloat16).to(DEV), B.to(torch.bfloat16).to(DEV))
+    torch.cuda.synchronize()
+    assert rtm.get_device_error() == 0
+    assert_bit_exact(C, (A.to(torch.int64) @ B.to(torch.int64)).numpy())
+
+
 @pytest.mark.parametrize("M,N,K", [(100, 258, 130), (64, 1030, 4098), (1, 1001, 3001),
-                                   (100, 24002, 130)],
-                         ids=["split1_4byte", "split4_4byte", "split2_2byte", "waves_4byte"])
+                                   (100, 24002, 130), (4097, 100, 8190)],
+                         ids=["split1_4byte", "split4_4byte", "split2_2byte", "waves_4byte",
+                              "tall_split4_4byte"])
 def test_muted_producers_every_wait_gives_up(M, N, K):
     """The producer warps load nothing: the MMA issuer's and the epilogue's
     bounded waits run out after 50 ms, every thread still reaches the cluster
