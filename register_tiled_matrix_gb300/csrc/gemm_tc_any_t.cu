@@ -1,6 +1,7 @@
 // bf16 x bf16 (or fp16 x fp16) -> fp32 product C = A.B for short products
 // (M <= 128) whose A or B rows do not start on 16-byte boundaries, computed as
-// its transpose C^T = B^T.A^T with K split over a cluster.
+// its transpose C^T = B^T.A^T with K split over a cluster; and, without the
+// swap, for tall, narrow products on such rows.
 //
 // The tiling is the transposed kernel's of gemm_tc_t.cu ("寄存器Tiling跨架构
 // 解析", section 6: the accumulator tile is whatever the matrix instruction
@@ -11,7 +12,10 @@
 // stages 64 k-rows x 128 columns of B (two 64-column atoms, MN-major: the
 // MMA's A operand) and MN rows x 64 k of A (K-major: the MMA's B operand).
 // Nearly every staged byte is B, and B is read once, so the product is bound
-// by how fast B reaches shared memory.
+// by how fast B reaches shared memory. Without the swap (SWAP = false) the
+// same kernel serves tall, narrow products (M > 128, N <= 128, long K): A
+// (128 rows x 64 k, K-major) fills the MMA's 128-row side and B (64 k-rows x
+// MN = 64 or 128 columns, MN-major) its N side, as in gemm_tc_t.cu.
 //
 // The TMA producer thread is replaced by producer warps that copy the slice
 // with 2-, 4- or 8-byte accesses (the widest V for which every row of A and B
@@ -27,15 +31,18 @@
 // because the copies in flight pass through L1, which gets what the
 // shared-memory carve-out leaves.
 //
-// Columns of C are TMEM lanes, rows of C TMEM columns: with S = 1 four
-// epilogue warps store the accumulator directly (for each row of C the 32
-// lanes of a warp write 32 consecutive floats); with S > 1 each CTA writes
-// its partial tile into its idle stage memory, CTA r of the cluster sums rows
-// [r MN / S, (r + 1) MN / S) of the partials over the cluster in rank order
-// 0, 1, .., S-1 and stores them, and a second cluster barrier keeps every
-// partial alive until all have been read. The MMA sequence, the K-ranges and
-// the order of the sums are those of the TMA-fed transposed kernel, so both
-// give the same bits on the same values. C rows need only 4-byte alignment.
+// With the swap, columns of C are TMEM lanes and rows of C TMEM columns
+// (without it, the reverse): with S = 1 four epilogue warps store the
+// accumulator directly (with the swap, for each row of C the 32 lanes of a
+// warp write 32 consecutive floats; without it, a thread writes 32
+// consecutive floats of its row, as float4 where C rows are 16-byte
+// aligned); with S > 1 each CTA writes its partial tile into its idle stage
+// memory, CTA r of the cluster sums TMEM columns [r MN / S, (r + 1) MN / S)
+// of the partials over the cluster in rank order 0, 1, .., S-1 and stores
+// them, and a second cluster barrier keeps every partial alive until all
+// have been read. The MMA sequence, the K-ranges and the order of the sums
+// are those of the TMA-fed kernel of gemm_tc_t.cu, so both give the same bits
+// on the same values. C rows need only 4-byte alignment.
 //
 // Every mbarrier wait is bounded in time; a warp that gives up records
 // GEMM_ERR_TIMEOUT in the device error word and every thread still reaches
