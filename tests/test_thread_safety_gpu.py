@@ -25,12 +25,15 @@ CHILD = textwrap.dedent(r"""
 
     torch.cuda.init()
     jobs = []
-    for i in range(9):
+    for i in range(12):
         kind = ["f32", "f32_ws", "bf16", "bf16_small", "f16", "bf16_ws", "bf16_any", "f32",
-                "f32"][i]
+                "f32", "bf16_any", "bf16_any", "f32_ws"][i]
         M, N, K = [(300, 260, 129), (256, 64, 2048), (384, 264, 200), (96, 1024, 136),
                    (300, 264, 72), (300, 129, 77), (120, 100, 33), (1000, 1000, 999),
-                   (2000, 60, 2000)][i]
+                   (2000, 60, 2000),
+                   (64, 1030, 4098),    # transposed load-and-swizzle, K split over 4
+                   (1000, 120, 2052),   # the same without the swap (tall, narrow)
+                   (640, 518, 2047)][i]  # fp32 operands re-pitched into the workspace
         dt = {"f32": "f32", "f32_ws": "f32", "f16": "f16"}.get(kind, "bf16")
         A, B = workloads.make_inputs(M, N, K, "normal", dt, seed=i + 11)
         jobs.append((kind, A, B))
@@ -76,7 +79,7 @@ CHILD = textwrap.dedent(r"""
 """)
 
 
-def test_first_calls_from_eight_threads():
+def test_first_calls_from_many_threads():
     import register_tiled_matrix_gb300 as rtm
     rtm.build()  # build in this process; the child only loads the library
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT], capture_output=True, text=True,
