@@ -801,9 +801,15 @@ def run_configs(args) -> Optional[Dict]:
             entries.append(("gemm_bf16f32", lambda: rtm.gemm_bf16f32(A, B, out=C),
                             float(peaks["bf16_tflops"])))
             # Rows off 16-byte boundaries: with M > 128 the workspace entry
-            # re-pitches them for the TMA-fed CTA pairs; with M <= 128 it runs
-            # the same kernel as gemm_bf16f32 and is not timed again.
-            if (w.K % 8 or w.N % 8) and w.M > 128:
+            # re-pitches them for the TMA-fed CTA pairs; with M <= 128, and for
+            # tall, narrow products with long K (N <= 128, at least 32 64-deep
+            # K-blocks, the 128-row tiles fitting on the SMs), it runs the same
+            # kernel as gemm_bf16f32 and is not timed again.
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            cols = 64 if w.N <= 64 else 128
+            tall_narrow = (w.N <= 128 and (w.K + 63) // 64 >= 32 and
+                           (w.M + 127) // 128 * ((w.N + cols - 1) // cols) <= sms)
+            if (w.K % 8 or w.N % 8) and w.M > 128 and not tall_narrow:
                 wsb = torch.empty(rtm.gemm_bf16f32_workspace_bytes(w.M, w.N, w.K),
                                   dtype=torch.uint8, device="cuda")
                 entries.append(("gemm_bf16f32_ws (rows re-pitched, CTA pairs)",
